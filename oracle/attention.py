@@ -1,0 +1,136 @@
+"""Oracle fp64 tree attention, forward and backward (test infrastructure).
+
+Semantics from the AReaL "树训练" page: §树构建过程's diagram gives the mask
+(causal, with tree structure: a token attends only to its ancestors and
+itself); §注意力机制 computes masked softmax attention over the packed tree.
+The pages leave the scale and head grouping open; the readings here are the
+usual ones: scores ``q.k * scale`` with ``scale = 1/sqrt(d)`` unless given,
+and grouped-query attention where query head h reads key/value head
+``h // (Hq // Hkv)``.
+
+For query position i with ancestor-or-self set A(i):
+
+    S_ij = scale * q_i . k_j,           j in A(i)
+    LSE_i = log sum_{j in A(i)} exp(S_ij)
+    O_i   = sum_{j in A(i)} exp(S_ij - LSE_i) v_j
+
+and for an upstream gradient dO the exact gradient of <dO, O>:
+
+    P_ij = exp(S_ij - LSE_i),   D_i = dO_i . O_i
+    dV_j += P_ij dO_i,          dS_ij = P_ij (dO_i . v_j - D_i)
+    dQ_i = scale sum_j dS_ij k_j,   dK_j += scale dS_ij q_i
+
+(dK, dV summed over the query heads that share a key/value head). Padding
+rows give O = 0, LSE = 0 and zero gradients.
+
+Computation is organised node by node: the queries of one compressed node
+share their root path, so A(i) is a prefix of that path (all ancestor nodes'
+tokens, then the node's own tokens up to i). Everything is fp64 on the exact
+(bf16-representable) input values.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from .pack import OracleTree
+
+_CHUNK = 256   # query rows per block of work (memory bound only; no reordering of sums)
+
+
+def _root_path(tree: OracleTree, nid: int) -> np.ndarray:
+    """Flat positions from the root down to the end of node ``nid``."""
+    chain = []
+    while nid >= 0:
+        chain.append(nid)
+        nid = int(tree.node_parent[nid])
+    parts = [np.arange(tree.node_start[c], tree.node_end[c] + 1) for c in reversed(chain)]
+    return np.concatenate(parts)
+
+
+def _as64(x: torch.Tensor) -> torch.Tensor:
+    return x.detach().to("cpu").to(torch.float64)
+
+
+def attn_forward(tree: OracleTree, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                 scale: float | None = None, t_pad: int | None = None,
+                 nodes: list[int] | None = None):
+    """fp64 forward for one tree.
+
+    q ``[T, Hq, d]``, k/v ``[T, Hkv, d]`` (any float dtype; widened to fp64).
+    Returns O ``[T, Hq, d]`` and LSE ``[Hq, T]`` fp64 (pad rows 0). ``nodes``
+    restricts the work to those compressed nodes (rows elsewhere stay 0)."""
+    T = q.shape[0] if t_pad is None else t_pad
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    q64, k64, v64 = _as64(q), _as64(k), _as64(v)
+    O = torch.zeros((T, Hq, d), dtype=torch.float64)
+    LSE = torch.zeros((Hq, T), dtype=torch.float64)
+    node_list = range(len(tree.node_start)) if nodes is None else nodes
+    for nid in node_list:
+        path = torch.from_numpy(_root_path(tree, nid))
+        s0, s1 = int(tree.node_start[nid]), int(tree.node_end[nid])
+        base = path.numel() - (s1 - s0 + 1)
+        kp = k64[path].repeat_interleave(G, dim=1)        # [P, Hq, d]
+        vp = v64[path].repeat_interleave(G, dim=1)
+        for c0 in range(s0, s1 + 1, _CHUNK):
+            c1 = min(s1 + 1, c0 + _CHUNK)
+            qi = q64[c0:c1]                                # [m, Hq, d]
+            S = torch.einsum("mhd,phd->hmp", qi, kp) * scale
+            rows = torch.arange(c0 - s0, c1 - s0) + base   # path index of each query
+            allowed = torch.arange(path.numel())[None, :] <= rows[:, None]
+            S = S.masked_fill(~allowed[None], float("-inf"))
+            lse = torch.logsumexp(S, dim=-1)               # [Hq, m]
+            P = torch.exp(S - lse[..., None])
+            O[c0:c1] = torch.einsum("hmp,phd->mhd", P, vp)
+            LSE[:, c0:c1] = lse
+    return O, LSE
+
+
+def attn_backward(tree: OracleTree, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  dO: torch.Tensor, scale: float | None = None, t_pad: int | None = None,
+                  nodes: list[int] | None = None):
+    """fp64 gradients (dQ, dK, dV) of ``<dO, O>`` for one tree.
+
+    Uses the fp64 forward's own O and LSE. ``nodes`` restricts the QUERY
+    nodes whose contributions are accumulated (dK/dV then hold only those
+    contributions; dQ rows of other nodes stay 0)."""
+    T = q.shape[0] if t_pad is None else t_pad
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    q64, k64, v64, do64 = _as64(q), _as64(k), _as64(v), _as64(dO)
+    dQ = torch.zeros((T, Hq, d), dtype=torch.float64)
+    dKh = torch.zeros((T, Hq, d), dtype=torch.float64)   # per query head, summed per group below
+    dVh = torch.zeros((T, Hq, d), dtype=torch.float64)
+    node_list = range(len(tree.node_start)) if nodes is None else nodes
+    for nid in node_list:
+        path = torch.from_numpy(_root_path(tree, nid))
+        s0, s1 = int(tree.node_start[nid]), int(tree.node_end[nid])
+        base = path.numel() - (s1 - s0 + 1)
+        kp = k64[path].repeat_interleave(G, dim=1)
+        vp = v64[path].repeat_interleave(G, dim=1)
+        for c0 in range(s0, s1 + 1, _CHUNK):
+            c1 = min(s1 + 1, c0 + _CHUNK)
+            qi, doi = q64[c0:c1], do64[c0:c1]
+            S = torch.einsum("mhd,phd->hmp", qi, kp) * scale
+            rows = torch.arange(c0 - s0, c1 - s0) + base
+            allowed = torch.arange(path.numel())[None, :] <= rows[:, None]
+            S = S.masked_fill(~allowed[None], float("-inf"))
+            lse = torch.logsumexp(S, dim=-1)
+            P = torch.exp(S - lse[..., None])              # [Hq, m, P]
+            Oi = torch.einsum("hmp,phd->mhd", P, vp)
+            Di = (doi * Oi).sum(-1).transpose(0, 1)         # [Hq, m]
+            dP = torch.einsum("mhd,phd->hmp", doi, vp)
+            dS = P * (dP - Di[..., None])
+            dQ[c0:c1] = scale * torch.einsum("hmp,phd->mhd", dS, kp)
+            dKh.index_add_(0, path, scale * torch.einsum("hmp,mhd->phd", dS, qi))
+            dVh.index_add_(0, path, torch.einsum("hmp,mhd->phd", P, doi))
+    dK = dKh.view(T, Hkv, G, d).sum(2)
+    dV = dVh.view(T, Hkv, G, d).sum(2)
+    return dQ, dK, dV
