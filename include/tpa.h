@@ -1,0 +1,280 @@
+/*
+ * tpa.h — C ABI of libtpa, prefix-shared tree attention on GB300 (sm_103a).
+ *
+ * The method is "tree training" as described on the AReaL documentation page
+ * "树训练" (tree training): sequences that share a prefix are packed into one
+ * prefix trie so that every shared token is computed once; attention inside a
+ * packed tree is causal with tree structure (a token attends only to its
+ * ancestors and itself); log-probabilities are gathered back per original
+ * sequence from the packed rows.
+ *
+ * Conventions for every call:
+ *  - Every function returns an int status (TPA_OK = 0, negative = error) and
+ *    never aborts or throws.  tpa_status_string() names a status.
+ *  - The library owns only the host memory of a tpa_tree (freed by
+ *    tpa_tree_free).  All device memory is allocated by the caller and passed
+ *    as plain device pointers; the library allocates no device memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Device work is enqueued asynchronously on it; a launch failure
+ *    is reported as TPA_ERR_CUDA by the call that launched it.  Kernel-side
+ *    failures (a bounded wait that ran out) are recorded in a device status
+ *    word and reported by tpa_sync_status().
+ *  - Tensors are dense, row-major, with the layouts stated per call.
+ *    bf16 means IEEE bfloat16 stored as uint16.
+ */
+#ifndef TPA_H_
+#define TPA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* BLOCK_SIZE of the tree-training page (§注意力机制, FlexAttention block mask):
+ * max_tokens_per_mb must be a multiple of it (§配置, note under the table). */
+#define TPA_BLOCK_SIZE 128
+
+enum tpa_status_code {
+  TPA_OK = 0,
+  TPA_ERR_INVALID_ARG = -1,        /* null pointer, bad size, bad alignment, unsupported shape */
+  TPA_ERR_EMPTY_SEQUENCE = -2,     /* a sequence of length 0 */
+  TPA_ERR_SEQ_TOO_LONG = -3,       /* a sequence longer than max_tokens_per_mb */
+  TPA_ERR_NO_MEMORY = -4,          /* host allocation failed */
+  TPA_ERR_CUDA = -5,               /* a CUDA runtime call or kernel launch failed */
+  TPA_ERR_DEVICE_TIMEOUT = -6,     /* a kernel's bounded wait ran out (kernel returned early) */
+  TPA_ERR_UNSUPPORTED_DEVICE = -7, /* current device is not compute capability 10.3 */
+  TPA_ERR_BUFFER_TOO_SMALL = -8    /* a caller buffer is smaller than required */
+};
+
+/* ------------------------------------------------------------------------ */
+/* Packing: tree training page, §树构建过程 steps 2-3 and §数据结构 TrieNode.  */
+/* ------------------------------------------------------------------------ */
+
+typedef struct tpa_tree tpa_tree; /* opaque; host memory owned by the library */
+
+typedef struct {
+  int32_t n_trees;            /* B: one tree per micro-batch */
+  int32_t t_pad;              /* T_pad = max_tokens_per_mb (every tree padded to it) */
+  int32_t n_seqs;             /* number of input sequences */
+  int32_t max_nodes;          /* largest compressed-node count of any tree */
+  int64_t total_seq_tokens;   /* sum of input lengths */
+  int64_t total_tree_tokens;  /* sum over trees of real (non-pad) positions */
+  int64_t total_nodes;        /* sum over trees of compressed nodes */
+  int64_t ancestor_pairs;     /* sum over real positions of (depth + 1) */
+  double tree_token_ratio;    /* total_tree_tokens / total_seq_tokens (§指标和监控) */
+  uint64_t blob_bytes;        /* size of the metadata blob (host and device copies) */
+} tpa_tree_info;
+
+/*
+ * Per-tree flattened layout, as plain arrays inside one metadata blob.
+ * The blob is built on the host by tpa_tree_pack; tpa_tree_upload copies it
+ * verbatim into a caller device buffer; tpa_tree_make_view fills this struct
+ * with pointers into either copy.  Position p of tree b lives at index
+ * b * t_pad + p.  Positions are in preorder (§数据结构: nodes listed in
+ * preorder; node tokens at inclusive [start_idx, end_idx]); positions
+ * p >= n_tokens[b] are padding.
+ */
+typedef struct {
+  int32_t n_trees, t_pad, n_seqs, max_nodes;
+  int64_t total_seq_tokens;
+  int64_t total_tree_tokens;
+  const int32_t* tokens;      /* [B*T_pad] token id; pad -1 */
+  const int32_t* subtree_end; /* [B*T_pad] E[p]: last position of the subtree of p's node;
+                                 key p is visible to query i iff p <= i <= E[p]; pad -1 */
+  const int32_t* parent;      /* [B*T_pad] position of the parent token; -1 under the root and at pad */
+  const int32_t* depth;       /* [B*T_pad] number of ancestors = position id; pad 0 */
+  const int32_t* node_id;     /* [B*T_pad] compressed node of p (tree-local, preorder); pad -1 */
+  const int32_t* child_off;   /* [B*(T_pad+1)] CSR: children of p are child_pos[b*T_pad + child_off[b*(T_pad+1)+p] ..
+                                 child_off[b*(T_pad+1)+p+1]) in ascending position order */
+  const int32_t* child_pos;   /* [B*T_pad] child positions (tree-local); unused tail -1 */
+  const int32_t* n_tokens;    /* [B] real positions per tree */
+  const int64_t* tok_base;    /* [B+1] exclusive prefix sum of n_tokens (compact row numbering) */
+  const int32_t* node_info;   /* [B*max_nodes*4] per node: start, end (inclusive), parent node (-1 under
+                                 the root), subtree end; unused tail -1 */
+  const int32_t* n_nodes;     /* [B] */
+  const int32_t* seq_tree;    /* [n_seqs] tree holding each input sequence */
+  const int64_t* seq_off;     /* [n_seqs+1] offsets of each sequence (same as the input offsets) */
+  const int32_t* seq_pos;     /* [total_seq_tokens] tree position of every input token */
+} tpa_tree_view;
+
+/*
+ * tpa_tree_pack — build the packed trees (tree training page, §树构建过程:
+ * step 2 greedy first-fit-decreasing insertion into a trie, step 3 merging
+ * linear chains into compressed nodes; §配置: each tree holds at most
+ * max_tokens_per_mb tokens, a multiple of 128).
+ *   tokens        [seq_offsets[n_seqs]] int32 token ids (>= 0), host memory
+ *   seq_offsets   [n_seqs+1] int64, seq_offsets[0] = 0, non-decreasing, host
+ *   n_seqs        >= 1
+ *   max_tokens_per_mb  > 0 and a multiple of TPA_BLOCK_SIZE
+ *   out           receives a new tree handle (set to NULL on error)
+ * Rules: sequences are taken longest first (equal lengths in input order);
+ * each goes into the first existing tree (creation order) whose token count
+ * plus the sequence's unshared tokens fits, else into a new tree; a node
+ * starts at a trie vertex whose parent is the root or branches, and extends
+ * while the vertex has exactly one child; children are laid out in insertion
+ * order.  Errors: TPA_ERR_INVALID_ARG, TPA_ERR_EMPTY_SEQUENCE,
+ * TPA_ERR_SEQ_TOO_LONG, TPA_ERR_NO_MEMORY.  Host only; thread-safe.
+ */
+int tpa_tree_pack(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
+                  int32_t max_tokens_per_mb, tpa_tree** out);
+
+/* Sizes and counts of a packed tree set.  Errors: TPA_ERR_INVALID_ARG. */
+int tpa_tree_get_info(const tpa_tree* tree, tpa_tree_info* info);
+
+/* Host copy of the metadata blob (info.blob_bytes bytes, 256-byte aligned,
+ * valid until tpa_tree_free).  NULL on a NULL tree. */
+const void* tpa_tree_host_blob(const tpa_tree* tree);
+
+/* Fill `view` with pointers into a blob copy starting at `base` (the host
+ * blob or a device buffer written by tpa_tree_upload).  Pure pointer
+ * arithmetic.  Errors: TPA_ERR_INVALID_ARG. */
+int tpa_tree_make_view(const tpa_tree* tree, const void* base, tpa_tree_view* view);
+
+/* Copy the host blob into `dev_blob` (a caller device buffer of at least
+ * info.blob_bytes bytes, 256-byte aligned) on `stream` (cudaMemcpyAsync,
+ * host-to-device).  The tree must stay alive until the copy has run.
+ * Errors: TPA_ERR_INVALID_ARG, TPA_ERR_BUFFER_TOO_SMALL, TPA_ERR_CUDA. */
+int tpa_tree_upload(const tpa_tree* tree, void* dev_blob, uint64_t dev_bytes, void* stream);
+
+/* Release a tree handle (NULL is ignored). */
+void tpa_tree_free(tpa_tree* tree);
+
+/* ------------------------------------------------------------------------ */
+/* Block classification: tree training page, §树构建过程 step 4 (mask
+ * generation) and §注意力机制 (block mask, BLOCK_SIZE 128, empty blocks are
+ * skipped).  A 128x128 tile (query block qb, key block kb) is EMPTY when no
+ * query in it sees any key in it, FULL when every query sees every key, and
+ * PARTIAL otherwise.                                                        */
+/* ------------------------------------------------------------------------ */
+
+enum { TPA_BLOCK_EMPTY = 0, TPA_BLOCK_PARTIAL = 1, TPA_BLOCK_FULL = 2 };
+
+typedef struct {
+  int32_t n_trees, n_blk;     /* n_blk = T_pad / 128 */
+  int32_t cap;                /* entries reserved per tree per CSR = n_blk*(n_blk+1)/2 */
+  int32_t pad_;
+  uint8_t* cls;               /* [B][n_blk][n_blk] class of (qb, kb) */
+  int32_t* q_ptr;             /* [B][n_blk+1] CSR by query block (tree-local offsets) */
+  int32_t* q_idx;             /* [B][cap] entries 2*kb + (FULL ? 1 : 0), ascending kb */
+  int32_t* k_ptr;             /* [B][n_blk+1] CSR by key block */
+  int32_t* k_idx;             /* [B][cap] entries 2*qb + (FULL ? 1 : 0), ascending qb */
+} tpa_blockmask_view;
+
+/* Bytes of one device buffer holding a block mask for (n_trees, t_pad). */
+uint64_t tpa_blockmask_bytes(int32_t n_trees, int32_t t_pad);
+
+/* Slice a caller buffer of tpa_blockmask_bytes() bytes (256-byte aligned)
+ * into a view.  Errors: TPA_ERR_INVALID_ARG. */
+int tpa_blockmask_make_view(void* base, int32_t n_trees, int32_t t_pad, tpa_blockmask_view* view);
+
+/* Classify every tile of every tree from the device subtree_end array and
+ * build both CSR lists (two kernels on `stream`).  `tree` must be a view of
+ * the DEVICE blob; `mask` a view of a device buffer.  Integer only; results
+ * are deterministic.  Errors: TPA_ERR_INVALID_ARG, TPA_ERR_CUDA. */
+int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask_view* mask, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Tree attention (tree training page, §树构建过程 mask caption and
+ * §注意力机制): for query position i of tree b and query head h,
+ *   O_i = sum_{j: j <= i <= E[j]} softmax_j(scale * q_i . k_j) v_j
+ * with key/value head h / (Hq / Hkv) (grouped-query attention) and
+ * LSE_i = log sum_j exp(scale * q_i . k_j) (natural log).  Pad rows give
+ * O = 0 and LSE = 0.  Computed in fp32 from bf16 inputs with an online
+ * softmax on tcgen05 tensor cores; empty tiles are skipped and the ancestor
+ * test runs only on partial tiles.                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tpa_tree_attn_fwd
+ *   q [B, T_pad, Hq, d] bf16;  k, v [B, T_pad, Hkv, d] bf16 (device, 16-byte aligned;
+ *     pad rows are read and must hold finite values)
+ *   o [B, T_pad, Hq, d] bf16 (written);  lse [B, Hq, T_pad] fp32 (written)
+ *   head_dim d in {64, 128};  Hq % Hkv == 0;  softmax_scale <= 0 selects 1/sqrt(d)
+ * `tree` and `mask` are views of device buffers (mask filled by
+ * tpa_block_classify for the same tree).  Errors: TPA_ERR_INVALID_ARG,
+ * TPA_ERR_UNSUPPORTED_DEVICE, TPA_ERR_CUDA.
+ */
+int tpa_tree_attn_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
+                      const void* q, const void* k, const void* v, void* o, float* lse,
+                      int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
+                      float softmax_scale, void* stream);
+
+/* Workspace bytes needed by tpa_tree_attn_bwd: an fp32 dQ accumulator
+ * [B, T_pad, Hq, d] and fp32 D = rowsum(dO * O) [B, Hq, T_pad]. */
+uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32_t n_heads_q,
+                                           int32_t head_dim);
+
+/*
+ * tpa_tree_attn_bwd — gradients of <dO, O> for the forward above:
+ *   P_ij = exp(scale q_i.k_j - LSE_i), D_i = dO_i . O_i,
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ * dK/dV summed over the query heads of each key/value head.
+ *   q, k, v, o, lse: as produced for / by tpa_tree_attn_fwd (o, lse read)
+ *   dout [B, T_pad, Hq, d] bf16 (pad rows read, must be finite)
+ *   dq [B, T_pad, Hq, d], dk, dv [B, T_pad, Hkv, d] bf16 (written; pad rows 0)
+ *   workspace: device buffer of tpa_tree_attn_bwd_workspace_bytes() bytes,
+ *     256-byte aligned, contents overwritten
+ * Errors: as tpa_tree_attn_fwd, plus TPA_ERR_BUFFER_TOO_SMALL.
+ */
+int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
+                      const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                      void* workspace, uint64_t workspace_bytes,
+                      int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
+                      float softmax_scale, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Log-probabilities and entropy (tree training page, §对数概率计算): labels
+ * cannot come from rolling input_ids; each tree row is processed once (the
+ * node-level cache) and the within-node and node-to-child transition labels
+ * of that row are gathered in the same pass; results are then regathered
+ * per original sequence.                                                   */
+/* ------------------------------------------------------------------------ */
+
+enum { TPA_LOGITS_COMPACT = 0, TPA_LOGITS_PADDED = 1 };
+
+/*
+ * tpa_tree_logprobs_entropy
+ *   logits   bf16 rows of width `vocab`, device; row of (tree b, position p) is
+ *            tok_base[b] + p (TPA_LOGITS_COMPACT) or b * T_pad + p
+ *            (TPA_LOGITS_PADDED); consecutive rows `row_stride` elements apart
+ *            (row_stride >= vocab, multiple of 8; base 16-byte aligned)
+ *   pos_logp    [B*T_pad] fp32: at position c with parent r,
+ *               log_softmax(logits[row r])[token c]; 0 under the root and at pad
+ *   pos_entropy [B*T_pad] fp32: -sum_v p_v log p_v of row p (natural log); 0 at pad
+ *   seq_logp    [total_seq_tokens] fp32: for sequence s at token t,
+ *               pos_logp[next position of s] (t < L-1) and 0 at t = L-1
+ *   seq_entropy [total_seq_tokens] fp32: pos_entropy at each token of s
+ * All outputs are device buffers and are written completely.  Errors:
+ * TPA_ERR_INVALID_ARG, TPA_ERR_CUDA.
+ */
+int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* logits, int64_t row_stride,
+                              int32_t layout, int32_t vocab, float* pos_logp, float* pos_entropy,
+                              float* seq_logp, float* seq_entropy, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronize `stream`, then read and clear the device status words of all
+ * kernels: TPA_OK, TPA_ERR_DEVICE_TIMEOUT or TPA_ERR_CUDA. */
+int tpa_sync_status(void* stream);
+
+/* TPA_OK when the current CUDA device is compute capability 10.3 (sm_103),
+ * TPA_ERR_UNSUPPORTED_DEVICE otherwise, TPA_ERR_CUDA without a device. */
+int tpa_device_check(void);
+
+/* Static, human-readable name of a status code. */
+const char* tpa_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int tpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPA_H_ */

@@ -1,0 +1,19 @@
+"""prefix_shared_tree_attention_gb300 — tree training's hot path on GB300.
+
+A thin Python binding over libtpa (include/tpa.h): argument marshalling and
+torch-owned device memory only; every step runs in the library (the C++
+packer on the host, CUDA kernels for sm_103a on the device). Functions keep
+the C names without the ``tpa_`` prefix:
+
+    tree = tree_pack(seqs, max_tokens_per_mb)           # host trie packer
+    dtree = tree.upload(device)                         # metadata -> HBM
+    mask = block_classify(dtree)                        # 128x128 tile classes + CSR
+    o, lse = tree_attn_fwd(dtree, mask, q, k, v)
+    dq, dk, dv = tree_attn_bwd(dtree, mask, q, k, v, o, lse, dout)
+    pos_logp, pos_ent, seq_logp, seq_ent = tree_logprobs_entropy(dtree, logits)
+"""
+from ._abi import BLOCK_SIZE, LOGITS_COMPACT, LOGITS_PADDED, STATUS, TpaError, lib  # noqa: F401
+from .api import (  # noqa: F401
+    BlockMask, DeviceTree, Tree, block_classify, device_check, sync_status, tree_attn_bwd,
+    tree_attn_bwd_workspace_bytes, tree_attn_fwd, tree_logprobs_entropy, tree_pack,
+)

@@ -1,0 +1,121 @@
+// Block classification of the packed trees (tree training page, §树构建过程
+// step 4 "mask generation" and §注意力机制: a block mask with BLOCK_SIZE 128
+// lets the attention skip empty blocks).
+//
+// Key j (real, j < n) is visible to query i iff j <= i <= E[j], E = subtree
+// end of j's node.  For a tile (qb, kb) the number of visible pairs is
+//   cnt = sum_{j in kb} max(0, min(E[j], q1) - max(j, q0) + 1),
+// q0 = 128 qb, q1 = q0 + 127; the tile is EMPTY when cnt = 0, FULL when
+// cnt = 128 * 128 and PARTIAL otherwise.  Two CSR lists follow: per query
+// block its non-empty key blocks (forward), per key block its non-empty
+// query blocks (backward), each entry 2 * block + (FULL ? 1 : 0).
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace {
+
+__device__ unsigned int g_status_classify = 0;
+
+constexpr int kB = TPA_BLOCK_SIZE;
+
+// grid (n_blk, B), 128 threads: one CTA per key block; warp w handles query
+// blocks qb = kb + w, kb + w + 4, ... with lane l covering keys l, l+32, ...
+__global__ void __launch_bounds__(128) classify_kernel(const int32_t* __restrict__ subtree_end,
+                                                        const int32_t* __restrict__ n_tokens,
+                                                        int32_t t_pad, int32_t n_blk,
+                                                        uint8_t* __restrict__ cls) {
+  __shared__ int e_s[kB];
+  __shared__ int emax_s[4];
+  const int b = blockIdx.y, kb = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = n_tokens[b];
+  const int j = kb * kB + tid;
+  const int e = (j < n) ? subtree_end[int64_t(b) * t_pad + j] : -1;
+  e_s[tid] = e;
+  int m = e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) emax_s[warp] = m;
+  __syncthreads();
+  const int emax = max(max(emax_s[0], emax_s[1]), max(emax_s[2], emax_s[3]));
+  uint8_t* out = cls + int64_t(b) * n_blk * n_blk + kb;   // column kb, row stride n_blk
+  const int qb_last = (emax < 0) ? -1 : emax / kB;        // no key of this block reaches beyond
+  for (int qb = warp; qb < n_blk; qb += 4) {
+    int c = TPA_BLOCK_EMPTY;
+    if (qb >= kb && qb <= qb_last) {
+      const int q0 = qb * kB, q1 = q0 + kB - 1;
+      int cnt = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int jj = kb * kB + lane + 32 * u;
+        const int ee = e_s[lane + 32 * u];
+        if (ee >= 0) cnt += max(0, min(ee, q1) - max(jj, q0) + 1);
+      }
+      cnt = warp_sum(cnt);
+      c = (cnt == 0) ? TPA_BLOCK_EMPTY : (cnt == kB * kB ? TPA_BLOCK_FULL : TPA_BLOCK_PARTIAL);
+    }
+    if (lane == 0) out[int64_t(qb) * n_blk] = uint8_t(c);
+  }
+}
+
+// grid (B, 2), blockDim >= n_blk: direction 0 builds the per-query-block CSR,
+// direction 1 the per-key-block CSR.  Thread `line` owns one row / column.
+__global__ void __launch_bounds__(1024) csr_kernel(const uint8_t* __restrict__ cls, int32_t n_blk,
+                                                    int32_t cap, int32_t* __restrict__ q_ptr,
+                                                    int32_t* __restrict__ q_idx,
+                                                    int32_t* __restrict__ k_ptr,
+                                                    int32_t* __restrict__ k_idx) {
+  __shared__ int scan_s[1024];
+  const int b = blockIdx.x, dir = blockIdx.y;
+  const int line = threadIdx.x;
+  const uint8_t* c = cls + int64_t(b) * n_blk * n_blk;
+  const int64_t s_line = dir == 0 ? n_blk : 1;   // stride between lines
+  const int64_t s_elem = dir == 0 ? 1 : n_blk;   // stride along a line
+  int cnt = 0;
+  if (line < n_blk)
+    for (int o = 0; o < n_blk; ++o) cnt += c[line * s_line + o * s_elem] != TPA_BLOCK_EMPTY;
+  scan_s[line] = cnt;
+  __syncthreads();
+  for (int off = 1; off < blockDim.x; off <<= 1) {   // inclusive Hillis-Steele scan
+    const int add = line >= off ? scan_s[line - off] : 0;
+    __syncthreads();
+    scan_s[line] += add;
+    __syncthreads();
+  }
+  if (line >= n_blk) return;
+  int32_t* ptr = (dir == 0 ? q_ptr : k_ptr) + int64_t(b) * (n_blk + 1);
+  int32_t* idx = (dir == 0 ? q_idx : k_idx) + int64_t(b) * cap;
+  int pos = scan_s[line] - cnt;
+  ptr[line] = pos;
+  if (line == n_blk - 1) ptr[n_blk] = scan_s[line];
+  for (int o = 0; o < n_blk; ++o) {
+    const uint8_t v = c[line * s_line + o * s_elem];
+    if (v != TPA_BLOCK_EMPTY) idx[pos++] = 2 * o + (v == TPA_BLOCK_FULL ? 1 : 0);
+  }
+}
+
+}  // namespace
+
+TPA_DEFINE_STATUS_READER(tpa_internal_status_classify, g_status_classify)
+
+extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
+                                  void* stream) {
+  if (!tree || !mask || !tree->subtree_end || !tree->n_tokens || !mask->cls || !mask->q_ptr ||
+      !mask->q_idx || !mask->k_ptr || !mask->k_idx)
+    return TPA_ERR_INVALID_ARG;
+  if (tree->t_pad % kB || mask->n_blk != tree->t_pad / kB || mask->n_trees != tree->n_trees ||
+      mask->n_blk > 1024 || tree->n_trees < 1)
+    return TPA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int n_blk = mask->n_blk;
+  classify_kernel<<<dim3(n_blk, tree->n_trees), 128, 0, st>>>(tree->subtree_end, tree->n_tokens,
+                                                              tree->t_pad, n_blk, mask->cls);
+  TPA_CUDA_TRY(cudaGetLastError());
+  const int threads = n_blk <= 32 ? 32 : ((n_blk + 31) / 32) * 32;
+  csr_kernel<<<dim3(tree->n_trees, 2), threads, 0, st>>>(mask->cls, n_blk, mask->cap, mask->q_ptr,
+                                                         mask->q_idx, mask->k_ptr, mask->k_idx);
+  TPA_CUDA_TRY(cudaGetLastError());
+  return TPA_OK;
+}

@@ -1,0 +1,53 @@
+// Device-side helpers shared by libtpa's kernels: launch checks, the
+// per-translation-unit status word, and small integer utilities.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tpa.h"
+
+// Codes written into a translation unit's device status word.
+enum : unsigned int {
+  TPA_DEV_OK = 0,
+  TPA_DEV_TIMEOUT = 1,  // a bounded mbarrier wait ran out; the kernel returned early
+};
+
+#define TPA_CUDA_TRY(expr)                        \
+  do {                                            \
+    if ((expr) != cudaSuccess) {                  \
+      (void)cudaGetLastError();                   \
+      return TPA_ERR_CUDA;                        \
+    }                                             \
+  } while (0)
+
+// Reads and optionally clears a device status word.  Must run after the
+// stream that may have written it has been synchronised.
+#define TPA_DEFINE_STATUS_READER(fn_name, symbol)                                  \
+  int fn_name(bool clear) {                                                        \
+    unsigned int v = 0;                                                            \
+    if (cudaMemcpyFromSymbol(&v, symbol, sizeof(v)) != cudaSuccess) {              \
+      (void)cudaGetLastError();                                                    \
+      return TPA_ERR_CUDA;                                                         \
+    }                                                                              \
+    if (clear && v != 0) {                                                         \
+      const unsigned int z = 0;                                                    \
+      if (cudaMemcpyToSymbol(symbol, &z, sizeof(z)) != cudaSuccess) {              \
+        (void)cudaGetLastError();                                                  \
+        return TPA_ERR_CUDA;                                                       \
+      }                                                                            \
+    }                                                                              \
+    return v == 0 ? TPA_OK : TPA_ERR_DEVICE_TIMEOUT;                               \
+  }
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}

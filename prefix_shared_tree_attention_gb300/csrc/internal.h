@@ -1,0 +1,14 @@
+// Declarations shared by the translation units of libtpa (not part of the ABI).
+#pragma once
+#include <cstdint>
+
+#include "tpa.h"
+
+uint64_t tpa_internal_blob_bytes(const tpa_tree* tree);
+
+// Each CUDA translation unit keeps its own device status word; these read
+// (and clear) it.  They return TPA_OK, TPA_ERR_DEVICE_TIMEOUT or TPA_ERR_CUDA.
+int tpa_internal_status_classify(bool clear);
+int tpa_internal_status_logprobs(bool clear);
+int tpa_internal_status_fwd(bool clear);
+int tpa_internal_status_bwd(bool clear);

@@ -1,0 +1,197 @@
+// Log-probabilities and entropies of a packed tree (tree training page,
+// §对数概率计算): each tree row is processed exactly once (the node-level
+// cache of the page), and the labels of that row — the next token inside its
+// node and the first token of every child node — are gathered in the same
+// pass; a second kernel regathers the per-position values per input sequence.
+//
+// Row kernel: one CTA streams one logits row (bf16, 16-byte vector loads)
+// and keeps, per thread, the running max m, s = sum exp(x - m) and
+// t = sum exp(x - m) * x; after a block reduction
+//   lse = m + log s,   entropy = lse - t / s   (= -sum p log p),
+//   pos_logp[c] = x[token c] - lse   for every child position c of the row.
+// HBM-bound: each logits element is read once.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace {
+
+__device__ unsigned int g_status_logprobs = 0;
+
+constexpr int kRowThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+struct Acc {
+  float m, s, t;  // running max, sum exp(x - m), sum exp(x - m) * x
+};
+
+__device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return;
+  const float ca = ex2((a.m - m) * kLog2e), cb = ex2((b.m - m) * kLog2e);
+  a.s = a.s * ca + b.s * cb;
+  a.t = a.t * ca + b.t * cb;
+  a.m = m;
+}
+
+// Fold 8 values (one 16-byte vector) into the accumulator.
+__device__ __forceinline__ void acc_add8(Acc& a, const uint4 v) {
+  float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  float mc = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                   fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  if (mc > a.m) {
+    const float c = ex2((a.m - mc) * kLog2e);
+    a.s *= c;
+    a.t *= c;
+    a.m = mc;
+  }
+  const float mb = a.m * kLog2e;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float e = ex2(fmaf(x[i], kLog2e, -mb));
+    a.s += e;
+    a.t = fmaf(e, x[i], a.t);
+  }
+}
+
+__device__ __forceinline__ void acc_add1(Acc& a, float x) {
+  if (x > a.m) {
+    const float c = ex2((a.m - x) * kLog2e);
+    a.s *= c;
+    a.t *= c;
+    a.m = x;
+  }
+  const float e = ex2((x - a.m) * kLog2e);
+  a.s += e;
+  a.t = fmaf(e, x, a.t);
+}
+
+// grid (T_pad, B): CTA (p, b) handles tree position p of tree b.
+__global__ void __launch_bounds__(kRowThreads) row_kernel(
+    const uint16_t* __restrict__ logits, int64_t row_stride, int32_t layout, int32_t vocab,
+    int32_t t_pad, const int32_t* __restrict__ n_tokens, const int64_t* __restrict__ tok_base,
+    const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
+    const int32_t* __restrict__ child_off, const int32_t* __restrict__ child_pos,
+    float* __restrict__ pos_logp, float* __restrict__ pos_entropy) {
+  const int p = blockIdx.x, b = blockIdx.y;
+  const int64_t at = int64_t(b) * t_pad + p;
+  const int n = n_tokens[b];
+  if (p >= n) {  // padding position
+    if (threadIdx.x == 0) {
+      pos_logp[at] = 0.f;
+      pos_entropy[at] = 0.f;
+    }
+    return;
+  }
+  const int64_t row = (layout == TPA_LOGITS_COMPACT) ? tok_base[b] + p : int64_t(b) * t_pad + p;
+  const uint16_t* x = logits + row * row_stride;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const int nvec = vocab >> 3;
+
+  Acc a{-INFINITY, 0.f, 0.f};
+  int i = threadIdx.x;
+  for (; i + 3 * kRowThreads < nvec; i += 4 * kRowThreads) {
+    const uint4 v0 = __ldcs(xv + i);
+    const uint4 v1 = __ldcs(xv + i + kRowThreads);
+    const uint4 v2 = __ldcs(xv + i + 2 * kRowThreads);
+    const uint4 v3 = __ldcs(xv + i + 3 * kRowThreads);
+    acc_add8(a, v0);
+    acc_add8(a, v1);
+    acc_add8(a, v2);
+    acc_add8(a, v3);
+  }
+  for (; i < nvec; i += kRowThreads) acc_add8(a, __ldcs(xv + i));
+  for (int k = (nvec << 3) + threadIdx.x; k < vocab; k += kRowThreads)
+    acc_add1(a, __uint_as_float(uint32_t(x[k]) << 16));
+
+  // block reduction of (m, s, t)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Acc bo{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o),
+           __shfl_xor_sync(0xffffffffu, a.t, o)};
+    acc_merge(a, bo);
+  }
+  __shared__ Acc part[kRowThreads / 32];
+  __shared__ float lse_s;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) part[warp] = a;
+  __syncthreads();
+  if (warp == 0) {
+    a = lane < kRowThreads / 32 ? part[lane] : Acc{-INFINITY, 0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Acc bo{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o),
+             __shfl_xor_sync(0xffffffffu, a.t, o)};
+      acc_merge(a, bo);
+    }
+    if (lane == 0) {
+      const float lse = a.m + __log2f(a.s) * kLn2;
+      lse_s = lse;
+      pos_entropy[at] = lse - a.t / a.s;
+      if (parent[at] < 0) pos_logp[at] = 0.f;  // no parent row: no label for this position
+    }
+  }
+  __syncthreads();
+  const int c0 = child_off[int64_t(b) * (t_pad + 1) + p];
+  const int c1 = child_off[int64_t(b) * (t_pad + 1) + p + 1];
+  for (int c = c0 + threadIdx.x; c < c1; c += kRowThreads) {
+    const int cp = child_pos[int64_t(b) * t_pad + c];
+    const int tok = tokens[int64_t(b) * t_pad + cp];
+    const float xl = __uint_as_float(uint32_t(x[tok]) << 16);
+    pos_logp[int64_t(b) * t_pad + cp] = xl - lse_s;
+  }
+}
+
+// grid (n_seqs): per input sequence s at token t,
+//   seq_entropy[t] = pos_entropy[g_t],  seq_logp[t] = pos_logp[g_{t+1}] (0 at the end).
+__global__ void __launch_bounds__(256) seq_gather_kernel(
+    int32_t t_pad, const int32_t* __restrict__ seq_tree, const int64_t* __restrict__ seq_off,
+    const int32_t* __restrict__ seq_pos, const float* __restrict__ pos_logp,
+    const float* __restrict__ pos_entropy, float* __restrict__ seq_logp,
+    float* __restrict__ seq_entropy) {
+  const int s = blockIdx.x;
+  const int64_t o0 = seq_off[s], o1 = seq_off[s + 1];
+  const int64_t base = int64_t(seq_tree[s]) * t_pad;
+  for (int64_t i = o0 + threadIdx.x; i < o1; i += blockDim.x) {
+    seq_entropy[i] = pos_entropy[base + seq_pos[i]];
+    seq_logp[i] = (i + 1 < o1) ? pos_logp[base + seq_pos[i + 1]] : 0.f;
+  }
+}
+
+}  // namespace
+
+TPA_DEFINE_STATUS_READER(tpa_internal_status_logprobs, g_status_logprobs)
+
+extern "C" int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* logits,
+                                         int64_t row_stride, int32_t layout, int32_t vocab,
+                                         float* pos_logp, float* pos_entropy, float* seq_logp,
+                                         float* seq_entropy, void* stream) {
+  if (!tree || !logits || !pos_logp || !pos_entropy || !seq_logp || !seq_entropy) return TPA_ERR_INVALID_ARG;
+  if (vocab < 1 || row_stride < vocab || (row_stride & 7) || (reinterpret_cast<uintptr_t>(logits) & 15))
+    return TPA_ERR_INVALID_ARG;
+  if (layout != TPA_LOGITS_COMPACT && layout != TPA_LOGITS_PADDED) return TPA_ERR_INVALID_ARG;
+  if (tree->n_trees < 1 || tree->t_pad < 1 || tree->n_seqs < 1) return TPA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  row_kernel<<<dim3(tree->t_pad, tree->n_trees), kRowThreads, 0, st>>>(
+      static_cast<const uint16_t*>(logits), row_stride, layout, vocab, tree->t_pad, tree->n_tokens,
+      tree->tok_base, tree->tokens, tree->parent, tree->child_off, tree->child_pos, pos_logp,
+      pos_entropy);
+  TPA_CUDA_TRY(cudaGetLastError());
+  seq_gather_kernel<<<tree->n_seqs, 256, 0, st>>>(tree->t_pad, tree->seq_tree, tree->seq_off,
+                                                  tree->seq_pos, pos_logp, pos_entropy, seq_logp,
+                                                  seq_entropy);
+  TPA_CUDA_TRY(cudaGetLastError());
+  return TPA_OK;
+}

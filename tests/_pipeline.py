@@ -1,0 +1,76 @@
+"""Shared helpers of the GPU parity tests: run the library path on seeded
+inputs and compare against the oracle with the stated tolerances."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from synth import CONFIGS, make_dout, make_qkv, make_sequences
+
+ATTN_MAX_ABS = 2e-2   # attention outputs and gradients vs fp64
+ATTN_REL_L2 = 5e-3
+LOGP_ABS = 1e-3       # log-probs and entropies vs fp64
+
+
+def assert_attn_close(got: torch.Tensor, ref: torch.Tensor, what: str,
+                      max_abs: float = ATTN_MAX_ABS, rel_l2: float = ATTN_REL_L2) -> tuple[float, float]:
+    g = got.detach().to("cpu", torch.float64)
+    r = ref.detach().to("cpu", torch.float64)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert torch.isfinite(g).all(), f"{what}: non-finite values"
+    err = (g - r).abs().max().item() if g.numel() else 0.0
+    nrm = r.norm().item()
+    rel = (g - r).norm().item() / nrm if nrm > 0 else (g - r).norm().item()
+    assert err <= max_abs and rel <= rel_l2, f"{what}: max-abs {err:.3e}, rel-L2 {rel:.3e}"
+    return err, rel
+
+
+def pack_and_upload(tpa, seqs, mb, device="cuda"):
+    tree = tpa.tree_pack(seqs, mb)
+    dtree = tree.upload(device)
+    mask = tpa.block_classify(dtree)
+    return tree, dtree, mask
+
+
+def random_inputs(B, T, hq, hkv, d, seed, device="cuda"):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, T, hq, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, T, hkv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, T, hkv, d), generator=g).to(torch.bfloat16)
+    do = torch.randn((B, T, hq, d), generator=g).to(torch.bfloat16)
+    return [x.to(device) for x in (q, k, v, do)], (q, k, v, do)
+
+
+def workload(cid: int):
+    cfg = CONFIGS[cid]
+    seqs = make_sequences(cid)
+    return cfg, seqs
+
+
+def workload_tensors(cid: int, B: int, T: int):
+    cfg = CONFIGS[cid]
+    q, k, v = make_qkv(cid, B, T, cfg.n_heads_q, cfg.n_heads_kv, cfg.head_dim)
+    do = make_dout(cid, B, T, cfg.n_heads_q, cfg.head_dim)
+    return q, k, v, do
+
+
+def leaf_nodes(tree: oracle.OracleTree, count: int, max_len: int = 10**9) -> list[int]:
+    """Up to ``count`` leaf nodes (no child node), shortest first: their keys
+    are seen only by their own queries, so a node-restricted oracle gives
+    their exact dK/dV rows."""
+    has_child = np.zeros(len(tree.node_start), dtype=bool)
+    has_child[tree.node_parent[tree.node_parent >= 0]] = True
+    leaves = [int(n) for n in np.nonzero(~has_child)[0]]
+    leaves.sort(key=lambda n: int(tree.node_end[n] - tree.node_start[n]))
+    return [n for n in leaves if tree.node_end[n] - tree.node_start[n] + 1 <= max_len][:count]
+
+
+def node_rows(tree: oracle.OracleTree, nodes: list[int]) -> torch.Tensor:
+    return torch.cat([torch.arange(int(tree.node_start[n]), int(tree.node_end[n]) + 1) for n in nodes])
+
+
+def scale_for(d: int) -> float:
+    return 1.0 / math.sqrt(d)

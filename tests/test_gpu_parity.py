@@ -1,0 +1,266 @@
+"""GPU parity: the library path (through the C ABI) against the oracle.
+
+Block classes and CSR lists are compared bit-exactly; attention outputs and
+gradients within max-abs 2e-2 and relative-L2 5e-3 of fp64; log-probs and
+entropies within 1e-3 absolute. Small cases compare every output; the full
+workload sizes compare sampled nodes (leaf nodes for dK/dV, whose keys only
+their own queries see) and sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.mask import block_classes, block_csr
+from synth import CONFIGS, make_logits, random_small_sequences
+from _pipeline import (LOGP_ABS, assert_attn_close, leaf_nodes, node_rows, pack_and_upload,
+                       random_inputs, workload, workload_tensors)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tpa():
+    import prefix_shared_tree_attention_gb300 as tpa
+    tpa.lib()
+    tpa.device_check()
+    return tpa
+
+
+def _check_mask(tpa, pk, mask, T):
+    arr = {k: v.cpu().numpy() for k, v in mask.arrays().items()}
+    for b, t in enumerate(pk.trees):
+        cls = block_classes(t, T)
+        assert np.array_equal(arr["cls"][b], cls), f"tree {b}: block classes differ"
+        csr = block_csr(cls)
+        nq = len(csr["q_idx"])
+        assert np.array_equal(arr["q_ptr"][b], csr["q_ptr"])
+        assert np.array_equal(arr["q_idx"][b][:nq], csr["q_idx"])
+        assert np.array_equal(arr["k_ptr"][b], csr["k_ptr"])
+        assert np.array_equal(arr["k_idx"][b][:nq], csr["k_idx"])
+
+
+# ---------------------------------------------------------------- block classes
+
+@pytest.mark.parametrize("seed", range(6))
+def test_classify_random(tpa, seed):
+    rng = np.random.default_rng(seed)
+    seqs = random_small_sequences(rng, 12, 300, 3, min_len=20)
+    T = 128 * int(rng.integers(4, 9))
+    pk = oracle.tree_pack(seqs, T)
+    _, _, mask = pack_and_upload(tpa, seqs, T)
+    _check_mask(tpa, pk, mask, T)
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 5])
+def test_classify_workloads(tpa, cid):
+    cfg, seqs = workload(cid)
+    pk = oracle.tree_pack(seqs, cfg.max_tokens_per_mb)
+    _, _, mask = pack_and_upload(tpa, seqs, cfg.max_tokens_per_mb)
+    _check_mask(tpa, pk, mask, cfg.max_tokens_per_mb)
+
+
+# ---------------------------------------------------------------- attention, full oracle
+
+CASES = [
+    # (seed, n_seqs, max_len, vocab, T_pad, hq, hkv, d)
+    (0, 6, 200, 3, 384, 2, 2, 64),
+    (1, 8, 300, 4, 512, 4, 2, 64),
+    (2, 5, 250, 3, 384, 4, 1, 128),
+    (3, 10, 180, 2, 256, 2, 2, 128),
+    (4, 3, 128, 50, 256, 2, 1, 64),     # exact block multiple, little sharing
+    (5, 14, 120, 3, 512, 8, 2, 128),    # several trees
+]
+
+
+def _run_full_case(tpa, seqs, T, hq, hkv, d, seed, check_bwd=True):
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    B = tree.n_trees
+    (q, k, v, do), (qc, kc, vc, doc) = random_inputs(B, T, hq, hkv, d, seed)
+    o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    if check_bwd:
+        dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do)
+    tpa.sync_status()
+    for b, t in enumerate(pk.trees):
+        O, L = oracle.attn_forward(t, qc[b], kc[b], vc[b], t_pad=T)
+        assert_attn_close(o[b], O, f"O tree {b}")
+        assert_attn_close(lse[b], L, f"LSE tree {b}", max_abs=2e-3, rel_l2=1e-4)
+        assert torch.all(o[b, t.n:] == 0) and torch.all(lse[b, :, t.n:] == 0)
+        if check_bwd:
+            dQ, dK, dV = oracle.attn_backward(t, qc[b], kc[b], vc[b], doc[b], t_pad=T)
+            assert_attn_close(dq[b], dQ, f"dQ tree {b}")
+            assert_attn_close(dk[b], dK, f"dK tree {b}")
+            assert_attn_close(dv[b], dV, f"dV tree {b}")
+            assert torch.all(dq[b, t.n:] == 0) and torch.all(dk[b, t.n:] == 0) and torch.all(dv[b, t.n:] == 0)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{c[0]}" for c in CASES])
+def test_attention_small(tpa, case):
+    seed, n, L, V, T, hq, hkv, d = case
+    rng = np.random.default_rng(500 + seed)
+    seqs = random_small_sequences(rng, n, L, V, min_len=1)
+    _run_full_case(tpa, seqs, T, hq, hkv, d, seed)
+
+
+def test_attention_single_chain_minimal(tpa):
+    # one sequence filling exactly one block: a single PARTIAL (causal) tile
+    _run_full_case(tpa, [list(range(128))], 128, 2, 2, 64, 7)
+
+
+def test_attention_duplicates_and_singletons(tpa):
+    seqs = [[5, 6, 7, 8]] * 4 + [[9]] + [[5, 6]] + [list(range(100, 300))]
+    _run_full_case(tpa, seqs, 256, 4, 2, 128, 8)
+
+
+def test_attention_config1_full(tpa):
+    cfg, seqs = workload(1)
+    T = cfg.max_tokens_per_mb
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    q, k, v, do = workload_tensors(1, tree.n_trees, T)
+    o, lse = tpa.tree_attn_fwd(dtree, mask, q.cuda(), k.cuda(), v.cuda())
+    dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, q.cuda(), k.cuda(), v.cuda(), o, lse, do.cuda())
+    tpa.sync_status()
+    t = pk.trees[0]
+    O, L = oracle.attn_forward(t, q[0], k[0], v[0], t_pad=T)
+    dQ, dK, dV = oracle.attn_backward(t, q[0], k[0], v[0], do[0], t_pad=T)
+    assert_attn_close(o[0], O, "O")
+    assert_attn_close(dq[0], dQ, "dQ")
+    assert_attn_close(dk[0], dK, "dK")
+    assert_attn_close(dv[0], dV, "dV")
+
+
+def test_attention_deterministic_forward(tpa):
+    rng = np.random.default_rng(77)
+    seqs = random_small_sequences(rng, 10, 300, 3)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, 512)
+    (q, k, v, _), _ = random_inputs(tree.n_trees, 512, 4, 2, 128, 3)
+    o1, l1 = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    o2, l2 = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    tpa.sync_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ---------------------------------------------------------------- attention, full-size workloads (sampled)
+
+@pytest.mark.parametrize("cid", [2, 3, 5])
+def test_attention_workload_sampled(tpa, cid):
+    cfg, seqs = workload(cid)
+    T = cfg.max_tokens_per_mb
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    q, k, v, do = workload_tensors(cid, tree.n_trees, T)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = tpa.tree_attn_fwd(dtree, mask, qd, kd, vd)
+    dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, qd, kd, vd, o, lse, dod)
+    tpa.sync_status()
+    trees = [0, pk.n_trees - 1] if pk.n_trees > 1 else [0]
+    for b in trees:
+        t = pk.trees[b]
+        leaves = leaf_nodes(t, 2, max_len=1200)
+        nodes = sorted(set(leaves + [0]))
+        O, L = oracle.attn_forward(t, q[b], k[b], v[b], t_pad=T, nodes=nodes)
+        rows = node_rows(t, nodes)
+        assert_attn_close(o[b].cpu()[rows], O[rows], f"cfg{cid} O tree {b}")
+        assert_attn_close(lse[b].cpu()[:, rows], L[:, rows], f"cfg{cid} LSE tree {b}", max_abs=2e-3, rel_l2=1e-4)
+        dQ, dK, dV = oracle.attn_backward(t, q[b], k[b], v[b], do[b], t_pad=T, nodes=leaves)
+        lrows = node_rows(t, leaves)
+        assert_attn_close(dq[b].cpu()[lrows], dQ[lrows], f"cfg{cid} dQ tree {b}")
+        assert_attn_close(dk[b].cpu()[lrows], dK[lrows], f"cfg{cid} dK tree {b}")
+        assert_attn_close(dv[b].cpu()[lrows], dV[lrows], f"cfg{cid} dV tree {b}")
+        assert torch.all(o[b, t.n:] == 0) and torch.all(dk[b, t.n:] == 0)
+
+
+# ---------------------------------------------------------------- log-probs / entropy
+
+def _check_logprobs(tpa, pk, seqs, dtree, logits, layout, row_base, seq_ids, pos_sample):
+    pl, pe, sl, se = tpa.tree_logprobs_entropy(dtree, logits, layout=layout)
+    tpa.sync_status()
+    rows_needed = sorted({int(row_base[int(pk.seq_tree[s])] + p) for s in seq_ids for p in pk.seq_pos[s]} |
+                         {int(row_base[b] + p) for b, ps in pos_sample.items() for p in ps} |
+                         {int(row_base[b] + pk.trees[b].parent[p]) for b, ps in pos_sample.items() for p in ps
+                          if pk.trees[b].parent[p] >= 0})
+    idx = torch.as_tensor(rows_needed)
+    sub = logits[idx.cuda()].cpu()
+    remap = {r: i for i, r in enumerate(rows_needed)}
+
+    class Rows:  # row-indexable view over the copied rows
+        def __getitem__(self, r):
+            if isinstance(r, torch.Tensor):
+                return sub[torch.as_tensor([remap[int(x)] for x in r.reshape(-1)]).reshape(r.shape)]
+            return sub[remap[int(r)]]
+
+    lp, ent = oracle.sequence_logprobs_entropy(pk, seqs, Rows(), row_base, seq_ids)
+    offs = np.concatenate([[0], np.cumsum([len(s) for s in seqs])])
+    sl_c, se_c = sl.cpu().double().numpy(), se.cpu().double().numpy()
+    for u, s in enumerate(seq_ids):
+        assert np.abs(sl_c[offs[s]:offs[s + 1]] - lp[u]).max() <= LOGP_ABS, f"seq {s} logp"
+        assert np.abs(se_c[offs[s]:offs[s + 1]] - ent[u]).max() <= LOGP_ABS, f"seq {s} entropy"
+    for b, ps in pos_sample.items():
+        plp, pent = oracle.position_logprobs_entropy(pk, Rows(), row_base, b, ps)
+        assert np.abs(pl[b].cpu().double().numpy()[ps] - plp).max() <= LOGP_ABS
+        assert np.abs(pe[b].cpu().double().numpy()[ps] - pent).max() <= LOGP_ABS
+        n = pk.trees[b].n
+        assert torch.all(pl[b, n:] == 0) and torch.all(pe[b, n:] == 0)
+
+
+def test_logprobs_config1_full(tpa):
+    cfg, seqs = workload(1)
+    T = cfg.max_tokens_per_mb
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    rows = tree.info.total_tree_tokens
+    logits = make_logits(1, rows, cfg.logits_vocab).cuda()
+    row_base = [0]
+    _check_logprobs(tpa, pk, seqs, dtree, logits, "compact", row_base, list(range(len(seqs))),
+                    {0: list(range(pk.trees[0].n))})
+
+
+def test_logprobs_padded_layout_odd_vocab(tpa):
+    rng = np.random.default_rng(9)
+    seqs = random_small_sequences(rng, 9, 200, 3, min_len=2)
+    T = 256
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    V, stride = 1003, 1008   # ragged vector tail, padded row stride
+    buf = (2 * torch.randn((pk.n_trees * T, stride), generator=torch.Generator().manual_seed(4))).to(torch.bfloat16)
+    logits = buf.cuda()[:, :V]
+    row_base = [b * T for b in range(pk.n_trees)]
+    _check_logprobs(tpa, pk, seqs, dtree, logits, "padded", row_base, list(range(len(seqs))),
+                    {b: list(range(pk.trees[b].n)) for b in range(pk.n_trees)})
+
+
+def test_logprobs_config4_sampled(tpa):
+    cfg, seqs = workload(4)
+    T = cfg.max_tokens_per_mb
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    rows = tree.info.total_tree_tokens
+    logits = make_logits(4, rows, cfg.logits_vocab, device="cuda")
+    row_base = [int(x) for x in tree.arrays()["tok_base"][:-1]]
+    rng = np.random.default_rng(4)
+    seq_ids = sorted(rng.choice(len(seqs), size=3, replace=False).tolist())
+    pos = {b: sorted(rng.choice(pk.trees[b].n, size=64, replace=False).tolist()) for b in (0, pk.n_trees - 1)}
+    _check_logprobs(tpa, pk, seqs, dtree, logits, "compact", row_base, seq_ids, pos)
+
+
+# ---------------------------------------------------------------- argument checks through the ABI
+
+def test_invalid_arguments(tpa):
+    tree, dtree, mask = pack_and_upload(tpa, [[1, 2, 3]], 128)
+    (q, k, v, do), _ = random_inputs(1, 128, 4, 2, 64, 0)
+    import ctypes as C
+    L = tpa.lib()
+    rc = L.tpa_tree_attn_fwd(C.byref(dtree.view), C.byref(mask.view), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                             q.data_ptr(), None, 4, 2, 96, 0.0, None)
+    assert rc == -1  # head_dim 96 unsupported (and lse missing)
+    rc = L.tpa_tree_attn_fwd(C.byref(dtree.view), C.byref(mask.view), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                             q.data_ptr(), q.data_ptr(), 4, 3, 64, 0.0, None)
+    assert rc == -1  # Hq % Hkv != 0
+    o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tpa.TpaError) as e:
+        tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=small)
+    assert e.value.name == "TPA_ERR_BUFFER_TOO_SMALL"
+    tpa.sync_status()
