@@ -1,0 +1,412 @@
+"""Benchmark of the tree-training hot path on GB300.
+
+One step = one pass of every device row of the path over the GRPO-shaped
+workload (8 prompts x 8 samples, bimodal responses, max_tokens_per_mb 8192,
+32 query / 8 kv heads, head_dim 128) with its log-prob pass over bf16 logits
+of width 151936 on the same packed trees:
+    block classification -> tree attention forward -> tree attention backward
+    -> log-softmax / entropy / label gather -> per-sequence regather.
+The packed metadata and every input are resident in HBM when the timed
+region starts (``value``); ``e2e`` repeats the step through the public API
+from host buffers: host packing, metadata upload, host->device copies of
+q, k, v, dO and logits from pinned memory, the device work, and the
+device->host copies of O, dQ, dK, dV and the per-sequence log-probs and
+entropies.
+
+Metric: ancestor-pair attention FLOPs (FlashAttention convention, forward
+4 P d Hq, backward 2.5x, i.e. 14 P d Hq per step, P = sum of depth + 1 over
+tree tokens) per second of the whole step; tree tokens/s is reported beside
+it. Every input (q alone is 470 MB) is larger than the 129 MB L2, so no flush
+is needed between steps.
+
+``--impl reference`` times the CPU oracle (fp64, host cores) on a bounded
+sample of the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tree-attn fwd+bwd TFLOP/s on ancestor pairs (% bf16 peak); tree tokens/s"
+UNIT = "TFLOP/s"
+WORKLOAD = ("GRPO-shaped: 8 prompts x 8 samples, prompts 256-1024, responses 70% 50-200 / 30% 800-2048 "
+            "tokens, vocab 32000, max_tokens_per_mb 8192, 32 q / 8 kv heads, head_dim 128, bf16; "
+            "log-probs over bf16 logits [tree tokens, 151936] on the same trees")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _pairs(tree_arrays, n_tokens):
+    d = tree_arrays["depth"]
+    return int(sum(int((d[b, :n] + 1).sum()) for b, n in enumerate(n_tokens)))
+
+
+# ---------------------------------------------------------------- CPU oracle (reference arm / cpu_baseline)
+
+def _oracle_sample(cfg, seqs, budget_pairs: int):
+    """Nodes of tree 0 (shortest first) whose ancestor pairs sum to about
+    ``budget_pairs``; returns (tree, nodes, pairs)."""
+    import numpy as np
+    import oracle
+    pk = oracle.tree_pack(seqs, cfg.max_tokens_per_mb)
+    t = pk.trees[0]
+    order = np.argsort(t.node_end - t.node_start, kind="stable")
+    nodes, pairs = [], 0
+    for nid in order:
+        s0, s1 = int(t.node_start[nid]), int(t.node_end[nid])
+        p = int((t.depth[s0:s1 + 1] + 1).sum())
+        if pairs + p > budget_pairs and nodes:
+            continue
+        nodes.append(int(nid))
+        pairs += p
+        if pairs >= budget_pairs:
+            break
+    return pk, t, nodes, pairs
+
+
+def _oracle_step(cfg, t, nodes, q, k, v, do):
+    import oracle
+    oracle.attn_forward(t, q, k, v, t_pad=cfg.max_tokens_per_mb, nodes=nodes)
+    oracle.attn_backward(t, q, k, v, do, t_pad=cfg.max_tokens_per_mb, nodes=nodes)
+
+
+def cpu_oracle_run(steps: int, warmup: int, budget_pairs: int):
+    """Time the fp64 oracle's attention fwd+bwd on a bounded sample."""
+    import torch
+    from synth import CONFIGS, make_sequences
+    cfg = CONFIGS[2]
+    seqs = make_sequences(2)
+    pk, t, nodes, pairs = _oracle_sample(cfg, seqs, budget_pairs)
+    T = cfg.max_tokens_per_mb
+    g = torch.Generator().manual_seed(2001)
+    q = torch.randn((T, cfg.n_heads_q, cfg.head_dim), generator=g).to(torch.bfloat16)
+    k = torch.randn((T, cfg.n_heads_kv, cfg.head_dim), generator=g).to(torch.bfloat16)
+    v = torch.randn((T, cfg.n_heads_kv, cfg.head_dim), generator=g).to(torch.bfloat16)
+    do = torch.randn((T, cfg.n_heads_q, cfg.head_dim), generator=g).to(torch.bfloat16)
+    for _ in range(warmup):
+        _oracle_step(cfg, t, nodes, q, k, v, do)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        _oracle_step(cfg, t, nodes, q, k, v, do)
+        times.append(time.perf_counter() - t0)
+    flops = 14.0 * pairs * cfg.head_dim * cfg.n_heads_q
+    sec = sum(times) / len(times)
+    sample = (f"oracle fp64 attention fwd+bwd on {len(nodes)} nodes of tree 0 (shortest first), "
+              f"{pairs} ancestor pairs x {cfg.n_heads_q} heads x d {cfg.head_dim}; "
+              f"{sec:.2f} s per step")
+    return {"value": flops / sec / 1e12, "sec_per_step": sec, "pairs": pairs, "nodes": len(nodes),
+            "sample": sample, "cores": torch.get_num_threads(), "tree_tokens_per_s":
+            sum(int(t.node_end[n] - t.node_start[n] + 1) for n in nodes) / sec}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    r = cpu_oracle_run(args.steps, args.warmup, args.oracle_pairs)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["sec_per_step"] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "bounded oracle sample"},
+        "cpu_baseline": {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import prefix_shared_tree_attention_gb300 as tpa
+    from synth import CONFIGS, flatten_sequences, make_dout, make_logits, make_qkv, make_sequences
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tpa.device_check()
+    cfg, lcfg = CONFIGS[2], CONFIGS[4]
+    seed = 2 + 1000 * rank  # weak scaling: every rank packs and processes its own batch of trees
+    seqs = make_sequences(2, seed=seed)
+    toks, offs = flatten_sequences(seqs)
+    T, Hq, Hkv, d, V = cfg.max_tokens_per_mb, cfg.n_heads_q, cfg.n_heads_kv, cfg.head_dim, lcfg.logits_vocab
+
+    tree = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
+    info = tree.info
+    B = info.n_trees
+    rows = info.total_tree_tokens
+    pairs = int(info.ancestor_pairs)
+    flops_fwd = 4.0 * pairs * d * Hq
+    flops_step = 14.0 * pairs * d * Hq
+
+    dtree = tree.upload(dev)
+    mask = tpa.BlockMask(B, T, dev)
+    qh, kh, vh = make_qkv(2, B, T, Hq, Hkv, d)
+    doh = make_dout(2, B, T, Hq, d)
+    q, k, v, do = (x.to(dev) for x in (qh, kh, vh, doh))
+    logits = make_logits(4, rows, V, device=str(dev))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty(x.shape, dtype=torch.float32, device=dev) for x in (q, k, v))
+    ws = torch.empty(tpa.tree_attn_bwd_workspace_bytes(B, T, Hq, d), dtype=torch.uint8, device=dev)
+    N = info.total_seq_tokens
+    lp_out = (torch.empty((B, T), dtype=torch.float32, device=dev), torch.empty((B, T), dtype=torch.float32, device=dev),
+              torch.empty(N, dtype=torch.float32, device=dev), torch.empty(N, dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+    n_launch_per_step = 2 + 1 + 2 + 2  # classify+csr, fwd, bwd pre+main (fp32 grads), rows+regather
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        tpa.block_classify(dtree, out=mask)
+        if ev: ev[1].record(stream)
+        tpa.tree_attn_fwd(dtree, mask, q, k, v, out=o, lse=lse)
+        if ev: ev[2].record(stream)
+        tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv))
+        if ev: ev[3].record(stream)
+        tpa.tree_logprobs_entropy(dtree, logits, out=lp_out)
+        if ev: ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    tpa.sync_status()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    tpa.sync_status()
+    total_ms = t_start.elapsed_time(t_end)
+    seg = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    t_cls, t_fwd, t_bwd, t_lp = seg.mean(axis=0)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    clocks = clk.summary()
+
+    # ------------------------------------------------ end to end from host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda x: x.pin_memory()
+        qp, kp, vp, dop = pin(qh), pin(kh), pin(vh), pin(doh)
+        lg_host = torch.empty((rows, V), dtype=torch.bfloat16, pin_memory=True)
+        lg_host.copy_(logits)
+        out_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv)]
+        seq_host = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+        blob_buf = torch.empty(int(info.blob_bytes), dtype=torch.uint8, device=dev)
+
+        def e2e_step():
+            tr = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
+            dt = tr.upload(dev, buffer=blob_buf)
+            q.copy_(qp, non_blocking=True); k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True); do.copy_(dop, non_blocking=True)
+            logits.copy_(lg_host, non_blocking=True)
+            tpa.block_classify(dt, out=mask)
+            tpa.tree_attn_fwd(dt, mask, q, k, v, out=o, lse=lse)
+            tpa.tree_attn_bwd(dt, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv))
+            tpa.tree_logprobs_entropy(dt, logits, out=lp_out)
+            for h_, d_ in zip(out_host, (o, dq, dk, dv)):
+                h_.copy_(d_, non_blocking=True)
+            seq_host[0].copy_(lp_out[2], non_blocking=True)
+            seq_host[1].copy_(lp_out[3], non_blocking=True)
+            torch.cuda.synchronize(dev)
+            return tr
+
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        for _ in range(max(1, min(args.warmup, 2))):
+            e2e_step()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e2e_sec = (time.perf_counter() - t0) / e2e_steps
+        if world > 1:
+            tt = torch.tensor([e2e_sec], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_sec = float(tt.item())
+        tpa.sync_status()
+        h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, dop, lg_host)) + int(info.blob_bytes)
+        d2h = sum(x.numel() * x.element_size() for x in out_host) + 2 * 4 * N
+        e2e = {"value": world * flops_step / e2e_sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_sec * 1e3,
+               "includes": "host pack + metadata upload + pinned H2D of q,k,v,dO,logits + device step + "
+                           "D2H of O,dQ,dK,dV,seq log-probs/entropies"}
+
+    peaks, peak_kind = _peaks()
+    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    attn_tflops = (flops_step / 1e12) / ((t_fwd + t_bwd) / 1e3)
+    bwd_tflops = (10.0 * pairs * d * Hq / 1e12) / (t_bwd / 1e3)
+    fwd_tflops = (flops_fwd / 1e12) / (t_fwd / 1e3)
+    lp_bytes = rows * V * 2 + 4 * 4 * B * T + 8 * N
+    lp_gbs = lp_bytes / (t_lp / 1e3) / 1e9
+    dominant = max((("tpa_tree_attn_bwd", t_bwd), ("tpa_tree_attn_fwd", t_fwd), ("tpa_tree_logprobs_entropy", t_lp)),
+                   key=lambda x: x[1])[0]
+    if dominant == "tpa_tree_logprobs_entropy":
+        roof = {"bound": "hbm", "achieved": lp_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": lp_gbs / peaks["hbm_gbs"], "traffic": None}
+    elif dominant == "tpa_tree_attn_bwd":
+        roof = {"bound": "tensor", "achieved": bwd_tflops, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": bwd_tflops / peak_sus, "traffic": None}
+    else:
+        roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": fwd_tflops / peak_sus, "traffic": None}
+    roof.update({"kernel": dominant, "peak_kind": f"{peak_kind} bf16 sustained" if roof["unit"] == "TFLOP/s"
+                 else f"{peak_kind} HBM copy", "algorithmic_per_launch":
+                 (10.0 * pairs * d * Hq if dominant == "tpa_tree_attn_bwd" else
+                  flops_fwd if dominant == "tpa_tree_attn_fwd" else lp_bytes)})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = cpu_oracle_run(1, 0, args.oracle_pairs)
+        cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+
+    value = world * flops_step / (ms_step / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n_trees": B, "tree_tokens": rows, "original_tokens": int(N),
+                   "tree_token_ratio": info.tree_token_ratio, "ancestor_pairs": pairs,
+                   "flops_per_step": flops_step, "l2": "inputs larger than L2 (129 MB); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tree_tokens_per_s": world * rows / (ms_step / 1e3),
+        "frac_of_bf16_peak": value / peak_sus,
+        "breakdown_ms": {"block_classify": t_cls, "attn_fwd": t_fwd, "attn_bwd": t_bwd, "logprobs_entropy": t_lp},
+        "attn_fwd_bwd_tflops": attn_tflops, "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
+        "logprobs_gbs": lp_gbs, "logprobs_frac_hbm": lp_gbs / peaks["hbm_gbs"],
+        "roofline": roof, "clocks": clocks, "gpu_launches": n_launch_per_step * args.steps,
+        "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-pairs", type=int, default=600000,
+                    help="ancestor pairs in the oracle's bounded sample")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    rank, world, local = _dist()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" and torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -201,10 +201,14 @@ int tpa_tree_attn_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
                       int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
                       float softmax_scale, void* stream);
 
-/* Workspace bytes needed by tpa_tree_attn_bwd: an fp32 dQ accumulator
- * [B, T_pad, Hq, d] and fp32 D = rowsum(dO * O) [B, Hq, T_pad]. */
+/* Gradient output types of tpa_tree_attn_bwd. */
+enum { TPA_GRAD_F32 = 0, TPA_GRAD_BF16 = 1 };
+
+/* Workspace bytes needed by tpa_tree_attn_bwd: fp32 D = rowsum(dO * O)
+ * [B, Hq, T_pad], plus, for TPA_GRAD_BF16 only, an fp32 dQ accumulator
+ * [B, T_pad, Hq, d].  0 on invalid arguments. */
 uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32_t n_heads_q,
-                                           int32_t head_dim);
+                                           int32_t head_dim, int32_t grad_dtype);
 
 /*
  * tpa_tree_attn_bwd — gradients of <dO, O> for the forward above:
@@ -214,9 +218,14 @@ uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32
  * dK/dV summed over the query heads of each key/value head.
  *   q, k, v, o, lse: as produced for / by tpa_tree_attn_fwd (o, lse read)
  *   dout [B, T_pad, Hq, d] bf16 (pad rows read, must be finite)
- *   dq [B, T_pad, Hq, d], dk, dv [B, T_pad, Hkv, d] bf16 (written; pad rows 0)
+ *   dq [B, T_pad, Hq, d], dk, dv [B, T_pad, Hkv, d] (written; pad rows 0), fp32 for
+ *     grad_dtype = TPA_GRAD_F32 or bf16 for TPA_GRAD_BF16.  Accumulation is fp32
+ *     either way; fp32 outputs keep gradients of magnitude >= 8 within 2e-2 of
+ *     the exact values, which a bf16 output (spacing 0.0625 there) cannot.
  *   workspace: device buffer of tpa_tree_attn_bwd_workspace_bytes() bytes,
  *     256-byte aligned, contents overwritten
+ * dQ is accumulated across key tiles with fp32 atomics, so its last bits may
+ * differ between runs; dK and dV are deterministic.
  * Errors: as tpa_tree_attn_fwd, plus TPA_ERR_BUFFER_TOO_SMALL.
  */
 int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
@@ -224,7 +233,7 @@ int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
                       void* workspace, uint64_t workspace_bytes,
                       int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
-                      float softmax_scale, void* stream);
+                      float softmax_scale, int32_t grad_dtype, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Log-probabilities and entropy (tree training page, §对数概率计算): labels

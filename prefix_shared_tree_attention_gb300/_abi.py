@@ -14,6 +14,7 @@ STATUS = {
 }
 BLOCK_SIZE = 128
 LOGITS_COMPACT, LOGITS_PADDED = 0, 1
+GRAD_F32, GRAD_BF16 = 0, 1
 
 _i32p = C.POINTER(C.c_int32)
 _i64p = C.POINTER(C.c_int64)
@@ -60,11 +61,12 @@ PROTOTYPES = {
     "tpa_tree_attn_fwd": (C.c_int, [C.POINTER(TreeView), C.POINTER(BlockMaskView), C.c_void_p, C.c_void_p,
                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
                                     C.c_float, C.c_void_p]),
-    "tpa_tree_attn_bwd_workspace_bytes": (C.c_uint64, [C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "tpa_tree_attn_bwd_workspace_bytes": (C.c_uint64, [C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                                       C.c_int32]),
     "tpa_tree_attn_bwd": (C.c_int, [C.POINTER(TreeView), C.POINTER(BlockMaskView), C.c_void_p, C.c_void_p,
                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                     C.c_void_p, C.c_void_p, C.c_uint64, C.c_int32, C.c_int32, C.c_int32,
-                                    C.c_float, C.c_void_p]),
+                                    C.c_float, C.c_int32, C.c_void_p]),
     "tpa_tree_logprobs_entropy": (C.c_int, [C.POINTER(TreeView), C.c_void_p, C.c_int64, C.c_int32, C.c_int32,
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "tpa_sync_status": (C.c_int, [C.c_void_p]),

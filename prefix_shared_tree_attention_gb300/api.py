@@ -9,7 +9,8 @@ from typing import Sequence
 import numpy as np
 import torch
 
-from ._abi import (LOGITS_COMPACT, LOGITS_PADDED, BlockMaskView, TreeInfo, TreeView, check, lib)
+from ._abi import (GRAD_BF16, GRAD_F32, LOGITS_COMPACT, LOGITS_PADDED, BlockMaskView, TreeInfo, TreeView,
+                   check, lib)
 
 
 def _stream_ptr(stream) -> int:
@@ -195,25 +196,36 @@ def tree_attn_fwd(dtree: DeviceTree, mask: BlockMask, q: torch.Tensor, k: torch.
     return o, lse
 
 
-def tree_attn_bwd_workspace_bytes(n_trees: int, t_pad: int, n_heads_q: int, head_dim: int) -> int:
-    return int(lib().tpa_tree_attn_bwd_workspace_bytes(n_trees, t_pad, n_heads_q, head_dim))
+_GRAD = {torch.float32: GRAD_F32, torch.bfloat16: GRAD_BF16}
+
+
+def tree_attn_bwd_workspace_bytes(n_trees: int, t_pad: int, n_heads_q: int, head_dim: int,
+                                  grad_dtype: torch.dtype = torch.float32) -> int:
+    return int(lib().tpa_tree_attn_bwd_workspace_bytes(n_trees, t_pad, n_heads_q, head_dim, _GRAD[grad_dtype]))
 
 
 def tree_attn_bwd(dtree: DeviceTree, mask: BlockMask, q, k, v, o, lse, dout,
                   softmax_scale: float | None = None, workspace: torch.Tensor | None = None,
-                  out: tuple | None = None, stream=None):
-    """Tree attention backward: returns dQ, dK, dV (bf16, shaped like q, k, v)."""
+                  out: tuple | None = None, grad_dtype: torch.dtype = torch.float32, stream=None):
+    """Tree attention backward: returns dQ, dK, dV shaped like q, k, v, in
+    ``grad_dtype`` (fp32 by default, or bf16)."""
     B, T, Hq, Hkv, d = _check_qkv(dtree, q, k, v)
     if dout.shape != q.shape or dout.dtype != torch.bfloat16 or not dout.is_contiguous():
         raise ValueError("dout must be a contiguous bf16 tensor shaped like q")
-    nbytes = tree_attn_bwd_workspace_bytes(B, T, Hq, d)
+    if grad_dtype not in _GRAD:
+        raise ValueError("grad_dtype must be torch.float32 or torch.bfloat16")
     if workspace is None:
+        nbytes = tree_attn_bwd_workspace_bytes(B, T, Hq, d, grad_dtype)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    if out is None:
+        out = tuple(torch.empty(x.shape, dtype=grad_dtype, device=x.device) for x in (q, k, v))
+    dq, dk, dv = out
+    if not all(x.dtype == grad_dtype and x.is_contiguous() for x in out):
+        raise ValueError("gradient buffers must be contiguous and of grad_dtype")
     check("tpa_tree_attn_bwd", lib().tpa_tree_attn_bwd(
         C.byref(dtree.view), C.byref(mask.view), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
         lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-        workspace.numel(), Hq, Hkv, d, float(softmax_scale or 0.0), _stream_ptr(stream)))
+        workspace.numel(), Hq, Hkv, d, float(softmax_scale or 0.0), _GRAD[grad_dtype], _stream_ptr(stream)))
     return dq, dk, dv
 
 

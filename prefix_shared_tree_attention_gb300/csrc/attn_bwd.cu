@@ -8,9 +8,10 @@
 // with dK/dV summed over the query heads of each key/value head.
 //
 // Kernels: (1) preprocess: D = rowsum(dO * O) in fp32 and a zeroed fp32 dQ
-// accumulator; (2) main: one CTA per (key tile, kv head, tree) walks the
-// non-empty query tiles of its key tile (per-key-block CSR) for every query
-// head of the group; (3) dQ accumulator -> bf16.
+// accumulator (the caller's dQ buffer itself for fp32 gradients); (2) main:
+// one CTA per (key tile, kv head, tree) walks the non-empty query tiles of
+// its key tile (per-key-block CSR) for every query head of the group;
+// (3) bf16 gradients only: dQ accumulator -> bf16.
 //
 // Main-kernel roles (192 threads):
 //   warp 4  TMA producer: K, V once; per step Q, dO (+ LSE, D rows);
@@ -44,9 +45,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdParams {
   const float* lse;     // [B, Hq, T]
   const float* dvec;    // D, [B, Hq, T]
-  float* dq_acc;        // [B, T, Hq, d] fp32
-  __nv_bfloat16* dk;    // [B, T, Hkv, d]
-  __nv_bfloat16* dv;
+  float* dq_acc;        // [B, T, Hq, d] fp32 (the dQ output itself when gradients are fp32)
+  void* dk;             // [B, T, Hkv, d], fp32 or bf16
+  void* dv;
   const int32_t* subtree_end;
   const int32_t* n_tokens;
   const int32_t* k_ptr;
@@ -79,7 +80,7 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-template <int D>
+template <int D, bool F32OUT>
 __global__ void __launch_bounds__(192, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -290,14 +291,33 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_arrive(tmem_free);
     }
     // dK, dV rows of this key tile
-    __nv_bfloat16* dk_row = p.dk + (int64_t(krow + r) * p.hkv + g) * D;
-    __nv_bfloat16* dv_row = p.dv + (int64_t(krow + r) * p.hkv + g) * D;
+    constexpr int ESZ = F32OUT ? 4 : 2;
+    uint8_t* dk_row = static_cast<uint8_t*>(p.dk) + (int64_t(krow + r) * p.hkv + g) * D * ESZ;
+    uint8_t* dv_row = static_cast<uint8_t*>(p.dv) + (int64_t(krow + r) * p.hkv + g) * D * ESZ;
     if (n_steps == 0) {
       const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int c = 0; c < D * ESZ / 16; ++c) {
         reinterpret_cast<uint4*>(dk_row)[c] = z;
         reinterpret_cast<uint4*>(dv_row)[c] = z;
+      }
+    } else if (ok && F32OUT) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t vv[32], kk[32];
+        tc::tmem_ld32(tmem + lane_base + 256 + c * 32, vv);
+        tc::tmem_ld32(tmem + lane_base + 256 + D + c * 32, kk);
+        tc::tmem_ld_wait();
+        uint4* dV4 = reinterpret_cast<uint4*>(dv_row + c * 128);
+        uint4* dK4 = reinterpret_cast<uint4*>(dk_row + c * 128);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          dV4[t] = make_uint4(vv[4 * t], vv[4 * t + 1], vv[4 * t + 2], vv[4 * t + 3]);
+          dK4[t] = make_uint4(__float_as_uint(__uint_as_float(kk[4 * t]) * p.scale),
+                              __float_as_uint(__uint_as_float(kk[4 * t + 1]) * p.scale),
+                              __float_as_uint(__uint_as_float(kk[4 * t + 2]) * p.scale),
+                              __float_as_uint(__uint_as_float(kk[4 * t + 3]) * p.scale));
+        }
       }
     } else if (ok) {
 #pragma unroll
@@ -312,8 +332,8 @@ __global__ void __launch_bounds__(192, 1)
           wv[u] = tc::pack_bf16(__uint_as_float(vv[2 * u]), __uint_as_float(vv[2 * u + 1]));
           wk[u] = tc::pack_bf16(__uint_as_float(kk[2 * u]) * p.scale, __uint_as_float(kk[2 * u + 1]) * p.scale);
         }
-        uint4* dV4 = reinterpret_cast<uint4*>(dv_row + c * 32);
-        uint4* dK4 = reinterpret_cast<uint4*>(dk_row + c * 32);
+        uint4* dV4 = reinterpret_cast<uint4*>(dv_row + c * 64);
+        uint4* dK4 = reinterpret_cast<uint4*>(dk_row + c * 64);
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           dV4[t] = make_uint4(wv[4 * t], wv[4 * t + 1], wv[4 * t + 2], wv[4 * t + 3]);
@@ -382,13 +402,15 @@ int grid_for(int64_t work, int per_block) {
   return int(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
-template <int D>
+template <int D, bool F32OUT>
 int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const void* q, const void* k,
                const void* v, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                void* dv, void* ws, int hq, int hkv, float scale, cudaStream_t st) {
   const int64_t rows = int64_t(tree->n_trees) * tree->t_pad;
-  float* dq_acc = static_cast<float*>(ws);
-  float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(uint64_t(rows) * hq * D * 4));
+  // workspace: D [B, Hq, T] fp32, then (bf16 gradients only) the fp32 dQ accumulator
+  float* dvec = static_cast<float*>(ws);
+  float* dq_acc = F32OUT ? static_cast<float*>(dq)
+                         : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(uint64_t(rows) * hq * 4));
   const int64_t n_rows = rows * hq;
   bwd_pre_kernel<D><<<grid_for(n_rows * 32, 256), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), tree->n_tokens,
@@ -403,8 +425,8 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.lse = lse;
   prm.dvec = dvec;
   prm.dq_acc = dq_acc;
-  prm.dk = static_cast<__nv_bfloat16*>(dk);
-  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.dk = dk;
+  prm.dv = dv;
   prm.subtree_end = tree->subtree_end;
   prm.n_tokens = tree->n_tokens;
   prm.k_ptr = mask->k_ptr;
@@ -417,9 +439,10 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   const uint32_t smem = BwdCfg<D>::BYTES;
-  TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  attn_bwd_kernel<D><<<dim3(mask->n_blk, hkv, tree->n_trees), 192, smem, st>>>(tq, tk, tv, tdo, prm);
+  TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  attn_bwd_kernel<D, F32OUT><<<dim3(mask->n_blk, hkv, tree->n_trees), 192, smem, st>>>(tq, tk, tv, tdo, prm);
   TPA_CUDA_TRY(cudaGetLastError());
+  if (F32OUT) return TPA_OK;
 
   const int64_t n8 = n_rows * D / 8;
   dq_convert_kernel<<<grid_for(n8, 256), 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
@@ -432,17 +455,19 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
 TPA_DEFINE_STATUS_READER(tpa_internal_status_bwd, g_status_bwd)
 
 extern "C" uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32_t n_heads_q,
-                                                      int32_t head_dim) {
+                                                      int32_t head_dim, int32_t grad_dtype) {
   if (n_trees < 1 || t_pad < 1 || n_heads_q < 1 || head_dim < 1) return 0;
+  if (grad_dtype != TPA_GRAD_F32 && grad_dtype != TPA_GRAD_BF16) return 0;
   const uint64_t rows = uint64_t(n_trees) * uint64_t(t_pad);
-  return align256(rows * n_heads_q * head_dim * 4) + align256(rows * n_heads_q * 4);
+  const uint64_t dvec = align256(rows * n_heads_q * 4);
+  return grad_dtype == TPA_GRAD_F32 ? dvec : dvec + align256(rows * n_heads_q * head_dim * 4);
 }
 
 extern "C" int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const void* q,
                                  const void* k, const void* v, const void* o, const float* lse,
                                  const void* dout, void* dq, void* dk, void* dv, void* workspace,
                                  uint64_t workspace_bytes, int32_t n_heads_q, int32_t n_heads_kv,
-                                 int32_t head_dim, float softmax_scale, void* stream) {
+                                 int32_t head_dim, float softmax_scale, int32_t grad_dtype, void* stream) {
   const int rc = tpa_internal_check_attn_args(tree, mask, n_heads_q, n_heads_kv, head_dim);
   if (rc != TPA_OK) return rc;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return TPA_ERR_INVALID_ARG;
@@ -452,13 +477,15 @@ extern "C" int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_
                        reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
                        reinterpret_cast<uintptr_t>(lse);
   if ((al & 15) || (reinterpret_cast<uintptr_t>(workspace) & 255)) return TPA_ERR_INVALID_ARG;
-  if (workspace_bytes < tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, head_dim))
+  if (grad_dtype != TPA_GRAD_F32 && grad_dtype != TPA_GRAD_BF16) return TPA_ERR_INVALID_ARG;
+  if (workspace_bytes <
+      tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, head_dim, grad_dtype))
     return TPA_ERR_BUFFER_TOO_SMALL;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(float(head_dim));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return head_dim == 128
-             ? launch_bwd<128>(tree, mask, q, k, v, o, lse, dout, dq, dk, dv, workspace, n_heads_q, n_heads_kv,
-                               scale, st)
-             : launch_bwd<64>(tree, mask, q, k, v, o, lse, dout, dq, dk, dv, workspace, n_heads_q, n_heads_kv,
-                              scale, st);
+  const bool f32 = grad_dtype == TPA_GRAD_F32;
+#define TPA_BWD_ARGS tree, mask, q, k, v, o, lse, dout, dq, dk, dv, workspace, n_heads_q, n_heads_kv, scale, st
+  if (head_dim == 128) return f32 ? launch_bwd<128, true>(TPA_BWD_ARGS) : launch_bwd<128, false>(TPA_BWD_ARGS);
+  return f32 ? launch_bwd<64, true>(TPA_BWD_ARGS) : launch_bwd<64, false>(TPA_BWD_ARGS);
+#undef TPA_BWD_ARGS
 }

@@ -28,6 +28,23 @@ def assert_attn_close(got: torch.Tensor, ref: torch.Tensor, what: str,
     return err, rel
 
 
+def bf16_half_ulp(x: torch.Tensor) -> torch.Tensor:
+    """Half the bf16 spacing at |x|: the least error any bf16 output of x has."""
+    ax = x.abs().clamp_min(2.0 ** -126)
+    return torch.exp2(torch.floor(torch.log2(ax)) - 8)
+
+
+def assert_attn_close_bf16_out(got: torch.Tensor, ref: torch.Tensor, what: str) -> None:
+    """Bound for bf16-valued outputs: the stated max-abs plus the rounding to
+    bf16 that the output type itself forces, element by element."""
+    g = got.detach().to("cpu", torch.float64)
+    r = ref.detach().to("cpu", torch.float64)
+    assert torch.isfinite(g).all(), f"{what}: non-finite values"
+    excess = ((g - r).abs() - (ATTN_MAX_ABS + bf16_half_ulp(r))).max().item()
+    rel = (g - r).norm().item() / max(r.norm().item(), 1e-30)
+    assert excess <= 0 and rel <= ATTN_REL_L2, f"{what}: excess {excess:.3e}, rel-L2 {rel:.3e}"
+
+
 def pack_and_upload(tpa, seqs, mb, device="cuda"):
     tree = tpa.tree_pack(seqs, mb)
     dtree = tree.upload(device)

@@ -13,7 +13,7 @@ import torch
 import oracle
 from oracle.mask import block_classes, block_csr
 from synth import CONFIGS, make_logits, random_small_sequences
-from _pipeline import (LOGP_ABS, assert_attn_close, leaf_nodes, node_rows, pack_and_upload,
+from _pipeline import (LOGP_ABS, assert_attn_close, assert_attn_close_bf16_out, leaf_nodes, node_rows, pack_and_upload,
                        random_inputs, workload, workload_tensors)
 
 pytestmark = pytest.mark.gpu
@@ -101,6 +101,27 @@ def test_attention_small(tpa, case):
     rng = np.random.default_rng(500 + seed)
     seqs = random_small_sequences(rng, n, L, V, min_len=1)
     _run_full_case(tpa, seqs, T, hq, hkv, d, seed)
+
+
+def test_attention_bf16_gradients(tpa):
+    rng = np.random.default_rng(501)
+    seqs = random_small_sequences(rng, 8, 300, 4, min_len=1)
+    T = 512
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    (q, k, v, do), (qc, kc, vc, doc) = random_inputs(tree.n_trees, T, 4, 2, 64, 1)
+    o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, grad_dtype=torch.bfloat16)
+    f32 = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do)
+    tpa.sync_status()
+    assert dq.dtype == torch.bfloat16 and dk.dtype == torch.bfloat16
+    for b, t in enumerate(pk.trees):
+        dQ, dK, dV = oracle.attn_backward(t, qc[b], kc[b], vc[b], doc[b], t_pad=T)
+        assert_attn_close_bf16_out(dq[b], dQ, f"bf16 dQ tree {b}")
+        assert_attn_close_bf16_out(dk[b], dK, f"bf16 dK tree {b}")
+        assert_attn_close_bf16_out(dv[b], dV, f"bf16 dV tree {b}")
+    # the bf16 outputs are the fp32 ones rounded (same accumulation)
+    assert torch.equal(dk, f32[1].to(torch.bfloat16)) and torch.equal(dv, f32[2].to(torch.bfloat16))
 
 
 def test_attention_single_chain_minimal(tpa):
@@ -261,6 +282,12 @@ def test_invalid_arguments(tpa):
     o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(tpa.TpaError) as e:
-        tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=small)
+        tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=small, grad_dtype=torch.bfloat16)
     assert e.value.name == "TPA_ERR_BUFFER_TOO_SMALL"
+    dq, dk, dv = (torch.empty(x.shape, dtype=torch.float32, device="cuda") for x in (q, k, v))
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    rc = L.tpa_tree_attn_bwd(C.byref(dtree.view), C.byref(mask.view), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                             o.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                             dv.data_ptr(), ws.data_ptr(), ws.numel(), 4, 2, 64, 0.0, 5, None)
+    assert rc == -1  # unknown gradient dtype
     tpa.sync_status()
