@@ -213,8 +213,16 @@ def run_gpu(args, rank, world, local):
     T, Hq, Hkv, d, V = cfg.max_tokens_per_mb, cfg.n_heads_q, cfg.n_heads_kv, cfg.head_dim, lcfg.logits_vocab
 
     tree = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
+    if args.max_trees and tree.n_trees > args.max_trees:
+        # profiling: keep only the sequences of the first trees and repack them
+        keep = tree.arrays()["seq_tree"] < args.max_trees
+        seqs = [s for s, kp in zip(seqs, keep) if kp]
+        toks, offs = flatten_sequences(seqs)
+        tree = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
     info = tree.info
     B = info.n_trees
+    run_attn = args.only in ("all", "attn")
+    run_lp = args.only in ("all", "logprobs")
     rows = info.total_tree_tokens
     pairs = int(info.ancestor_pairs)
     flops_fwd = 4.0 * pairs * d * Hq
@@ -225,7 +233,7 @@ def run_gpu(args, rank, world, local):
     qh, kh, vh = make_qkv(2, B, T, Hq, Hkv, d)
     doh = make_dout(2, B, T, Hq, d)
     q, k, v, do = (x.to(dev) for x in (qh, kh, vh, doh))
-    logits = make_logits(4, rows, V, device=str(dev))
+    logits = make_logits(4, rows, V, device=str(dev)) if run_lp else None
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty(x.shape, dtype=torch.float32, device=dev) for x in (q, k, v))
@@ -240,11 +248,14 @@ def run_gpu(args, rank, world, local):
         if ev: ev[0].record(stream)
         tpa.block_classify(dtree, out=mask)
         if ev: ev[1].record(stream)
-        tpa.tree_attn_fwd(dtree, mask, q, k, v, out=o, lse=lse)
+        if run_attn:
+            tpa.tree_attn_fwd(dtree, mask, q, k, v, out=o, lse=lse)
         if ev: ev[2].record(stream)
-        tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv))
+        if run_attn:
+            tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv))
         if ev: ev[3].record(stream)
-        tpa.tree_logprobs_entropy(dtree, logits, out=lp_out)
+        if run_lp:
+            tpa.tree_logprobs_entropy(dtree, logits, out=lp_out)
         if ev: ev[4].record(stream)
 
     for _ in range(args.warmup):
@@ -278,7 +289,7 @@ def run_gpu(args, rank, world, local):
 
     # ------------------------------------------------ end to end from host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.only == "all":
         pin = lambda x: x.pin_memory()
         qp, kp, vp, dop = pin(qh), pin(kh), pin(vh), pin(doh)
         lg_host = torch.empty((rows, V), dtype=torch.bfloat16, pin_memory=True)
@@ -328,11 +339,12 @@ def run_gpu(args, rank, world, local):
 
     peaks, peak_kind = _peaks()
     peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    attn_tflops = (flops_step / 1e12) / ((t_fwd + t_bwd) / 1e3)
-    bwd_tflops = (10.0 * pairs * d * Hq / 1e12) / (t_bwd / 1e3)
-    fwd_tflops = (flops_fwd / 1e12) / (t_fwd / 1e3)
+    rate = lambda work, ms: work / (ms / 1e3) if ms > 1e-6 else 0.0
+    attn_tflops = rate(flops_step / 1e12, t_fwd + t_bwd)
+    bwd_tflops = rate(10.0 * pairs * d * Hq / 1e12, t_bwd)
+    fwd_tflops = rate(flops_fwd / 1e12, t_fwd)
     lp_bytes = rows * V * 2 + 4 * 4 * B * T + 8 * N
-    lp_gbs = lp_bytes / (t_lp / 1e3) / 1e9
+    lp_gbs = rate(lp_bytes / 1e9, t_lp)
     dominant = max((("tpa_tree_attn_bwd", t_bwd), ("tpa_tree_attn_fwd", t_fwd), ("tpa_tree_logprobs_entropy", t_lp)),
                    key=lambda x: x[1])[0]
     if dominant == "tpa_tree_logprobs_entropy":
@@ -350,7 +362,7 @@ def run_gpu(args, rank, world, local):
                   flops_fwd if dominant == "tpa_tree_attn_fwd" else lp_bytes)})
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
         r = cpu_oracle_run(1, 0, args.oracle_pairs)
         cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
 
@@ -378,14 +390,18 @@ def run_gpu(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--oracle-pairs", type=int, default=600000,
+    ap.add_argument("--oracle-pairs", type=int, default=15000000,
                     help="ancestor pairs in the oracle's bounded sample")
+    ap.add_argument("--only", choices=["all", "attn", "logprobs"], default="all",
+                    help="profiling aid: run only part of the step (no e2e / CPU baseline then)")
+    ap.add_argument("--max-trees", type=int, default=0,
+                    help="profiling aid: keep only the sequences of the first N trees")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
