@@ -235,6 +235,38 @@ int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
                       int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
                       float softmax_scale, int32_t grad_dtype, void* stream);
 
+/*
+ * tpa_tree_attn_bwd_noalloc — tpa_tree_attn_bwd for callers that cannot
+ * provide a device workspace.  The tree-training pages have no counterpart;
+ * this is a deployment variant.  Runtimes that reserve the whole device for
+ * their own memory pool (and forbid further cudaMalloc calls), or plain-C
+ * callers with no allocator at hand, cannot hand the library a workspace, so
+ * this call takes its scratch from a fixed 16 MiB array compiled into the
+ * library instead.  Every GPU that loads the library holds that array until
+ * the process exits.
+ *   Arguments: as tpa_tree_attn_bwd, without workspace / workspace_bytes.
+ *   Limit: the scratch of tpa_tree_attn_bwd_workspace_bytes() must fit in
+ *     16 MiB: B * T_pad * Hq * 4 bytes for TPA_GRAD_F32 (e.g. 8 trees of
+ *     8192 tokens with 64 query heads), plus B * T_pad * Hq * d * 4 for
+ *     TPA_GRAD_BF16.  Larger problems return TPA_ERR_BUFFER_TOO_SMALL and
+ *     enqueue nothing.
+ *   Allocation: none (no cudaMalloc, no cudaFree, no allocating library call).
+ *   Set-up: the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *     call's contents (each call rewrites all of the scratch it reads, so
+ *     nothing carries over).  Calls that overlap on the GPU — on different
+ *     streams, or from several host threads without ordering — race on it and
+ *     must be serialised by the caller.
+ * Errors: as tpa_tree_attn_bwd.
+ */
+int tpa_tree_attn_bwd_noalloc(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
+                              const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
+                              float softmax_scale, int32_t grad_dtype, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Log-probabilities and entropy (tree training page, §对数概率计算): labels
  * cannot come from rolling input_ids; each tree row is processed once (the

@@ -67,6 +67,10 @@ PROTOTYPES = {
                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                     C.c_void_p, C.c_void_p, C.c_uint64, C.c_int32, C.c_int32, C.c_int32,
                                     C.c_float, C.c_int32, C.c_void_p]),
+    "tpa_tree_attn_bwd_noalloc": (C.c_int, [C.POINTER(TreeView), C.POINTER(BlockMaskView), C.c_void_p,
+                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                                            C.c_int32, C.c_float, C.c_int32, C.c_void_p]),
     "tpa_tree_logprobs_entropy": (C.c_int, [C.POINTER(TreeView), C.c_void_p, C.c_int64, C.c_int32, C.c_int32,
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "tpa_sync_status": (C.c_int, [C.c_void_p]),

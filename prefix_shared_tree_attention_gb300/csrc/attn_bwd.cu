@@ -489,3 +489,68 @@ extern "C" int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_
   return f32 ? launch_bwd<64, true>(TPA_BWD_ARGS) : launch_bwd<64, false>(TPA_BWD_ARGS);
 #undef TPA_BWD_ARGS
 }
+
+// ---------------------------------------------------------------------------
+// Backward without a caller-provided workspace.
+//
+// Some callers cannot hand the library a device workspace: runtimes that
+// reserve the whole device for their own pool and forbid further cudaMalloc
+// calls, or plain-C integrations that have no allocator to draw from.  For
+// them the backward's scratch (D = rowsum(dO * O), and the fp32 dQ
+// accumulator when bf16 gradients are requested) lives in one fixed array
+// compiled into this library.  Every GPU that loads the library keeps that
+// array until the process exits.  Problems whose scratch does not fit are
+// rejected with TPA_ERR_BUFFER_TOO_SMALL before any work is enqueued.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr uint64_t kNoAllocScratchBytes = 16ull << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The host-side
+// name of a __device__ array is only a stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TPA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return TPA_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return TPA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TPA_OK;
+}
+
+}  // namespace
+
+extern "C" int tpa_tree_attn_bwd_noalloc(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
+                                         const void* q, const void* k, const void* v, const void* o,
+                                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                         int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
+                                         float softmax_scale, int32_t grad_dtype, void* stream) {
+  if (!tree) return TPA_ERR_INVALID_ARG;
+  const uint64_t need =
+      tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, head_dim, grad_dtype);
+  if (need == 0) return TPA_ERR_INVALID_ARG;
+  if (need > kNoAllocScratchBytes) return TPA_ERR_BUFFER_TOO_SMALL;
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != TPA_OK) return rc;
+  return tpa_tree_attn_bwd(tree, mask, q, k, v, o, lse, dout, dq, dk, dv, scratch, kNoAllocScratchBytes,
+                           n_heads_q, n_heads_kv, head_dim, softmax_scale, grad_dtype, stream);
+}
