@@ -160,6 +160,9 @@ typedef struct {
   int32_t* q_idx;             /* [B][cap] entries 2*kb + (FULL ? 1 : 0), ascending kb */
   int32_t* k_ptr;             /* [B][n_blk+1] CSR by key block */
   int32_t* k_idx;             /* [B][cap] entries 2*qb + (FULL ? 1 : 0), ascending qb */
+  uint32_t* qmask;            /* [B][cap][128][4] for each PARTIAL entry e of q_idx: row r holds the
+                                 visibility bits of query qb*128 + r (bit c of word c/32 = key
+                                 kb*128 + c visible); FULL entries' rows are not written */
 } tpa_blockmask_view;
 
 /* Bytes of one device buffer holding a block mask for (n_trees, t_pad). */

@@ -143,6 +143,7 @@ class BlockMask:
             "q_idx": self._slice(v.q_idx, 4 * B * cap, torch.int32, (B, cap)),
             "k_ptr": self._slice(v.k_ptr, 4 * B * (n + 1), torch.int32, (B, n + 1)),
             "k_idx": self._slice(v.k_idx, 4 * B * cap, torch.int32, (B, cap)),
+            "qmask": self._slice(v.qmask, 2048 * B * cap, torch.int32, (B, cap, 128, 4)),
         }
 
 

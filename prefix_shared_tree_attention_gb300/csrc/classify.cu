@@ -8,7 +8,9 @@
 // q0 = 128 qb, q1 = q0 + 127; the tile is EMPTY when cnt = 0, FULL when
 // cnt = 128 * 128 and PARTIAL otherwise.  Two CSR lists follow: per query
 // block its non-empty key blocks (forward), per key block its non-empty
-// query blocks (backward), each entry 2 * block + (FULL ? 1 : 0).
+// query blocks (backward), each entry 2 * block + (FULL ? 1 : 0).  A third
+// kernel writes, for every PARTIAL entry of the per-query-block list, the
+// 128x128 visibility bits the forward applies (one 16-byte row per query).
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -96,6 +98,38 @@ __global__ void __launch_bounds__(1024) csr_kernel(const uint8_t* __restrict__ c
   }
 }
 
+// grid (n_blk, B), 128 threads: for every PARTIAL entry of query block qb's
+// CSR row, thread r writes the 128-bit visibility row of query qb*128 + r:
+// bit c of word c/32 is set iff key kb*128 + c is visible (j <= i <= E[j]).
+__global__ void __launch_bounds__(128) qmask_kernel(const int32_t* __restrict__ subtree_end,
+                                                     const int32_t* __restrict__ n_tokens, int32_t t_pad,
+                                                     int32_t n_blk, int32_t cap,
+                                                     const int32_t* __restrict__ q_ptr,
+                                                     const int32_t* __restrict__ q_idx,
+                                                     uint4* __restrict__ qmask) {
+  __shared__ int e_s[kB];
+  const int b = blockIdx.y, qb = blockIdx.x, r = threadIdx.x;
+  const int n = n_tokens[b];
+  const int i = qb * kB + r;
+  const int32_t* ptr = q_ptr + int64_t(b) * (n_blk + 1);
+  for (int e = ptr[qb]; e < ptr[qb + 1]; ++e) {
+    const int ent = q_idx[int64_t(b) * cap + e];
+    if (ent & 1) continue;  // FULL: no mask needed (uniform across the CTA)
+    const int kb = ent >> 1;
+    __syncthreads();
+    const int jr = kb * kB + r;
+    e_s[r] = (jr < n) ? subtree_end[int64_t(b) * t_pad + jr] : -1;
+    __syncthreads();
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int c = 0; c < kB; ++c) {
+      const int j = kb * kB + c;
+      if (j <= i && i <= e_s[c]) w[c >> 5] |= 1u << (c & 31);
+    }
+    qmask[(int64_t(b) * cap + e) * kB + r] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace
 
 TPA_DEFINE_STATUS_READER(tpa_internal_status_classify, g_status_classify)
@@ -103,7 +137,7 @@ TPA_DEFINE_STATUS_READER(tpa_internal_status_classify, g_status_classify)
 extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
                                   void* stream) {
   if (!tree || !mask || !tree->subtree_end || !tree->n_tokens || !mask->cls || !mask->q_ptr ||
-      !mask->q_idx || !mask->k_ptr || !mask->k_idx)
+      !mask->q_idx || !mask->k_ptr || !mask->k_idx || !mask->qmask)
     return TPA_ERR_INVALID_ARG;
   if (tree->t_pad % kB || mask->n_blk != tree->t_pad / kB || mask->n_trees != tree->n_trees ||
       mask->n_blk > 1024 || tree->n_trees < 1)
@@ -116,6 +150,10 @@ extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask
   const int threads = n_blk <= 32 ? 32 : ((n_blk + 31) / 32) * 32;
   csr_kernel<<<dim3(tree->n_trees, 2), threads, 0, st>>>(mask->cls, n_blk, mask->cap, mask->q_ptr,
                                                          mask->q_idx, mask->k_ptr, mask->k_idx);
+  TPA_CUDA_TRY(cudaGetLastError());
+  qmask_kernel<<<dim3(n_blk, tree->n_trees), 128, 0, st>>>(tree->subtree_end, tree->n_tokens, tree->t_pad,
+                                                           n_blk, mask->cap, mask->q_ptr, mask->q_idx,
+                                                           reinterpret_cast<uint4*>(mask->qmask));
   TPA_CUDA_TRY(cudaGetLastError());
   return TPA_OK;
 }

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from oracle.mask import block_classes, block_csr
+from oracle.mask import _mask_rows, block_classes, block_csr
 from synth import CONFIGS, make_logits, random_small_sequences
 from _pipeline import (LOGP_ABS, assert_attn_close, assert_attn_close_bf16_out, leaf_nodes, node_rows, pack_and_upload,
                        random_inputs, workload, workload_tensors)
@@ -27,7 +27,7 @@ def tpa():
     return tpa
 
 
-def _check_mask(tpa, pk, mask, T):
+def _check_mask(tpa, pk, mask, T, check_bits=True):
     arr = {k: v.cpu().numpy() for k, v in mask.arrays().items()}
     for b, t in enumerate(pk.trees):
         cls = block_classes(t, T)
@@ -38,6 +38,22 @@ def _check_mask(tpa, pk, mask, T):
         assert np.array_equal(arr["q_idx"][b][:nq], csr["q_idx"])
         assert np.array_equal(arr["k_ptr"][b], csr["k_ptr"])
         assert np.array_equal(arr["k_idx"][b][:nq], csr["k_idx"])
+        if not check_bits:
+            continue
+        # visibility bits of every PARTIAL tile, from the oracle's parent-walk rows
+        for qb in range(T // 128):
+            if qb * 128 >= t.n:
+                break
+            rows = _mask_rows(t, qb * 128, qb * 128 + 128, T)
+            for e in range(csr["q_ptr"][qb], csr["q_ptr"][qb + 1]):
+                ent = int(csr["q_idx"][e])
+                if ent & 1:
+                    continue
+                kb = ent >> 1
+                tile = rows[:, kb * 128:(kb + 1) * 128].astype(np.uint64)
+                words = (tile.reshape(128, 4, 32) << np.arange(32, dtype=np.uint64)).sum(-1)
+                got = arr["qmask"][b, e].astype(np.int64) & 0xFFFFFFFF
+                assert np.array_equal(got, words.astype(np.int64)), f"tree {b} qb {qb} kb {kb} bits"
 
 
 # ---------------------------------------------------------------- block classes
@@ -57,7 +73,7 @@ def test_classify_workloads(tpa, cid):
     cfg, seqs = workload(cid)
     pk = oracle.tree_pack(seqs, cfg.max_tokens_per_mb)
     _, _, mask = pack_and_upload(tpa, seqs, cfg.max_tokens_per_mb)
-    _check_mask(tpa, pk, mask, cfg.max_tokens_per_mb)
+    _check_mask(tpa, pk, mask, cfg.max_tokens_per_mb, check_bits=cid in (1, 2))
 
 
 # ---------------------------------------------------------------- attention, full oracle
