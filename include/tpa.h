@@ -163,6 +163,9 @@ typedef struct {
   uint32_t* qmask;            /* [B][cap][128][4] for each PARTIAL entry e of q_idx: row r holds the
                                  visibility bits of query qb*128 + r (bit c of word c/32 = key
                                  kb*128 + c visible); FULL entries' rows are not written */
+  uint32_t* sched;            /* [16] work counters of the attention kernels: zeroed by
+                                 tpa_block_classify and left at zero by every attention call, so
+                                 attention calls that use the same mask must not overlap on the GPU */
 } tpa_blockmask_view;
 
 /* Bytes of one device buffer holding a block mask for (n_trees, t_pad). */
@@ -208,8 +211,8 @@ int tpa_tree_attn_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
 enum { TPA_GRAD_F32 = 0, TPA_GRAD_BF16 = 1 };
 
 /* Workspace bytes needed by tpa_tree_attn_bwd: fp32 D = rowsum(dO * O)
- * [B, Hq, T_pad], plus, for TPA_GRAD_BF16 only, an fp32 dQ accumulator
- * [B, T_pad, Hq, d].  0 on invalid arguments. */
+ * [B, Hq, T_pad] (the same for both gradient types).  0 on invalid
+ * arguments. */
 uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32_t n_heads_q,
                                            int32_t head_dim, int32_t grad_dtype);
 
@@ -227,8 +230,8 @@ uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32
  *     the exact values, which a bf16 output (spacing 0.0625 there) cannot.
  *   workspace: device buffer of tpa_tree_attn_bwd_workspace_bytes() bytes,
  *     256-byte aligned, contents overwritten
- * dQ is accumulated across key tiles with fp32 atomics, so its last bits may
- * differ between runs; dK and dV are deterministic.
+ * dK/dV (per key tile) and dQ (per query tile) are accumulated in tensor
+ * memory by separate kernels without atomics: results are deterministic.
  * Errors: as tpa_tree_attn_fwd, plus TPA_ERR_BUFFER_TOO_SMALL.
  */
 int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
@@ -249,10 +252,9 @@ int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
  * the process exits.
  *   Arguments: as tpa_tree_attn_bwd, without workspace / workspace_bytes.
  *   Limit: the scratch of tpa_tree_attn_bwd_workspace_bytes() must fit in
- *     16 MiB: B * T_pad * Hq * 4 bytes for TPA_GRAD_F32 (e.g. 8 trees of
- *     8192 tokens with 64 query heads), plus B * T_pad * Hq * d * 4 for
- *     TPA_GRAD_BF16.  Larger problems return TPA_ERR_BUFFER_TOO_SMALL and
- *     enqueue nothing.
+ *     16 MiB: B * T_pad * Hq * 4 bytes (e.g. 8 trees of 8192 tokens with 64
+ *     query heads, or one 65536-token tree with 64 query heads).  Larger
+ *     problems return TPA_ERR_BUFFER_TOO_SMALL and enqueue nothing.
  *   Allocation: none (no cudaMalloc, no cudaFree, no allocating library call).
  *   Set-up: the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress with that device current) and caches it; make that

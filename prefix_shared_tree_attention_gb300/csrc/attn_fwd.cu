@@ -7,9 +7,12 @@
 // classifier); PARTIAL tiles apply the precomputed 128-bit row masks, FULL
 // tiles apply nothing.
 //
-// One CTA = one 128-query tile of NH query heads that share a key/value head
-// (NH = 2 when the group size allows it), so every K/V tile is loaded once
-// for both heads and the mask is shared.  Warp roles:
+// Persistent kernel: one CTA per SM takes work items from a global counter
+// (heaviest first; one 128-query tile of
+// NH query heads that share a key/value head, NH = 2 when the group size
+// allows it), so K/V tiles are loaded once for both heads and the mask is
+// shared, and one item's fill and drain (Q load, first S, O epilogue) overlap
+// its neighbours'.  Barrier phases run on across items.  Warp roles:
 //   warpgroup h < NH  softmax of head h: thread r owns query row r (TMEM lane
 //                     r); fp32 online softmax in the log2 domain with packed
 //                     f32x2 arithmetic; P (bf16) goes to TMEM over the S
@@ -17,8 +20,8 @@
 //                     O is rescaled in TMEM only when the running max grows
 //                     by more than 2^8 (exact: numerator and denominator keep
 //                     the same stale max).
-//   warp 4*NH         TMA producer: Q of each head once, then K and V tiles
-//                     through separate rings.
+//   warp 4*NH         TMA producer: Q of each item, then K and V tiles through
+//                     separate rings.
 //   warp 4*NH+1       MMA issuer (one thread).  Per key tile j and head h:
 //                     PV_h(j) then S_h(j+1), so head B's softmax runs while
 //                     head A's MMAs run (ping-pong) and the tensor core always
@@ -48,11 +51,11 @@ constexpr uint32_t kSmemMax = 232448;      // 227 KB opt-in per CTA
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
-  const int32_t* n_tokens;
   const int32_t* q_ptr;
   const int32_t* q_idx;
   const uint4* qmask;
-  int32_t t_pad, n_blk, cap, hq, hkv;
+  uint32_t* sched;   // [0] next work item, [1] finished CTAs (both back to 0 at kernel end)
+  int32_t t_pad, n_blk, cap, hq, hkv, n_items;
   float scale_log2;  // softmax scale * log2(e)
 };
 
@@ -67,10 +70,11 @@ struct FwdCfg {
   static constexpr uint32_t OFF_K = OFF_Q + NH * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
   static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE;
-  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NH], p_full[NH], o_final, drain
-  static constexpr int NBAR = 1 + 4 * NS + 2 * NH + 2;
+  // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NH], p_full[NH],
+  // o_free[NH], o_final, drain, item_full[2], item_empty[2]
+  static constexpr int NBAR = 2 + 4 * NS + 3 * NH + 2 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;  // + alignment slack
   static constexpr int THREADS = 128 * NH + 64;
   static constexpr uint32_t TMEM_COLS = NH == 2 ? 512 : 256;
   static_assert(NS >= 1, "shared memory too small");
@@ -117,6 +121,24 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
   tc::tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(r + 32));
 }
 
+// Work item -> (tree, first query head, query block); deepest blocks first.
+struct Item {
+  int b, h0, qb, e0, n_it;
+};
+template <int NH>
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int it) {
+  Item r;
+  const int per_tree = p.n_blk * (p.hq / NH);
+  r.b = it / per_tree;
+  const int rem = it - r.b * per_tree;
+  r.h0 = (rem / p.n_blk) * NH;
+  r.qb = p.n_blk - 1 - rem % p.n_blk;
+  const int32_t* rp = p.q_ptr + r.b * (p.n_blk + 1);
+  r.e0 = rp[r.qb];
+  r.n_it = rp[r.qb + 1] - r.e0;
+  return r;
+}
+
 template <int D, int NH>
 __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -131,31 +153,29 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   uint8_t* sV = smem + C::OFF_V;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bar;
-  uint64_t* k_full = bar + 1;
-  uint64_t* k_empty = bar + 1 + NS;
-  uint64_t* v_full = bar + 1 + 2 * NS;
-  uint64_t* v_empty = bar + 1 + 3 * NS;
-  uint64_t* s_full = bar + 1 + 4 * NS;
-  uint64_t* p_full = bar + 1 + 4 * NS + NH;
-  uint64_t* o_final = bar + 1 + 4 * NS + 2 * NH;
+  uint64_t* q_empty = bar + 1;
+  uint64_t* k_full = bar + 2;
+  uint64_t* k_empty = k_full + NS;
+  uint64_t* v_full = k_empty + NS;
+  uint64_t* v_empty = v_full + NS;
+  uint64_t* s_full = v_empty + NS;
+  uint64_t* p_full = s_full + NH;
+  uint64_t* o_free = p_full + NH;
+  uint64_t* o_final = o_free + NH;
   uint64_t* drain = o_final + 1;
+  uint64_t* item_full = drain + 1;   // [2]
+  uint64_t* item_empty = drain + 3;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z;
-  const int h0 = blockIdx.y * NH;  // first query head of this CTA
-  const int qb = p.n_blk - 1 - blockIdx.x;  // deepest (usually heaviest) query blocks first
-  const int g = h0 / (p.hq / p.hkv);
-  const int32_t* rp = p.q_ptr + b * (p.n_blk + 1);
-  const int e0 = rp[qb];
-  const int n_it = rp[qb + 1] - e0;
-  const int32_t* list = p.q_idx + int64_t(b) * p.cap + e0;
-  const int row0 = b * p.t_pad + qb * kB;  // global row of the tile's first query
+  const int hkv_group = p.hq / p.hkv;
   constexpr int W_TMA = 4 * NH, W_MMA = 4 * NH + 1;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(k_full + s, 1);
       tc::mbar_init(k_empty + s, 1);
@@ -165,9 +185,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     for (int h = 0; h < NH; ++h) {
       tc::mbar_init(s_full + h, 1);
       tc::mbar_init(p_full + h, 128);
+      tc::mbar_init(o_free + h, 128);
     }
     tc::mbar_init(o_final, 1);
     tc::mbar_init(drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(item_full + s, 1);
+      tc::mbar_init(item_empty + s, 1 + 128 * NH);
+    }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -177,129 +202,197 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Issuer warps run converged (waits, counters and descriptors stay
+  // warp-uniform); the elected lane alone issues each copy, MMA and commit.
+  auto wait_u = [&](uint64_t* b_, uint32_t par) {
+    return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_fwd));
+  };
   if (warp == W_TMA) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_it > 0) {
+    if (tc::elect_one()) {
       tc::tma_prefetch_desc(&tm_q);
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
-      tc::mbar_arrive_expect_tx(q_full, NH * TILE);
-      for (int h = 0; h < NH; ++h)
-        for (int c = 0; c < NCH; ++c)
-          tc::tma_load_3d(sQ + h * TILE + c * kChunk, &tm_q, q_full, c * 64, h0 + h, row0);
+    }
+    __syncwarp();
+    int kt = 0, vt = 0, nq = 0;  // ring counters and non-empty items so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      // fetch the next work item and hand it to the other roles
+      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+      int it = 0;
+      if (lane == 0) it = int(atomicAdd(p.sched, 1u));
+      it = __shfl_sync(0xffffffffu, it, 0);
+      if (tc::elect_one()) {
+        item_ring[k & 1] = it < p.n_items ? it : -1;
+        tc::mbar_arrive(item_full + (k & 1));
+      }
+      __syncwarp();
+      if (it >= p.n_items) break;
+      const Item I = decode_item<NH>(p, it);
+      if (I.n_it == 0) continue;
+      const int32_t* list = p.q_idx + int64_t(I.b) * p.cap + I.e0;
+      const int g = I.h0 / hkv_group;
+      if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
+      if (tc::elect_one()) {
+        tc::mbar_arrive_expect_tx(q_full, NH * TILE);
+        for (int h = 0; h < NH; ++h)
+          for (int c = 0; c < NCH; ++c)
+            tc::tma_load_3d(sQ + h * TILE + c * kChunk, &tm_q, q_full, c * 64, I.h0 + h, I.b * p.t_pad + I.qb * kB);
+      }
+      __syncwarp();
       // K runs ahead of V by one tile: the MMA needs K(j+1) before V(j).
       int kj = 0, vj = 0;
-      bool ok = true;
-      while (ok && (kj < n_it || vj < n_it)) {
-        const bool do_k = kj < n_it && kj <= vj + 1;
+      while (kj < I.n_it || vj < I.n_it) {
+        const bool do_k = kj < I.n_it && kj <= vj + 1;
         const int j = do_k ? kj : vj;
-        const int s = j % NS;
-        const int krow = b * p.t_pad + (list[j] >> 1) * kB;
-        if (do_k) {
-          if (!(ok = tc::mbar_wait(k_empty + s, ((j / NS) & 1) ^ 1, abort_flag, &g_status_fwd))) break;
-          tc::mbar_arrive_expect_tx(k_full + s, TILE);
+        const int krow = I.b * p.t_pad + (list[j] >> 1) * kB;
+        const int gx = (do_k ? kt : vt) + j, s = gx % NS;
+        if (!(ok = wait_u((do_k ? k_empty : v_empty) + s, ((gx / NS) & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          uint64_t* fb = (do_k ? k_full : v_full) + s;
+          uint8_t* dst = (do_k ? sK : sV) + s * TILE;
+          tc::mbar_arrive_expect_tx(fb, TILE);
           for (int c = 0; c < NCH; ++c)
-            tc::tma_load_3d(sK + s * TILE + c * kChunk, &tm_k, k_full + s, c * 64, g, krow);
-          ++kj;
-        } else {
-          if (!(ok = tc::mbar_wait(v_empty + s, ((j / NS) & 1) ^ 1, abort_flag, &g_status_fwd))) break;
-          tc::mbar_arrive_expect_tx(v_full + s, TILE);
-          for (int c = 0; c < NCH; ++c)
-            tc::tma_load_3d(sV + s * TILE + c * kChunk, &tm_v, v_full + s, c * 64, g, krow);
-          ++vj;
+            tc::tma_load_3d(dst + c * kChunk, do_k ? &tm_k : &tm_v, fb, c * 64, g, krow);
         }
+        __syncwarp();
+        if (do_k) ++kj; else ++vj;
       }
-      if (*abort_flag) {  // let the copies already issued land before the CTA exits
-        volatile int never = 0;
-        for (int j = (kj > NS ? kj - NS : 0); j < kj; ++j)
-          tc::mbar_wait(k_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
-        for (int j = (vj > NS ? vj - NS : 0); j < vj; ++j)
-          tc::mbar_wait(v_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
-      }
+      kt += kj;
+      vt += vj;
+      ++nq;
+    }
+    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
+      volatile int never = 0;
+      for (int j = (kt > NS ? kt - NS : 0); j < kt; ++j)
+        tc::mbar_wait(k_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
+      for (int j = (vt > NS ? vt - NS : 0); j < vt; ++j)
+        tc::mbar_wait(v_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
     }
     __syncwarp();
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_it > 0) {
-      constexpr uint32_t idesc_qk = tc::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, false, true);
-      const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
-      auto issue_s = [&](int h, int s) {  // S_h = Q_h K(s)^T
+    constexpr uint32_t idesc_qk = tc::idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, false, true);
+    // Descriptors are built once; a k-step or stage only adds (byte offset >> 4)
+    // to the 14-bit start-address field (shared addresses stay below 2^18).
+    const uint64_t dQ = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
+    const uint64_t dK = tc::smem_desc(tc::smem_u32(sK), 16, 1024);
+    const uint64_t dV = tc::smem_desc(tc::smem_u32(sV), kChunk, 1024);
+    auto issue_s = [&](int h, int s) {  // S_h = Q_h K(s)^T
+      const uint64_t qa = dQ + ((h * TILE) >> 4), kb_ = dK + ((s * TILE) >> 4);
+      if (tc::elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-          tc::mma_ss(tmem + h * 128, tc::smem_desc(aQ + h * TILE + off, 16, 1024),
-                     tc::smem_desc(aK + s * TILE + off, 16, 1024), idesc_qk, k > 0);
+          const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
+          tc::mma_ss(tmem + h * 128, qa + off, kb_ + off, idesc_qk, k > 0);
         }
-      };
-      auto issue_pv = [&](int h, int s, bool first) {  // O_h (+)= P_h V(s), P_h read from TMEM
-#pragma unroll
-        for (int k = 0; k < kB / 16; ++k) {
-          const uint64_t db = tc::smem_desc(aV + s * TILE + k * 2048, kChunk, 1024);
-          mma_ts(tmem + 128 * NH + h * 128, tmem + h * 128 + k * 8, db, idesc_pv, (!first || k > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = tc::mbar_wait(q_full, 0, abort_flag, &g_status_fwd) &&
-                tc::mbar_wait(k_full, 0, abort_flag, &g_status_fwd);
-      if (ok) {
-        tc::tc_fence_after();
-        for (int h = 0; h < NH; ++h) {
-          issue_s(h, 0);
-          tc::mma_commit(s_full + h);
-        }
-        tc::mma_commit(k_empty);
+        tc::mma_commit(s_full + h);
       }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int h, int s, bool first) {  // O_h (+)= P_h V(s), P_h read from TMEM
+      const uint64_t vb = dV + ((s * TILE) >> 4);
+      if (tc::elect_one()) {
+#pragma unroll
+        for (int k = 0; k < kB / 16; ++k)
+          mma_ts(tmem + 128 * NH + h * 128, tmem + h * 128 + k * 8, vb + ((k * 2048) >> 4), idesc_pv,
+                 (!first || k > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* b_) {
+      if (tc::elect_one()) tc::mma_commit(b_);
+      __syncwarp();
+    };
+    int kt = 0, vt = 0, tb = 0, nq = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
+      const int it = item_ring[k & 1];
+      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
+      __syncwarp();
+      if (it < 0) break;
+      const Item I = decode_item<NH>(p, it);
+      const int n_it = I.n_it;
+      if (n_it == 0) continue;
+      // S_h(0): the S regions were last read by the previous item's PV (issued
+      // earlier, executed in order) and its softmax (done before its p_full).
+      if (!(ok = wait_u(q_full, nq & 1) && wait_u(k_full + kt % NS, (kt / NS) & 1))) break;
+      tc::tc_fence_after();
+      for (int h = 0; h < NH; ++h) issue_s(h, kt % NS);
+      commit(k_empty + kt % NS);
+      if (n_it == 1) commit(q_empty);
       for (int j = 0; ok && j < n_it; ++j) {
-        const int s = j % NS, s1 = (j + 1) % NS;
+        const int gv = vt + j, sv = gv % NS;
+        const int gk1 = kt + j + 1, s1 = gk1 % NS;
         const bool more = j + 1 < n_it;
-        if (!(ok = tc::mbar_wait(v_full + s, (j / NS) & 1, abort_flag, &g_status_fwd))) break;
+        if (!(ok = wait_u(v_full + sv, (gv / NS) & 1))) break;
         for (int h = 0; h < NH && ok; ++h) {
-          if (!(ok = tc::mbar_wait(p_full + h, j & 1, abort_flag, &g_status_fwd))) break;
+          if (!(ok = wait_u(p_full + h, (tb + j) & 1))) break;
+          if (j == 0 && nq > 0 && !(ok = wait_u(o_free + h, (nq - 1) & 1))) break;
           tc::tc_fence_after();
-          issue_pv(h, s, j == 0);
+          issue_pv(h, sv, j == 0);
           if (more) {
-            if (h == 0 && !(ok = tc::mbar_wait(k_full + s1, ((j + 1) / NS) & 1, abort_flag, &g_status_fwd)))
-              break;
+            if (h == 0 && !(ok = wait_u(k_full + s1, (gk1 / NS) & 1))) break;
             tc::tc_fence_after();
             issue_s(h, s1);
-            tc::mma_commit(s_full + h);
           }
         }
         if (!ok) break;
-        tc::mma_commit(v_empty + s);
-        if (more) tc::mma_commit(k_empty + s1);
+        commit(v_empty + sv);
+        if (more) {
+          commit(k_empty + s1);
+          if (j + 2 == n_it) commit(q_empty);  // the item's last S was just issued
+        }
       }
-      if (ok) tc::mma_commit(o_final);
-      if (*abort_flag) {  // let issued MMAs finish before TMEM is released
-        volatile int never = 0;
-        tc::mma_commit(drain);
-        tc::mbar_wait(drain, 0, &never, &g_status_fwd, 100000000ull);
-      }
+      if (ok) commit(o_final);
+      kt += n_it;
+      vt += n_it;
+      tb += n_it;
+      ++nq;
+    }
+    if (*abort_flag && tc::elect_one()) {  // let issued MMAs finish before TMEM is released
+      volatile int never = 0;
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0, &never, &g_status_fwd, 100000000ull);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax (head h)
     const int h = warp >> 2;
     const int r = threadIdx.x & 127;   // query row within the tile = TMEM lane
-    const int i = qb * kB + r;         // query position in the tree
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + h * 128;
     const uint32_t tO = tmem + lane_base + 128 * NH + h * 128;
-    __nv_bfloat16* orow = p.o + (int64_t(row0 + r) * p.hq + h0 + h) * D;
-    float* lse_out = p.lse + (int64_t(b) * p.hq + h0 + h) * p.t_pad + i;
+    const uint64_t sl2 = f2(p.scale_log2, p.scale_log2);
     auto wait_all = [&](uint64_t* b_, uint32_t par) {
       return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_fwd));
     };
-    if (n_it == 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
+    int tb = 0, nq = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!wait_all(item_full + (k & 1), (k >> 1) & 1)) break;
+      const int it = item_ring[k & 1];
+      tc::mbar_arrive(item_empty + (k & 1));
+      if (it < 0) break;
+      const Item I = decode_item<NH>(p, it);
+      const int n_it = I.n_it;
+      const int row0 = I.b * p.t_pad + I.qb * kB;
+      const int i = I.qb * kB + r;     // query position in the tree
+      __nv_bfloat16* orow = p.o + (int64_t(row0 + r) * p.hq + I.h0 + h) * D;
+      float* lse_out = p.lse + (int64_t(I.b) * p.hq + I.h0 + h) * p.t_pad + i;
+      if (n_it == 0) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
-      *lse_out = 0.f;
-    } else {
-      const uint64_t sl2 = f2(p.scale_log2, p.scale_log2);
-      const uint4* qmask_row = p.qmask + (int64_t(b) * p.cap + e0) * kB + r;
+        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+        *lse_out = 0.f;
+        continue;
+      }
+      const int32_t* list = p.q_idx + int64_t(I.b) * p.cap + I.e0;
+      const uint4* qmask_row = p.qmask + (int64_t(I.b) * p.cap + I.e0) * kB + r;
       float m_run = -INFINITY, l_run = 0.f;
-      bool ok = true;
       int entry = list[0];
       uint4 mk = (entry & 1) ? make_uint4(0, 0, 0, 0) : qmask_row[0];
       for (int j = 0; j < n_it; ++j) {
@@ -309,7 +402,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
           entry = list[j + 1];
           if (!(entry & 1)) mk = qmask_row[int64_t(j + 1) * kB];
         }
-        if (!wait_all(s_full + h, j & 1)) { ok = false; break; }
+        if (!wait_all(s_full + h, (tb + j) & 1)) { ok = false; break; }
         tc::tc_fence_after();
         uint32_t sv[128];
 #pragma unroll
@@ -322,9 +415,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
           for (int c = 0; c < 128; ++c)
             if (!((w[c >> 5] >> (c & 31)) & 1u)) sv[c] = 0xff800000u;  // -inf
         }
-        float mx = -INFINITY;
+        // row max: 8 independent chains, then a short tree
+        float mxs[8];
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) mx = max3(mx, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        for (int t = 0; t < 8; ++t) mxs[t] = fmaxf(__uint_as_float(sv[2 * t]), __uint_as_float(sv[2 * t + 1]));
+#pragma unroll
+        for (int c = 16; c < 128; c += 16)
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            mxs[t] = max3(mxs[t], __uint_as_float(sv[c + 2 * t]), __uint_as_float(sv[c + 2 * t + 1]));
+        const float mx = fmaxf(max3(mxs[0], mxs[1], mxs[2]), max3(mxs[3], mxs[4], max3(mxs[5], mxs[6], mxs[7])));
         const float m_new = fmaxf(m_run, mx * p.scale_log2);
         const bool resc = m_new > m_run + kRescaleThreshold;
         float alpha = 1.f;
@@ -334,18 +434,18 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
         const uint64_t negm = f2(-m_use, -m_use);
-        uint64_t sum2 = f2(0.f, 0.f);
+        uint64_t sum2[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};  // 4 chains
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float a, bb;
           unf2(fma2(f2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sl2, negm), a, bb);
           const float p0 = tc::ex2(a), p1 = tc::ex2(bb);
-          sum2 = add2(sum2, f2(p0, p1));
+          sum2[c & 3] = add2(sum2[c & 3], f2(p0, p1));
           pk[c] = tc::pack_bf16(p0, p1);
         }
         float s_lo, s_hi;
-        unf2(sum2, s_lo, s_hi);
+        unf2(add2(add2(sum2[0], sum2[1]), add2(sum2[2], sum2[3])), s_lo, s_hi);
         l_run = l_run * alpha + (s_lo + s_hi);
 
         // O_h holds the result of PV_h(j-1): s_full(j) was committed after it.
@@ -365,27 +465,30 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         tc::tc_fence_before();
         tc::mbar_arrive(p_full + h);
       }
-      if (ok && wait_all(o_final, 0)) {
-        tc::tc_fence_after();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      if (!ok || !wait_all(o_final, nq & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tc::tmem_ld32(tO + c * 32, ov);
-          tc::tmem_ld_wait();
-          uint32_t w[16];
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tc::tmem_ld32(tO + c * 32, ov);
+        tc::tmem_ld_wait();
+        uint32_t w[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            w[u] = tc::pack_bf16(__uint_as_float(ov[2 * u]) * inv, __uint_as_float(ov[2 * u + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-        }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        *lse_out = l_run > 0.f ? (m_use + __log2f(l_run)) * kLn2 : 0.f;
+        for (int u = 0; u < 16; ++u)
+          w[u] = tc::pack_bf16(__uint_as_float(ov[2 * u]) * inv, __uint_as_float(ov[2 * u + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+        dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
       }
+      tc::tc_fence_before();
+      tc::mbar_arrive(o_free + h);  // O_h may be overwritten by the next item
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      *lse_out = l_run > 0.f ? (m_use + __log2f(l_run)) * kLn2 : 0.f;
+      tb += n_it;
+      ++nq;
     }
   }
 
@@ -393,14 +496,33 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   if (warp == W_MMA) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  if (threadIdx.x == 0) {  // the last CTA to finish rearms the work counter for the next call
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      p.sched[0] = 0;
+      p.sched[1] = 0;
+      __threadfence();
+    }
+  }
+}
+
+int num_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  return sms;
 }
 
 template <int D, int NH>
-int launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& prm,
-                   int n_blk, int hq, int n_trees, cudaStream_t st) {
+int launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams prm,
+                   int n_trees, cudaStream_t st) {
   using C = FwdCfg<D, NH>;
+  prm.n_items = prm.n_blk * (prm.hq / NH) * n_trees;
+  const int grid = prm.n_items < num_sms() ? prm.n_items : num_sms();
   TPA_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES));
-  attn_fwd_kernel<D, NH><<<dim3(n_blk, hq / NH, n_trees), C::THREADS, C::BYTES, st>>>(tq, tk, tv, prm);
+  attn_fwd_kernel<D, NH><<<grid, C::THREADS, C::BYTES, st>>>(tq, tk, tv, prm);
   TPA_CUDA_TRY(cudaGetLastError());
   return TPA_OK;
 }
@@ -416,18 +538,19 @@ int launch_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   FwdParams prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
-  prm.n_tokens = tree->n_tokens;
   prm.q_ptr = mask->q_ptr;
   prm.q_idx = mask->q_idx;
   prm.qmask = reinterpret_cast<const uint4*>(mask->qmask);
+  prm.sched = mask->sched;
   prm.t_pad = tree->t_pad;
   prm.n_blk = mask->n_blk;
   prm.cap = mask->cap;
   prm.hq = hq;
   prm.hkv = hkv;
+  prm.n_items = 0;
   prm.scale_log2 = scale * kLog2e;
-  if ((hq / hkv) % 2 == 0) return launch_fwd_cfg<D, 2>(tq, tk, tv, prm, mask->n_blk, hq, tree->n_trees, st);
-  return launch_fwd_cfg<D, 1>(tq, tk, tv, prm, mask->n_blk, hq, tree->n_trees, st);
+  if ((hq / hkv) % 2 == 0) return launch_fwd_cfg<D, 2>(tq, tk, tv, prm, tree->n_trees, st);
+  return launch_fwd_cfg<D, 1>(tq, tk, tv, prm, tree->n_trees, st);
 }
 
 }  // namespace
@@ -437,7 +560,7 @@ TPA_DEFINE_STATUS_READER(tpa_internal_status_fwd, g_status_fwd)
 int tpa_internal_check_attn_args(const tpa_tree_view* tree, const tpa_blockmask_view* mask, int hq,
                                  int hkv, int d) {
   if (!tree || !mask || !tree->subtree_end || !tree->n_tokens || !mask->q_ptr || !mask->q_idx ||
-      !mask->k_ptr || !mask->k_idx || !mask->qmask)
+      !mask->k_ptr || !mask->k_idx || !mask->qmask || !mask->sched)
     return TPA_ERR_INVALID_ARG;
   if (tree->n_trees < 1 || tree->n_trees > 65535 || tree->t_pad < kB || tree->t_pad % kB ||
       mask->n_trees != tree->n_trees || mask->n_blk != tree->t_pad / kB)

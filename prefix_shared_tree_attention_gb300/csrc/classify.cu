@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(1024) csr_kernel(const uint8_t* __restrict__ c
                                                     int32_t cap, int32_t* __restrict__ q_ptr,
                                                     int32_t* __restrict__ q_idx,
                                                     int32_t* __restrict__ k_ptr,
-                                                    int32_t* __restrict__ k_idx) {
+                                                    int32_t* __restrict__ k_idx,
+                                                    uint32_t* __restrict__ sched) {
   __shared__ int scan_s[1024];
   const int b = blockIdx.x, dir = blockIdx.y;
   const int line = threadIdx.x;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(1024) csr_kernel(const uint8_t* __restrict__ c
   int pos = scan_s[line] - cnt;
   ptr[line] = pos;
   if (line == n_blk - 1) ptr[n_blk] = scan_s[line];
+  if (b == 0 && dir == 0 && line < 16) sched[line] = 0;  // work counters of the attention kernels
   for (int o = 0; o < n_blk; ++o) {
     const uint8_t v = c[line * s_line + o * s_elem];
     if (v != TPA_BLOCK_EMPTY) idx[pos++] = 2 * o + (v == TPA_BLOCK_FULL ? 1 : 0);
@@ -137,7 +139,7 @@ TPA_DEFINE_STATUS_READER(tpa_internal_status_classify, g_status_classify)
 extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
                                   void* stream) {
   if (!tree || !mask || !tree->subtree_end || !tree->n_tokens || !mask->cls || !mask->q_ptr ||
-      !mask->q_idx || !mask->k_ptr || !mask->k_idx || !mask->qmask)
+      !mask->q_idx || !mask->k_ptr || !mask->k_idx || !mask->qmask || !mask->sched)
     return TPA_ERR_INVALID_ARG;
   if (tree->t_pad % kB || mask->n_blk != tree->t_pad / kB || mask->n_trees != tree->n_trees ||
       mask->n_blk > 1024 || tree->n_trees < 1)
@@ -149,7 +151,7 @@ extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask
   TPA_CUDA_TRY(cudaGetLastError());
   const int threads = n_blk <= 32 ? 32 : ((n_blk + 31) / 32) * 32;
   csr_kernel<<<dim3(tree->n_trees, 2), threads, 0, st>>>(mask->cls, n_blk, mask->cap, mask->q_ptr,
-                                                         mask->q_idx, mask->k_ptr, mask->k_idx);
+                                                         mask->q_idx, mask->k_ptr, mask->k_idx, mask->sched);
   TPA_CUDA_TRY(cudaGetLastError());
   qmask_kernel<<<dim3(n_blk, tree->n_trees), 128, 0, st>>>(tree->subtree_end, tree->n_tokens, tree->t_pad,
                                                            n_blk, mask->cap, mask->q_ptr, mask->q_idx,

@@ -11,7 +11,7 @@ namespace {
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
 struct MaskLayout {
-  uint64_t cls, q_ptr, q_idx, k_ptr, k_idx, qmask, total;
+  uint64_t cls, q_ptr, q_idx, k_ptr, k_idx, qmask, sched, total;
 };
 
 bool mask_layout(int32_t n_trees, int32_t t_pad, MaskLayout* L) {
@@ -25,6 +25,7 @@ bool mask_layout(int32_t n_trees, int32_t t_pad, MaskLayout* L) {
   L->k_ptr = o; o = align256(o + 4 * B * (n + 1));
   L->k_idx = o; o = align256(o + 4 * B * cap);
   L->qmask = o; o = align256(o + 2048 * B * cap);
+  L->sched = o; o = align256(o + 4 * 16);
   L->total = o;
   return true;
 }
@@ -89,6 +90,7 @@ int tpa_blockmask_make_view(void* base, int32_t n_trees, int32_t t_pad, tpa_bloc
   v->k_ptr = reinterpret_cast<int32_t*>(b + L.k_ptr);
   v->k_idx = reinterpret_cast<int32_t*>(b + L.k_idx);
   v->qmask = reinterpret_cast<uint32_t*>(b + L.qmask);
+  v->sched = reinterpret_cast<uint32_t*>(b + L.sched);
   return TPA_OK;
 }
 

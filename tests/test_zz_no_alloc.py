@@ -58,12 +58,12 @@ def test_noalloc_matches_workspace_entry_point(tpa, grad_dtype):
         for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
             assert g.dtype == grad_dtype
             assert_attn_close(g.float(), r.float(), f"call {call} {name}")
-        # dK and dV involve no atomics: identical to the regular entry point
-        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        # the backward has no atomics: identical to the regular entry point
+        assert all(torch.equal(g, r) for g, r in zip(got, ref))
 
 
 def test_noalloc_refuses_oversized_problem(tpa):
-    # 1 tree x 65536 positions x 128 query heads needs 32 MiB of scratch
+    # 1 tree x 65536 positions x 128 query heads needs 32 MiB of scratch (D alone)
     tree, dtree, mask = pack_and_upload(tpa, [[1, 2, 3]], 65536)
     buf = torch.zeros(1024, dtype=torch.float32, device="cuda")
     p = buf.data_ptr()
