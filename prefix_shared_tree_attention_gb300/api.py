@@ -144,6 +144,7 @@ class BlockMask:
             "k_ptr": self._slice(v.k_ptr, 4 * B * (n + 1), torch.int32, (B, n + 1)),
             "k_idx": self._slice(v.k_idx, 4 * B * cap, torch.int32, (B, cap)),
             "qmask": self._slice(v.qmask, 2048 * B * cap, torch.int32, (B, cap, 128, 4)),
+            "sched": self._slice(v.sched, 4 * 16, torch.int32, (16,)),
         }
 
 

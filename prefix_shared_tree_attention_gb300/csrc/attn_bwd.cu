@@ -7,24 +7,25 @@
 //   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
 // with dK/dV summed over the query heads of each key/value head.
 //
-// Three kernels, no atomics:
-//  (1) preprocess: D = rowsum(dO * O) in fp32.
-//  (2) KV kernel, one CTA per (key tile, kv head, tree): walks the non-empty
-//      query tiles of its key tile (per-key-block CSR) for every query head of
-//      the group and accumulates dK, dV in TMEM.  Per step the MMA issuer
-//      runs S^T = K Q^T and dP^T = V dO^T; the four compute warpgroups (thread
-//      r = key row r = TMEM lane r; warpgroup w = query columns [32w, 32w+32))
-//      write P^T and dS^T back into TMEM as packed bf16 over the columns they
-//      read, and the issuer runs dV += P^T dO and dK += dS^T Q with A read
-//      from TMEM.  The next step's S^T / dP^T are issued right behind dK, so
-//      the tensor core stays fed while the warpgroups compute.  A key only
-//      sees the query interval [j, E[j]], applied on PARTIAL tiles.
-//  (3) dQ kernel, one CTA per (query tile, query head, tree): walks the
+// Three kernels, no atomics on the hot loop:
+//  (1) preprocess: D = rowsum(dO * O) in fp32 (and zeroed fp32 dK/dV, which
+//      chunks of long key columns add into).
+//  (2) KV kernel: work items are (key tile, kv head, tree, chunk of up to 64
+//      steps of that key tile's column), a step being one (query head, query
+//      tile) pair of the per-key-block CSR.  Per step the MMA issuer runs
+//      S^T = K Q^T and dP^T = V dO^T; four compute warpgroups (thread r = key
+//      row r = TMEM lane r; warpgroup w = query columns [32w, 32w+32)) write
+//      P^T and dS^T back into TMEM as packed bf16, and the issuer runs
+//      dV += P^T dO and dK += dS^T Q with A read from TMEM.  A key only sees
+//      the query interval [j, E[j]], applied on PARTIAL tiles.
+//  (3) dQ kernel: work items are (query tile, query head, tree); it walks the
 //      query block's key tiles like the forward, recomputes S = Q K^T (double
 //      buffered in TMEM) and dP = dO V^T, forms dS = P (dP - D) with the
-//      forward's LSE and the precomputed partial-tile bit masks, writes dS as
-//      packed bf16 into TMEM and accumulates dQ += dS K in TMEM; dQ is stored
-//      once at the end.
+//      forward's LSE and the partial-tile bit masks, writes dS as packed bf16
+//      into TMEM and accumulates dQ += dS K in TMEM; dQ is stored once.
+// Both main kernels are persistent: one CTA per SM takes items from a counter
+// in the block-mask buffer, barrier phases run on across items, and the issuer
+// warps run converged with an elected lane issuing each copy, MMA and commit.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,6 +46,11 @@ constexpr int kB = 128;
 constexpr uint32_t kChunk = 128 * 128;  // bytes of a 128-row x 64-col bf16 tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kSmemMax = 232448;   // 227 KB opt-in per CTA
+constexpr int kNWG = 4;                    // compute warpgroups per CTA
+constexpr int kCW = kB / kNWG;             // columns per warpgroup (32)
+constexpr int kThreads = 128 * kNWG + 64;  // + TMA warp + MMA warp
+constexpr int kWTma = 4 * kNWG, kWMma = 4 * kNWG + 1;
+constexpr int kKvChunk = 64;               // steps per KV work item (fp32 gradients)
 
 struct BwdParams {
   const float* lse;     // [B, Hq, T]
@@ -59,7 +65,9 @@ struct BwdParams {
   const int32_t* q_ptr;
   const int32_t* q_idx;
   const uint4* qmask;
+  uint32_t* sched;      // work counters: [2..3] KV kernel, [4..5] dQ kernel
   int32_t t_pad, n_blk, cap, hq, hkv;
+  int32_t kv_chunk, kv_nchunk, kv_items, dq_items;
   float scale, scale_log2;
 };
 
@@ -73,17 +81,32 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Writes 16 fp32 values of one row as fp32 or bf16 (with a scale).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+// Writes 16 fp32 values of one row as fp32 or bf16 (with a scale), or adds
+// them into an fp32 row.
 template <bool F32OUT>
-__device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16], float scale) {
+__device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16], float scale, bool add) {
   if (F32OUT) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    float* f = reinterpret_cast<float*>(dst);
+    if (add) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
-      d4[t] = make_uint4(__float_as_uint(__uint_as_float(v[4 * t]) * scale),
-                         __float_as_uint(__uint_as_float(v[4 * t + 1]) * scale),
-                         __float_as_uint(__uint_as_float(v[4 * t + 2]) * scale),
-                         __float_as_uint(__uint_as_float(v[4 * t + 3]) * scale));
+      for (int t = 0; t < 4; ++t)
+        red_add_v4(f + 4 * t, __uint_as_float(v[4 * t]) * scale, __uint_as_float(v[4 * t + 1]) * scale,
+                   __uint_as_float(v[4 * t + 2]) * scale, __uint_as_float(v[4 * t + 3]) * scale);
+    } else {
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        d4[t] = make_uint4(__float_as_uint(__uint_as_float(v[4 * t]) * scale),
+                           __float_as_uint(__uint_as_float(v[4 * t + 1]) * scale),
+                           __float_as_uint(__uint_as_float(v[4 * t + 2]) * scale),
+                           __float_as_uint(__uint_as_float(v[4 * t + 3]) * scale));
+    }
   } else {
     uint32_t w[8];
 #pragma unroll
@@ -95,19 +118,40 @@ __device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16
   }
 }
 
-// =========================================================================== KV kernel
-
-constexpr int kNWG = 4;                    // compute warpgroups per CTA
-constexpr int kCW = kB / kNWG;             // columns per warpgroup (32)
-constexpr int kThreads = 128 * kNWG + 64;  // + TMA warp + MMA warp
-constexpr int kWTma = 4 * kNWG, kWMma = 4 * kNWG + 1;
-
 // Packed bf16 A operand written by the warpgroups: warpgroup w owns columns
-// [32w, 32w+32) of the region it read; P (or dS) for its 32 rows of K goes to
-// the first 16 columns of that range (second-operand values to the last 16).
-__device__ __forceinline__ uint32_t wg_a(uint32_t base, int k, uint32_t sub) {
-  return base + 32 * (k >> 1) + sub + 8 * (k & 1);
+// [32w, 32w+32) of the region it read and writes its 32 K-values packed into
+// the first 16 of them.
+__device__ __forceinline__ uint32_t wg_a(uint32_t base, int k) { return base + 32 * (k >> 1) + 8 * (k & 1); }
+
+// Item fetch shared by the producers of both kernels: one lane takes the next
+// index from the counter, the elected lane publishes it.
+// Returns -1 once the items are used up.
+__device__ __forceinline__ int fetch_item(uint32_t* counter, int n_items, volatile int* ring, uint64_t* full) {
+  uint32_t u = 0;
+  if ((threadIdx.x & 31) == 0) u = atomicAdd(counter, 1u);
+  u = __shfl_sync(0xffffffffu, u, 0);
+  const int it = u < uint32_t(n_items) ? int(u) : -1;  // unsigned: no index below 0
+  if (tc::elect_one()) {
+    *ring = it;
+    tc::mbar_arrive(full);
+  }
+  __syncwarp();
+  return it;
 }
+
+// The last CTA to finish rearms a kernel's work counter for the next call.
+__device__ __forceinline__ void rearm_counter(uint32_t* ctr) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+      ctr[0] = 0;
+      ctr[1] = 0;
+      __threadfence();
+    }
+  }
+}
+
+// =========================================================================== KV kernel
 
 template <int D>
 struct KvCfg {
@@ -122,13 +166,39 @@ struct KvCfg {
   static constexpr uint32_t OFF_LSE = OFF_DO + NS * TILE;   // NS x 128 fp32
   static constexpr uint32_t OFF_DV = OFF_LSE + NS * kB * 4; // NS x 128 fp32
   static constexpr uint32_t OFF_BAR = OFF_DV + NS * kB * 4;
-  // kv_full, q_full[NS], q_empty[NS], s_full, dp_full, p_ready, ds_ready, drain
-  static constexpr int NBAR = 1 + 2 * NS + 5;
+  // kv_full, kv_empty, q_full[NS], q_empty[NS], s_full, dp_full, p_ready, ds_ready, acc_full,
+  // acc_free, drain, item_full[2], item_empty[2]
+  static constexpr int NBAR = 2 + 2 * NS + 7 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;
   static_assert(NS >= 2, "shared memory budget");
   static_assert(BYTES <= kSmemMax, "shared memory budget");
 };
+
+struct KvItem {
+  int b, g, kb, n_col, s0, n;  // column of (b, g, kb); steps [s0, s0 + n)
+  const int32_t* list;
+};
+
+__device__ __forceinline__ KvItem decode_kv(const BwdParams& p, int it) {
+  KvItem r;
+  const int G = p.hq / p.hkv;
+  const int per_g = p.n_blk * p.kv_nchunk;
+  const int per_b = p.hkv * per_g;
+  r.b = it / per_b;
+  int rem = it - r.b * per_b;
+  r.g = rem / per_g;
+  rem -= r.g * per_g;
+  r.kb = rem / p.kv_nchunk;  // ascending key blocks: the longest columns first
+  const int ch = rem - r.kb * p.kv_nchunk;
+  const int32_t* kp = p.k_ptr + r.b * (p.n_blk + 1);
+  r.n_col = kp[r.kb + 1] - kp[r.kb];
+  r.list = p.k_idx + int64_t(r.b) * p.cap + kp[r.kb];
+  r.s0 = ch * p.kv_chunk;
+  const int total = G * r.n_col;
+  r.n = total - r.s0 < p.kv_chunk ? total - r.s0 : p.kv_chunk;
+  return r;
+}
 
 template <int D, bool F32OUT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -148,28 +218,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sDv = reinterpret_cast<float*>(smem + C::OFF_DV);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bar;
-  uint64_t* q_full = bar + 1;
-  uint64_t* q_empty = bar + 1 + NS;
-  uint64_t* s_full = bar + 1 + 2 * NS;
+  uint64_t* kv_empty = bar + 1;
+  uint64_t* q_full = bar + 2;
+  uint64_t* q_empty = q_full + NS;
+  uint64_t* s_full = q_empty + NS;
   uint64_t* dp_full = s_full + 1;
   uint64_t* p_ready = s_full + 2;
   uint64_t* ds_ready = s_full + 3;
-  uint64_t* drain = s_full + 4;
+  uint64_t* acc_full = s_full + 4;
+  uint64_t* acc_free = s_full + 5;
+  uint64_t* drain = s_full + 6;
+  uint64_t* item_full = s_full + 7;   // [2]
+  uint64_t* item_empty = s_full + 9;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // [2]
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, g = blockIdx.y, kb = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
   const int G = p.hq / p.hkv;
-  const int32_t* kp = p.k_ptr + b * (p.n_blk + 1);
-  const int n_col = kp[kb + 1] - kp[kb];
-  const int32_t* list = p.k_idx + int64_t(b) * p.cap + kp[kb];
-  const int n_steps = G * n_col;
-  const int krow = b * p.t_pad + kb * kB;
   constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  constexpr int NCONS = 1 + 128 * kNWG;  // item consumers: MMA warp (elected lane) + compute threads
 
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
+    tc::mbar_init(kv_empty, 1);
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(q_full + s, 1);
       tc::mbar_init(q_empty + s, 1);
@@ -178,7 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(dp_full, 1);
     tc::mbar_init(p_ready, 128 * kNWG);
     tc::mbar_init(ds_ready, 128 * kNWG);
+    tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_free, 128 * kNWG);
     tc::mbar_init(drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(item_full + s, 1);
+      tc::mbar_init(item_empty + s, NCONS);
+    }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -187,211 +265,274 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  auto wait_u = [&](uint64_t* b_, uint32_t par) {
+    return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_bwd));
+  };
 
   if (warp == kWTma) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_steps > 0) {
+    if (tc::elect_one()) {
       tc::tma_prefetch_desc(&tm_q);
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
       tc::tma_prefetch_desc(&tm_do);
-      tc::mbar_arrive_expect_tx(kv_full, 2 * TILE);
-      for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sK + c * kChunk, &tm_k, kv_full, c * 64, g, krow);
-      for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sV + c * kChunk, &tm_v, kv_full, c * 64, g, krow);
-      int s = 0;
-      for (; s < n_steps; ++s) {
-        const int st = s % NS;
-        if (!tc::mbar_wait(q_empty + st, ((s / NS) & 1) ^ 1, abort_flag, &g_status_bwd)) break;
-        const int h = g * G + s / n_col;
-        const int qb = list[s % n_col] >> 1;
-        const int qrow = b * p.t_pad + qb * kB;
-        const int64_t vec = (int64_t(b) * p.hq + h) * p.t_pad + qb * kB;
-        tc::mbar_arrive_expect_tx(q_full + st, 2 * TILE + 2 * kB * 4);
-        for (int c = 0; c < NCH; ++c)
-          tc::tma_load_3d(sQ + st * TILE + c * kChunk, &tm_q, q_full + st, c * 64, h, qrow);
-        for (int c = 0; c < NCH; ++c)
-          tc::tma_load_3d(sDO + st * TILE + c * kChunk, &tm_do, q_full + st, c * 64, h, qrow);
-        tc::bulk_load(sLSE + st * kB, p.lse + vec, kB * 4, q_full + st);
-        tc::bulk_load(sDv + st * kB, p.dvec + vec, kB * 4, q_full + st);
+    }
+    __syncwarp();
+    int qs = 0, nk = 0;  // Q ring steps and K/V loads so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+      const int it = fetch_item(p.sched + 2, p.kv_items, item_ring + (k & 1), item_full + (k & 1));
+      if (it < 0) break;
+      const KvItem I = decode_kv(p, it);
+      if (I.n <= 0) continue;
+      const int krow = I.b * p.t_pad + I.kb * kB;
+      if (!(ok = wait_u(kv_empty, (nk & 1) ^ 1))) break;
+      if (tc::elect_one()) {
+        tc::mbar_arrive_expect_tx(kv_full, 2 * TILE);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sK + c * kChunk, &tm_k, kv_full, c * 64, I.g, krow);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sV + c * kChunk, &tm_v, kv_full, c * 64, I.g, krow);
       }
-      if (*abort_flag) {  // let the copies already issued land before the CTA exits
-        volatile int never = 0;
-        tc::mbar_wait(kv_full, 0, &never, &g_status_bwd, 100000000ull);
-        for (int j = (s > NS ? s - NS : 0); j < s; ++j)
-          tc::mbar_wait(q_full + (j % NS), (j / NS) & 1, &never, &g_status_bwd, 100000000ull);
+      __syncwarp();
+      for (int t = 0; t < I.n; ++t) {
+        const int gs = qs + t, st = gs % NS;
+        if (!(ok = wait_u(q_empty + st, ((gs / NS) & 1) ^ 1))) break;
+        const int s = I.s0 + t;
+        const int h = I.g * G + s / I.n_col;
+        const int qb = I.list[s % I.n_col] >> 1;
+        if (tc::elect_one()) {
+          const int qrow = I.b * p.t_pad + qb * kB;
+          const int64_t vec = (int64_t(I.b) * p.hq + h) * p.t_pad + qb * kB;
+          tc::mbar_arrive_expect_tx(q_full + st, 2 * TILE + 2 * kB * 4);
+          for (int c = 0; c < NCH; ++c)
+            tc::tma_load_3d(sQ + st * TILE + c * kChunk, &tm_q, q_full + st, c * 64, h, qrow);
+          for (int c = 0; c < NCH; ++c)
+            tc::tma_load_3d(sDO + st * TILE + c * kChunk, &tm_do, q_full + st, c * 64, h, qrow);
+          tc::bulk_load(sLSE + st * kB, p.lse + vec, kB * 4, q_full + st);
+          tc::bulk_load(sDv + st * kB, p.dvec + vec, kB * 4, q_full + st);
+        }
+        __syncwarp();
       }
+      qs += I.n;
+      ++nk;
+    }
+    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
+      volatile int never = 0;
+      if (nk > 0) tc::mbar_wait(kv_full, (nk - 1) & 1, &never, &g_status_bwd, 100000000ull);
+      for (int j = (qs > NS ? qs - NS : 0); j < qs; ++j)
+        tc::mbar_wait(q_full + (j % NS), (j / NS) & 1, &never, &g_status_bwd, 100000000ull);
     }
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Per step s: dV(s) as soon as P^T(s) is in TMEM, then S^T(s+1) into the
-    // region P^T(s) came from (in order behind dV), then dK(s) once dS^T(s) is
-    // in TMEM, then dP^T(s+1) into the region dS^T(s) came from.
-    if (lane == 0 && n_steps > 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_kv = tc::idesc_bf16(128, D, false, true);
-      const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aQ = tc::smem_u32(sQ),
-                     aDO = tc::smem_u32(sDO);
-      auto issue_s = [&](int s) {  // S^T = K Q^T
-        const uint32_t qs = aQ + (s % NS) * TILE;
+    // Per step: dV as soon as P^T is in TMEM, then S^T of the next step into the
+    // region P^T came from (in order behind dV), then dK once dS^T is in TMEM,
+    // then dP^T of the next step into the region dS^T came from.
+    constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_kv = tc::idesc_bf16(128, D, false, true);
+    const uint64_t dK_ = tc::smem_desc(tc::smem_u32(sK), 16, 1024);
+    const uint64_t dV_ = tc::smem_desc(tc::smem_u32(sV), 16, 1024);
+    const uint64_t dQk = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);        // Q as K-major B
+    const uint64_t dDOk = tc::smem_desc(tc::smem_u32(sDO), 16, 1024);      // dO as K-major B
+    const uint64_t dQm = tc::smem_desc(tc::smem_u32(sQ), kChunk, 1024);    // Q as MN-major B
+    const uint64_t dDOm = tc::smem_desc(tc::smem_u32(sDO), kChunk, 1024);  // dO as MN-major B
+    auto issue_s_dp = [&](int gs, bool s_only, bool dp_only) {  // S^T = K Q^T ; dP^T = V dO^T
+      const uint32_t so = ((gs % NS) * TILE) >> 4;
+      if (tc::elect_one()) {
+        if (!dp_only) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-          tc::mma_ss(tmem + T_S, tc::smem_desc(aK + off, 16, 1024), tc::smem_desc(qs + off, 16, 1024), idesc_s,
-                     k > 0);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
+            tc::mma_ss(tmem + T_S, dK_ + off, dQk + so + off, idesc_s, k > 0);
+          }
+          tc::mma_commit(s_full);
         }
-        tc::mma_commit(s_full);
-      };
-      auto issue_dp = [&](int s) {  // dP^T = V dO^T
-        const uint32_t dos = aDO + (s % NS) * TILE;
+        if (!s_only) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-          tc::mma_ss(tmem + T_DP, tc::smem_desc(aV + off, 16, 1024), tc::smem_desc(dos + off, 16, 1024),
-                     idesc_s, k > 0);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
+            tc::mma_ss(tmem + T_DP, dV_ + off, dDOk + so + off, idesc_s, k > 0);
+          }
+          tc::mma_commit(dp_full);
         }
-        tc::mma_commit(dp_full);
-      };
-      bool ok = tc::mbar_wait(kv_full, 0, abort_flag, &g_status_bwd) &&
-                tc::mbar_wait(q_full, 0, abort_flag, &g_status_bwd);
-      if (ok) {
-        tc::tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
       }
-      for (int s = 0; ok && s < n_steps; ++s) {
-        const int st = s % NS;
-        const bool more = s + 1 < n_steps;
-        const uint32_t qs = aQ + st * TILE, dos = aDO + st * TILE;
-        if (!(ok = tc::mbar_wait(p_ready, s & 1, abort_flag, &g_status_bwd))) break;
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* b_) {
+      if (tc::elect_one()) tc::mma_commit(b_);
+      __syncwarp();
+    };
+    int qs = 0, nk = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
+      const int it = item_ring[k & 1];
+      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
+      __syncwarp();
+      if (it < 0) break;
+      const KvItem I = decode_kv(p, it);
+      const int n = I.n;
+      if (n <= 0) continue;
+      if (!(ok = wait_u(kv_full, nk & 1) && wait_u(q_full + qs % NS, (qs / NS) & 1))) break;
+      tc::tc_fence_after();
+      issue_s_dp(qs, false, false);
+      for (int t = 0; ok && t < n; ++t) {
+        const int gs = qs + t, st = gs % NS;
+        const bool more = t + 1 < n;
+        const uint32_t so = (st * TILE) >> 4;
+        if (!(ok = wait_u(p_ready, gs & 1))) break;
+        if (t == 0 && nk > 0 && !(ok = wait_u(acc_free, (nk - 1) & 1))) break;
         tc::tc_fence_after();
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < kB / 16; ++k)  // dV += P^T dO, P^T packed bf16 in TMEM
-          mma_ts(tmem + T_DV, wg_a(tmem + T_S, k, 0), tc::smem_desc(dos + k * 2048, kChunk, 1024), idesc_kv,
-                 (s > 0 || k > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kB / 16; ++kk)  // dV += P^T dO, P^T packed bf16 in TMEM
+            mma_ts(tmem + T_DV, wg_a(tmem + T_S, kk), dDOm + so + ((kk * 2048) >> 4), idesc_kv,
+                   (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
         if (more) {
-          if (!(ok = tc::mbar_wait(q_full + (s + 1) % NS, ((s + 1) / NS) & 1, abort_flag, &g_status_bwd))) break;
+          if (!(ok = wait_u(q_full + (gs + 1) % NS, ((gs + 1) / NS) & 1))) break;
           tc::tc_fence_after();
-          issue_s(s + 1);
+          issue_s_dp(gs + 1, true, false);
         }
-        if (!(ok = tc::mbar_wait(ds_ready, s & 1, abort_flag, &g_status_bwd))) break;
+        if (!(ok = wait_u(ds_ready, gs & 1))) break;
         tc::tc_fence_after();
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < kB / 16; ++k)  // dK += dS^T Q, dS^T packed bf16 in TMEM
-          mma_ts(tmem + T_DK, wg_a(tmem + T_DP, k, 0), tc::smem_desc(qs + k * 2048, kChunk, 1024), idesc_kv,
-                 (s > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(q_empty + st);
-        if (more)
-          issue_dp(s + 1);
-        else
-          tc::mma_commit(s_full);  // final: dV and dK complete
+          for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in TMEM
+            mma_ts(tmem + T_DK, wg_a(tmem + T_DP, kk), dQm + so + ((kk * 2048) >> 4), idesc_kv,
+                   (t > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(q_empty + st);
+        }
+        __syncwarp();
+        if (more) issue_s_dp(gs + 1, false, true);
       }
-      if (*abort_flag) {  // let issued MMAs finish before TMEM is released
-        volatile int never = 0;
-        tc::mma_commit(drain);
-        tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
-      }
+      if (!ok) break;
+      commit(kv_empty);  // K, V reads done once these complete
+      commit(acc_full);  // dK, dV complete
+      qs += n;
+      ++nk;
+    }
+    if (*abort_flag && tc::elect_one()) {  // let issued MMAs finish before TMEM is released
+      volatile int never = 0;
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
     }
     __syncwarp();
   } else if (warp < 4 * kNWG) {
     // ------------------------------------------------------------ compute warpgroups
     const int w = warp >> 2;              // query columns [32w, 32w+32) of this warpgroup
     const int r = threadIdx.x & 127;      // key row = TMEM lane
-    const int j = kb * kB + r;            // key position owned by this thread
-    const int n = p.n_tokens[b];
-    const int Ej = (j < n) ? p.subtree_end[krow + r] : -1;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    auto wait_all = [&](uint64_t* b_, uint32_t par) {
-      return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_bwd));
-    };
-    bool ok = true;
-    for (int s = 0; s < n_steps; ++s) {
-      const int st = s % NS;
-      const int entry = list[s % n_col];
-      const int qb = entry >> 1;
-      const bool full = entry & 1;
-      if (!wait_all(q_full + st, (s / NS) & 1) || !wait_all(s_full, s & 1)) { ok = false; break; }
-      tc::tc_fence_after();
-      // ---- P^T = exp2(S * scale*log2e - LSE*log2e) on this group's 32 query columns
-      float pf[kCW];
-      {
-        uint32_t sv[kCW];
-        tc::tmem_ld32(tmem + lane_base + T_S + kCW * w, sv);
-        const float4* l4 = reinterpret_cast<const float4*>(sLSE + st * kB + kCW * w);
-        tc::tmem_ld_wait();
-        const int lo = j - (qb * kB + kCW * w);  // visible query columns: [lo, hi]
-        const int hi = Ej - (qb * kB + kCW * w);
-#pragma unroll
-        for (int c4 = 0; c4 < kCW / 4; ++c4) {
-          const float4 l = l4[c4];
-          const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = 4 * c4 + u;
-            pf[c] = tc::ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[u] * kLog2e));
-          }
-        }
-        if (!full) {
-#pragma unroll
-          for (int c = 0; c < kCW; ++c)
-            if (c < lo || c > hi) pf[c] = 0.f;
-        }
-        uint32_t pw[kCW / 2];
-#pragma unroll
-        for (int u = 0; u < kCW / 2; ++u) pw[u] = tc::pack_bf16(pf[2 * u], pf[2 * u + 1]);
-        tc::tmem_st16(tmem + lane_base + T_S + kCW * w, pw);  // over the first half of what was read
-        tc::tmem_st_wait();
-      }
-      tc::tc_fence_before();
-      tc::mbar_arrive(p_ready);
-      // ---- dS^T = P^T (dP^T - D)
-      if (!wait_all(dp_full, s & 1)) { ok = false; break; }
-      tc::tc_fence_after();
-      {
-        uint32_t dpv[kCW];
-        tc::tmem_ld32(tmem + lane_base + T_DP + kCW * w, dpv);
-        const float4* d4 = reinterpret_cast<const float4*>(sDv + st * kB + kCW * w);
-        tc::tmem_ld_wait();
-        uint32_t dw[kCW / 2];
-#pragma unroll
-        for (int c4 = 0; c4 < kCW / 4; ++c4) {
-          const float4 dd = d4[c4];
-          const int c = 4 * c4;
-          dw[2 * c4] = tc::pack_bf16(pf[c] * (__uint_as_float(dpv[c]) - dd.x),
-                                     pf[c + 1] * (__uint_as_float(dpv[c + 1]) - dd.y));
-          dw[2 * c4 + 1] = tc::pack_bf16(pf[c + 2] * (__uint_as_float(dpv[c + 2]) - dd.z),
-                                         pf[c + 3] * (__uint_as_float(dpv[c + 3]) - dd.w));
-        }
-        tc::tmem_st16(tmem + lane_base + T_DP + kCW * w, dw);
-        tc::tmem_st_wait();
-      }
-      tc::tc_fence_before();
-      tc::mbar_arrive(ds_ready);
-    }
-    // ---- dK, dV rows of this key tile (warpgroup w: head-dim columns [w d/4, (w+1) d/4))
     constexpr int ESZ = F32OUT ? 4 : 2;
     constexpr int DW = D / kNWG;
-    const int64_t off = ((int64_t(krow + r) * p.hkv + g) * D + w * DW) * ESZ;
-    uint8_t* dk_row = static_cast<uint8_t*>(p.dk) + off;
-    uint8_t* dv_row = static_cast<uint8_t*>(p.dv) + off;
-    if (n_steps == 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
+    int qs = 0, nk = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!wait_u(item_full + (k & 1), (k >> 1) & 1)) break;
+      const int it = item_ring[k & 1];
+      tc::mbar_arrive(item_empty + (k & 1));
+      if (it < 0) break;
+      const KvItem I = decode_kv(p, it);
+      const int krow = I.b * p.t_pad + I.kb * kB;
+      const int64_t off = ((int64_t(krow + r) * p.hkv + I.g) * D + w * DW) * ESZ;
+      uint8_t* dk_row = static_cast<uint8_t*>(p.dk) + off;
+      uint8_t* dv_row = static_cast<uint8_t*>(p.dv) + off;
+      if (I.n <= 0) {
+        // a key tile no query sees: zero rows (fp32 outputs were zeroed by the preprocess)
+        if (!F32OUT && I.s0 == 0) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int c = 0; c < DW * ESZ / 16; ++c) {
-        reinterpret_cast<uint4*>(dk_row)[c] = z;
-        reinterpret_cast<uint4*>(dv_row)[c] = z;
+          for (int c = 0; c < DW * ESZ / 16; ++c) {
+            reinterpret_cast<uint4*>(dk_row)[c] = z;
+            reinterpret_cast<uint4*>(dv_row)[c] = z;
+          }
+        }
+        continue;
       }
-    } else if (ok && wait_all(s_full, n_steps & 1)) {
+      const int j = I.kb * kB + r;  // key position owned by this thread
+      const int n_tok = p.n_tokens[I.b];
+      const int Ej = (j < n_tok) ? p.subtree_end[krow + r] : -1;
+      for (int t = 0; t < I.n; ++t) {
+        const int gs = qs + t, st = gs % NS;
+        const int entry = I.list[(I.s0 + t) % I.n_col];
+        const int qb = entry >> 1;
+        const bool full = entry & 1;
+        if (!wait_u(q_full + st, (gs / NS) & 1) || !wait_u(s_full, gs & 1)) { ok = false; break; }
+        tc::tc_fence_after();
+        // ---- P^T = exp2(S * scale*log2e - LSE*log2e) on this group's 32 query columns
+        float pf[kCW];
+        {
+          uint32_t sv[kCW];
+          tc::tmem_ld32(tmem + lane_base + T_S + kCW * w, sv);
+          const float4* l4 = reinterpret_cast<const float4*>(sLSE + st * kB + kCW * w);
+          tc::tmem_ld_wait();
+          const int lo = j - (qb * kB + kCW * w);  // visible query columns: [lo, hi]
+          const int hi = Ej - (qb * kB + kCW * w);
+#pragma unroll
+          for (int c4 = 0; c4 < kCW / 4; ++c4) {
+            const float4 l = l4[c4];
+            const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = 4 * c4 + u;
+              pf[c] = tc::ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[u] * kLog2e));
+            }
+          }
+          if (!full) {
+#pragma unroll
+            for (int c = 0; c < kCW; ++c)
+              if (c < lo || c > hi) pf[c] = 0.f;
+          }
+          uint32_t pw[kCW / 2];
+#pragma unroll
+          for (int u = 0; u < kCW / 2; ++u) pw[u] = tc::pack_bf16(pf[2 * u], pf[2 * u + 1]);
+          tc::tmem_st16(tmem + lane_base + T_S + kCW * w, pw);  // over the first half of what was read
+          tc::tmem_st_wait();
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(p_ready);
+        // ---- dS^T = P^T (dP^T - D)
+        if (!wait_u(dp_full, gs & 1)) { ok = false; break; }
+        tc::tc_fence_after();
+        {
+          uint32_t dpv[kCW];
+          tc::tmem_ld32(tmem + lane_base + T_DP + kCW * w, dpv);
+          const float4* d4 = reinterpret_cast<const float4*>(sDv + st * kB + kCW * w);
+          tc::tmem_ld_wait();
+          uint32_t dw[kCW / 2];
+#pragma unroll
+          for (int c4 = 0; c4 < kCW / 4; ++c4) {
+            const float4 dd = d4[c4];
+            const int c = 4 * c4;
+            dw[2 * c4] = tc::pack_bf16(pf[c] * (__uint_as_float(dpv[c]) - dd.x),
+                                       pf[c + 1] * (__uint_as_float(dpv[c + 1]) - dd.y));
+            dw[2 * c4 + 1] = tc::pack_bf16(pf[c + 2] * (__uint_as_float(dpv[c + 2]) - dd.z),
+                                           pf[c + 3] * (__uint_as_float(dpv[c + 3]) - dd.w));
+          }
+          tc::tmem_st16(tmem + lane_base + T_DP + kCW * w, dw);
+          tc::tmem_st_wait();
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(ds_ready);
+      }
+      if (!ok || !wait_u(acc_full, nk & 1)) { ok = false; break; }
+      // ---- dK, dV rows of this key tile (warpgroup w: head-dim columns [w d/4, (w+1) d/4))
       tc::tc_fence_after();
+      const bool add = F32OUT && (G * I.n_col > p.kv_chunk);  // several chunks add into one row
 #pragma unroll
       for (int c = 0; c < DW / 16; ++c) {
         uint32_t vv[16], kk[16];
         tc::tmem_ld16(tmem + lane_base + T_DV + w * DW + c * 16, vv);
         tc::tmem_ld16(tmem + lane_base + T_DK + w * DW + c * 16, kk);
         tc::tmem_ld_wait();
-        store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f);
-        store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, p.scale);
+        store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, add);
+        store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, p.scale, add);
       }
+      tc::tc_fence_before();
+      tc::mbar_arrive(acc_free);
+      qs += I.n;
+      ++nk;
     }
   }
 
@@ -399,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   if (warp == kWMma) tc::tmem_dealloc(tmem, 512);
+  rearm_counter(p.sched + 2);
 }
 
 // =========================================================================== dQ kernel
@@ -414,13 +556,32 @@ struct DqCfg {
   static constexpr uint32_t OFF_K = 2 * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
   static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
-  // q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], dp_full, dp_free,
-  // ds_ready, dq_final, drain
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 7;
+  // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], dp_full,
+  // dp_free, ds_ready, dq_final, dq_free, drain, item_full[2], item_empty[2]
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 8 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;
   static_assert(BYTES <= kSmemMax, "shared memory budget");
 };
+
+struct DqItem {
+  int b, h, qb, e0, n;
+  const int32_t* list;
+};
+
+__device__ __forceinline__ DqItem decode_dq(const BwdParams& p, int it) {
+  DqItem r;
+  const int per_b = p.hq * p.n_blk;
+  r.b = it / per_b;
+  const int rem = it - r.b * per_b;
+  r.h = rem / p.n_blk;
+  r.qb = p.n_blk - 1 - rem % p.n_blk;  // deepest (usually heaviest) query blocks first
+  const int32_t* rp = p.q_ptr + r.b * (p.n_blk + 1);
+  r.e0 = rp[r.qb];
+  r.n = rp[r.qb + 1] - r.e0;
+  r.list = p.q_idx + int64_t(r.b) * p.cap + r.e0;
+  return r;
+}
 
 template <int D, bool F32OUT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -438,7 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + C::OFF_V;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bar;
-  uint64_t* k_full = bar + 1;
+  uint64_t* q_empty = bar + 1;
+  uint64_t* k_full = bar + 2;
   uint64_t* k_empty = k_full + NSK;
   uint64_t* v_full = k_empty + NSK;
   uint64_t* v_empty = v_full + NSV;
@@ -447,23 +609,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_free = s_full + 3;
   uint64_t* ds_ready = s_full + 4;
   uint64_t* dq_final = s_full + 5;
-  uint64_t* drain = s_full + 6;
+  uint64_t* dq_free = s_full + 6;
+  uint64_t* drain = s_full + 7;
+  uint64_t* item_full = s_full + 8;    // [2]
+  uint64_t* item_empty = s_full + 10;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // [2]
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int qb = p.n_blk - 1 - blockIdx.x;  // deepest (usually heaviest) query blocks first
-  const int g = h / (p.hq / p.hkv);
-  const int32_t* rp = p.q_ptr + b * (p.n_blk + 1);
-  const int e0 = rp[qb];
-  const int n_it = rp[qb + 1] - e0;
-  const int32_t* list = p.q_idx + int64_t(b) * p.cap + e0;
-  const int row0 = b * p.t_pad + qb * kB;
+  const int warp = threadIdx.x >> 5;
+  const int G = p.hq / p.hkv;
   constexpr uint32_t T_S0 = 0, T_DP = 256, T_DQ = 384;
+  constexpr int NCONS = 1 + 128 * kNWG;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
     for (int s = 0; s < NSK; ++s) {
       tc::mbar_init(k_full + s, 1);
       tc::mbar_init(k_empty + s, 1);
@@ -478,7 +639,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(dp_free, 128 * kNWG);
     tc::mbar_init(ds_ready, 128 * kNWG);
     tc::mbar_init(dq_final, 1);
+    tc::mbar_init(dq_free, 128 * kNWG);
     tc::mbar_init(drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(item_full + s, 1);
+      tc::mbar_init(item_empty + s, NCONS);
+    }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -487,145 +653,201 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  auto wait_u = [&](uint64_t* b_, uint32_t par) {
+    return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_bwd));
+  };
 
   if (warp == kWTma) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_it > 0) {
+    if (tc::elect_one()) {
       tc::tma_prefetch_desc(&tm_q);
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
       tc::tma_prefetch_desc(&tm_do);
-      tc::mbar_arrive_expect_tx(q_full, 2 * TILE);
-      for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sQ + c * kChunk, &tm_q, q_full, c * 64, h, row0);
-      for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sDO + c * kChunk, &tm_do, q_full, c * 64, h, row0);
+    }
+    __syncwarp();
+    int kt = 0, vt = 0, nq = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+      const int it = fetch_item(p.sched + 4, p.dq_items, item_ring + (k & 1), item_full + (k & 1));
+      if (it < 0) break;
+      const DqItem I = decode_dq(p, it);
+      if (I.n == 0) continue;
+      const int g = I.h / G;
+      const int row0 = I.b * p.t_pad + I.qb * kB;
+      if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
+      if (tc::elect_one()) {
+        tc::mbar_arrive_expect_tx(q_full, 2 * TILE);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sQ + c * kChunk, &tm_q, q_full, c * 64, I.h, row0);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sDO + c * kChunk, &tm_do, q_full, c * 64, I.h, row0);
+      }
+      __syncwarp();
       // Use order: K(0), K(1), V(0), K(2), V(1), ...: K runs ahead of V.
       int kj = 0, vj = 0;
-      bool ok = true;
-      while (ok && (kj < n_it || vj < n_it)) {
-        const bool do_k = kj < n_it && kj <= vj + 1;
+      while (kj < I.n || vj < I.n) {
+        const bool do_k = kj < I.n && kj <= vj + 1;
         const int jj = do_k ? kj : vj;
-        const int krow = b * p.t_pad + (list[jj] >> 1) * kB;
-        if (do_k) {
-          const int s = jj % NSK;
-          if (!(ok = tc::mbar_wait(k_empty + s, ((jj / NSK) & 1) ^ 1, abort_flag, &g_status_bwd))) break;
-          tc::mbar_arrive_expect_tx(k_full + s, TILE);
-          for (int c = 0; c < NCH; ++c)
-            tc::tma_load_3d(sK + s * TILE + c * kChunk, &tm_k, k_full + s, c * 64, g, krow);
-          ++kj;
-        } else {
-          const int s = jj % NSV;
-          if (!(ok = tc::mbar_wait(v_empty + s, ((jj / NSV) & 1) ^ 1, abort_flag, &g_status_bwd))) break;
-          tc::mbar_arrive_expect_tx(v_full + s, TILE);
-          for (int c = 0; c < NCH; ++c)
-            tc::tma_load_3d(sV + s * TILE + c * kChunk, &tm_v, v_full + s, c * 64, g, krow);
-          ++vj;
+        const int krow = I.b * p.t_pad + (I.list[jj] >> 1) * kB;
+        const int ns = do_k ? NSK : NSV;
+        const int gx = (do_k ? kt : vt) + jj, s = gx % ns;
+        if (!(ok = wait_u((do_k ? k_empty : v_empty) + s, ((gx / ns) & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          uint64_t* fb = (do_k ? k_full : v_full) + s;
+          uint8_t* dst = (do_k ? sK : sV) + s * TILE;
+          tc::mbar_arrive_expect_tx(fb, TILE);
+          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(dst + c * kChunk, do_k ? &tm_k : &tm_v, fb, c * 64, g, krow);
         }
+        __syncwarp();
+        if (do_k) ++kj; else ++vj;
       }
-      if (*abort_flag) {
-        volatile int never = 0;
-        for (int jj = (kj > NSK ? kj - NSK : 0); jj < kj; ++jj)
-          tc::mbar_wait(k_full + (jj % NSK), (jj / NSK) & 1, &never, &g_status_bwd, 100000000ull);
-        for (int jj = (vj > NSV ? vj - NSV : 0); jj < vj; ++jj)
-          tc::mbar_wait(v_full + (jj % NSV), (jj / NSV) & 1, &never, &g_status_bwd, 100000000ull);
-      }
+      kt += kj;
+      vt += vj;
+      ++nq;
+    }
+    if (*abort_flag && tc::elect_one()) {
+      volatile int never = 0;
+      for (int jj = (kt > NSK ? kt - NSK : 0); jj < kt; ++jj)
+        tc::mbar_wait(k_full + (jj % NSK), (jj / NSK) & 1, &never, &g_status_bwd, 100000000ull);
+      for (int jj = (vt > NSV ? vt - NSV : 0); jj < vt; ++jj)
+        tc::mbar_wait(v_full + (jj % NSV), (jj / NSV) & 1, &never, &g_status_bwd, 100000000ull);
     }
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ MMA issuer
     // Per key tile j: dP(j+1) as soon as dP(j) has been read, dQ(j) once dS(j)
     // is in TMEM, then S(j+2) into the buffer dS(j) came from.
-    if (lane == 0 && n_it > 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_q = tc::idesc_bf16(128, D, false, true);
-      const uint32_t aQ = tc::smem_u32(sQ), aDO = tc::smem_u32(sDO), aK = tc::smem_u32(sK),
-                     aV = tc::smem_u32(sV);
-      auto issue_s = [&](int jj) -> bool {  // S(jj) = Q K^T into buffer jj % 2
-        const int s = jj % NSK;
-        if (!tc::mbar_wait(k_full + s, (jj / NSK) & 1, abort_flag, &g_status_bwd)) return false;
-        tc::tc_fence_after();
+    constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_q = tc::idesc_bf16(128, D, false, true);
+    const uint64_t dQ_ = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
+    const uint64_t dDO_ = tc::smem_desc(tc::smem_u32(sDO), 16, 1024);
+    const uint64_t dKk = tc::smem_desc(tc::smem_u32(sK), 16, 1024);      // K as K-major B
+    const uint64_t dKm = tc::smem_desc(tc::smem_u32(sK), kChunk, 1024);  // K as MN-major B
+    const uint64_t dV_ = tc::smem_desc(tc::smem_u32(sV), 16, 1024);
+    int kt = 0, vt = 0, tb = 0, nq = 0;
+    auto issue_s = [&](int jj) -> bool {  // S(jj) = Q K^T into buffer (tb + jj) % 2
+      const int gk = kt + jj, s = gk % NSK, buf = (tb + jj) & 1;
+      if (!wait_u(k_full + s, (gk / NSK) & 1)) return false;
+      tc::tc_fence_after();
+      if (tc::elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-          tc::mma_ss(tmem + T_S0 + (jj & 1) * 128, tc::smem_desc(aQ + off, 16, 1024),
-                     tc::smem_desc(aK + s * TILE + off, 16, 1024), idesc_s, k > 0);
+          const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
+          tc::mma_ss(tmem + T_S0 + buf * 128, dQ_ + off, dKk + ((s * TILE) >> 4) + off, idesc_s, k > 0);
         }
-        tc::mma_commit(s_full + (jj & 1));
-        return true;
-      };
-      auto issue_dp = [&](int jj) -> bool {  // dP(jj) = dO V^T
-        const int s = jj % NSV;
-        if (!tc::mbar_wait(v_full + s, (jj / NSV) & 1, abort_flag, &g_status_bwd)) return false;
-        tc::tc_fence_after();
+        tc::mma_commit(s_full + buf);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int jj) -> bool {  // dP(jj) = dO V^T
+      const int gv = vt + jj, s = gv % NSV;
+      if (!wait_u(v_full + s, (gv / NSV) & 1)) return false;
+      tc::tc_fence_after();
+      if (tc::elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kChunk + (k & 3) * 32;
-          tc::mma_ss(tmem + T_DP, tc::smem_desc(aDO + off, 16, 1024),
-                     tc::smem_desc(aV + s * TILE + off, 16, 1024), idesc_s, k > 0);
+          const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
+          tc::mma_ss(tmem + T_DP, dDO_ + off, dV_ + ((s * TILE) >> 4) + off, idesc_s, k > 0);
         }
         tc::mma_commit(dp_full);
         tc::mma_commit(v_empty + s);
-        return true;
-      };
-      bool ok = tc::mbar_wait(q_full, 0, abort_flag, &g_status_bwd);
-      ok = ok && issue_s(0);
-      if (ok && n_it > 1) ok = issue_s(1);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto commit = [&](uint64_t* b_) {
+      if (tc::elect_one()) tc::mma_commit(b_);
+      __syncwarp();
+    };
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
+      const int it = item_ring[k & 1];
+      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
+      __syncwarp();
+      if (it < 0) break;
+      const DqItem I = decode_dq(p, it);
+      const int n = I.n;
+      if (n == 0) continue;
+      if (!(ok = wait_u(q_full, nq & 1))) break;
+      ok = issue_s(0);
+      if (ok && n > 1) ok = issue_s(1);
       ok = ok && issue_dp(0);
-      for (int jj = 0; ok && jj < n_it; ++jj) {
-        if (jj + 1 < n_it) {
-          if (!(ok = tc::mbar_wait(dp_free, jj & 1, abort_flag, &g_status_bwd))) break;
+      if (ok && n == 1) commit(q_empty);  // Q and dO have been read by every MMA issued
+      for (int jj = 0; ok && jj < n; ++jj) {
+        if (jj + 1 < n) {
+          if (!(ok = wait_u(dp_free, (tb + jj) & 1))) break;
           if (!(ok = issue_dp(jj + 1))) break;
+          if (jj + 2 == n) commit(q_empty);  // the item's last S and last dP are issued
         }
-        if (!(ok = tc::mbar_wait(ds_ready, jj & 1, abort_flag, &g_status_bwd))) break;
+        if (!(ok = wait_u(ds_ready, (tb + jj) & 1))) break;
+        if (jj == 0 && nq > 0 && !(ok = wait_u(dq_free, (nq - 1) & 1))) break;
         tc::tc_fence_after();
-        const int s = jj % NSK;
+        const int gk = kt + jj, s = gk % NSK;
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < kB / 16; ++k)  // dQ += dS K, dS packed bf16 in S buffer jj % 2
-          mma_ts(tmem + T_DQ, wg_a(tmem + T_S0 + (jj & 1) * 128, k, 0),
-                 tc::smem_desc(aK + s * TILE + k * 2048, kChunk, 1024), idesc_q, (jj > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(k_empty + s);
-        if (jj + 2 < n_it && !(ok = issue_s(jj + 2))) break;  // buffer jj % 2: dS(jj) read above
+          for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K, dS packed bf16 in S buffer (tb+jj) % 2
+            mma_ts(tmem + T_DQ, wg_a(tmem + T_S0 + ((tb + jj) & 1) * 128, kk),
+                   dKm + ((s * TILE) >> 4) + ((kk * 2048) >> 4), idesc_q, (jj > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(k_empty + s);
+        }
+        __syncwarp();
+        if (jj + 2 < n && !(ok = issue_s(jj + 2))) break;  // the buffer dS(jj) came from
       }
-      if (ok) tc::mma_commit(dq_final);
-      if (*abort_flag) {
-        volatile int never = 0;
-        tc::mma_commit(drain);
-        tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
-      }
+      if (!ok) break;
+      commit(dq_final);
+      kt += n;
+      vt += n;
+      tb += n;
+      ++nq;
+    }
+    if (*abort_flag && tc::elect_one()) {
+      volatile int never = 0;
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
     }
     __syncwarp();
   } else if (warp < 4 * kNWG) {
     // ------------------------------------------------------------ compute warpgroups
     const int w = warp >> 2;          // key columns [32w, 32w+32) of this warpgroup
     const int r = threadIdx.x & 127;  // query row = TMEM lane
-    const int i = qb * kB + r;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     constexpr int ESZ = F32OUT ? 4 : 2;
     constexpr int DW = D / kNWG;
-    uint8_t* dq_row = static_cast<uint8_t*>(p.dq) + ((int64_t(row0 + r) * p.hq + h) * D + w * DW) * ESZ;
-    auto wait_all = [&](uint64_t* b_, uint32_t par) {
-      return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_bwd));
-    };
-    if (n_it == 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
+    int tb = 0, nq = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!wait_u(item_full + (k & 1), (k >> 1) & 1)) break;
+      const int it = item_ring[k & 1];
+      tc::mbar_arrive(item_empty + (k & 1));
+      if (it < 0) break;
+      const DqItem I = decode_dq(p, it);
+      const int row0 = I.b * p.t_pad + I.qb * kB;
+      uint8_t* dq_row = static_cast<uint8_t*>(p.dq) + ((int64_t(row0 + r) * p.hq + I.h) * D + w * DW) * ESZ;
+      if (I.n == 0) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int c = 0; c < DW * ESZ / 16; ++c) reinterpret_cast<uint4*>(dq_row)[c] = z;
-    } else {
-      const int64_t vec = (int64_t(b) * p.hq + h) * p.t_pad + i;
+        for (int c = 0; c < DW * ESZ / 16; ++c) reinterpret_cast<uint4*>(dq_row)[c] = z;
+        continue;
+      }
+      const int64_t vec = (int64_t(I.b) * p.hq + I.h) * p.t_pad + I.qb * kB + r;
       const float nlse2 = -p.lse[vec] * kLog2e;
       const float drow = p.dvec[vec];
-      const uint32_t* qmask_row = reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(b) * p.cap + e0) * kB + r) + w;
-      bool ok = true;
-      int entry = list[0];
+      const uint32_t* qmask_row =
+          reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(I.b) * p.cap + I.e0) * kB + r) + w;
+      int entry = I.list[0];
       uint32_t mk = (entry & 1) ? 0u : qmask_row[0];
-      for (int jj = 0; jj < n_it; ++jj) {
+      for (int jj = 0; jj < I.n; ++jj) {
         const bool full = entry & 1;
         const uint32_t mcur = mk;  // this group's 32 key columns
-        if (jj + 1 < n_it) {
-          entry = list[jj + 1];
+        if (jj + 1 < I.n) {
+          entry = I.list[jj + 1];
           if (!(entry & 1)) mk = qmask_row[int64_t(jj + 1) * kB * 4];
         }
-        const uint32_t tS = tmem + lane_base + T_S0 + (jj & 1) * 128;
-        if (!wait_all(s_full + (jj & 1), (jj >> 1) & 1)) { ok = false; break; }
+        const int gt = tb + jj;
+        const uint32_t tS = tmem + lane_base + T_S0 + (gt & 1) * 128;
+        if (!wait_u(s_full + (gt & 1), (gt >> 1) & 1)) { ok = false; break; }
         tc::tc_fence_after();
         float pf[kCW];
         {
@@ -640,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!((mcur >> c) & 1u)) pf[c] = 0.f;
           }
         }
-        if (!wait_all(dp_full, jj & 1)) { ok = false; break; }
+        if (!wait_u(dp_full, gt & 1)) { ok = false; break; }
         tc::tc_fence_after();
         {
           uint32_t dpv[kCW];
@@ -659,16 +881,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_before();
         tc::mbar_arrive(ds_ready);
       }
-      if (ok && wait_all(dq_final, 0)) {
-        tc::tc_fence_after();
+      if (!ok || !wait_u(dq_final, nq & 1)) { ok = false; break; }
+      tc::tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < DW / 16; ++c) {
-          uint32_t v[16];
-          tc::tmem_ld16(tmem + lane_base + T_DQ + w * DW + c * 16, v);
-          tc::tmem_ld_wait();
-          store_row16<F32OUT>(dq_row + c * 16 * ESZ, v, p.scale);
-        }
+      for (int c = 0; c < DW / 16; ++c) {
+        uint32_t v[16];
+        tc::tmem_ld16(tmem + lane_base + T_DQ + w * DW + c * 16, v);
+        tc::tmem_ld_wait();
+        store_row16<F32OUT>(dq_row + c * 16 * ESZ, v, p.scale, false);
       }
+      tc::tc_fence_before();
+      tc::mbar_arrive(dq_free);
+      tb += I.n;
+      ++nq;
     }
   }
 
@@ -676,15 +901,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   if (warp == kWMma) tc::tmem_dealloc(tmem, 512);
+  rearm_counter(p.sched + 4);
 }
 
 // D[b, h, i] = sum_d dO * O (fp32) for real rows, 0 for pad rows; one warp per
-// (b, i, h) row.
+// (b, i, h) row.  With fp32 gradients it also zeroes dK and dV, which the
+// chunks of long key columns add into.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dout,
                                                       const int32_t* __restrict__ n_tokens, int32_t t_pad,
-                                                      int32_t hq, int64_t n_rows, float* __restrict__ dvec) {
+                                                      int32_t hq, int64_t n_rows, float* __restrict__ dvec,
+                                                      float4* __restrict__ zero_a, float4* __restrict__ zero_b,
+                                                      int64_t n_zero4) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
   for (int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < n_rows; row += warps) {
@@ -693,26 +922,45 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const int b = int(bt / t_pad), i = int(bt % t_pad);
     float s = 0.f;
     if (i < n_tokens[b]) {
-      constexpr int PER = D / 32;  // elements per lane
+      constexpr int PER = D / 32;  // elements per lane: one 8- or 4-byte load of each
       const __nv_bfloat16* a = o + row * D + lane * PER;
       const __nv_bfloat16* c = dout + row * D + lane * PER;
+      if (PER == 4) {
+        const uint2 va = *reinterpret_cast<const uint2*>(a), vc = *reinterpret_cast<const uint2*>(c);
+        s = __uint_as_float(va.x << 16) * __uint_as_float(vc.x << 16) +
+            __uint_as_float(va.x & 0xffff0000u) * __uint_as_float(vc.x & 0xffff0000u) +
+            __uint_as_float(va.y << 16) * __uint_as_float(vc.y << 16) +
+            __uint_as_float(va.y & 0xffff0000u) * __uint_as_float(vc.y & 0xffff0000u);
+      } else {
 #pragma unroll
-      for (int e = 0; e < PER; ++e) s += __bfloat162float(a[e]) * __bfloat162float(c[e]);
+        for (int e = 0; e < PER; ++e) s += __bfloat162float(a[e]) * __bfloat162float(c[e]);
+      }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     }
     if (lane == 0) dvec[(int64_t(b) * hq + h) * t_pad + i] = s;
   }
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < n_zero4; k += int64_t(gridDim.x) * blockDim.x) {
+    zero_a[k] = z;
+    zero_b[k] = z;
+  }
 }
 
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
+int num_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  return sms;
+}
+
 int grid_for(int64_t work, int per_block) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (work + per_block - 1) / per_block;
-  const int64_t cap = int64_t(sms) * 8;
+  const int64_t cap = int64_t(num_sms()) * 8;
   return int(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
@@ -723,9 +971,10 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   const int64_t rows = int64_t(tree->n_trees) * tree->t_pad;
   float* dvec = static_cast<float*>(ws);  // workspace: D [B, Hq, T] fp32
   const int64_t n_rows = rows * hq;
+  const int64_t n_zero4 = F32OUT ? rows * hkv * D / 4 : 0;
   bwd_pre_kernel<D><<<grid_for(n_rows * 32, 256), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), tree->n_tokens,
-      tree->t_pad, hq, n_rows, dvec);
+      tree->t_pad, hq, n_rows, dvec, static_cast<float4*>(dk), static_cast<float4*>(dv), n_zero4);
   TPA_CUDA_TRY(cudaGetLastError());
 
   CUtensorMap tq, tk, tv, tdo;
@@ -745,21 +994,30 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.q_ptr = mask->q_ptr;
   prm.q_idx = mask->q_idx;
   prm.qmask = reinterpret_cast<const uint4*>(mask->qmask);
+  prm.sched = mask->sched;
   prm.t_pad = tree->t_pad;
   prm.n_blk = mask->n_blk;
   prm.cap = mask->cap;
   prm.hq = hq;
   prm.hkv = hkv;
+  const int G = hq / hkv;
+  // Chunks of long key columns add into zeroed fp32 rows; bf16 outputs keep
+  // one item per column.
+  prm.kv_chunk = F32OUT ? kKvChunk : G * mask->n_blk;
+  prm.kv_nchunk = (G * mask->n_blk + prm.kv_chunk - 1) / prm.kv_chunk;
+  prm.kv_items = tree->n_trees * hkv * mask->n_blk * prm.kv_nchunk;
+  prm.dq_items = tree->n_trees * hq * mask->n_blk;
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
+  const int sms = num_sms();
   TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_kv_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     KvCfg<D>::BYTES));
-  attn_bwd_kv_kernel<D, F32OUT><<<dim3(mask->n_blk, hkv, tree->n_trees), kThreads, KvCfg<D>::BYTES, st>>>(
+  attn_bwd_kv_kernel<D, F32OUT><<<prm.kv_items < sms ? prm.kv_items : sms, kThreads, KvCfg<D>::BYTES, st>>>(
       tq, tk, tv, tdo, prm);
   TPA_CUDA_TRY(cudaGetLastError());
   TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     DqCfg<D>::BYTES));
-  attn_bwd_dq_kernel<D, F32OUT><<<dim3(mask->n_blk, hq, tree->n_trees), kThreads, DqCfg<D>::BYTES, st>>>(
+  attn_bwd_dq_kernel<D, F32OUT><<<prm.dq_items < sms ? prm.dq_items : sms, kThreads, DqCfg<D>::BYTES, st>>>(
       tq, tk, tv, tdo, prm);
   TPA_CUDA_TRY(cudaGetLastError());
   return TPA_OK;

@@ -220,15 +220,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     for (int k = 0; ok; ++k) {
       // fetch the next work item and hand it to the other roles
       if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
-      int it = 0;
-      if (lane == 0) it = int(atomicAdd(p.sched, 1u));
-      it = __shfl_sync(0xffffffffu, it, 0);
+      uint32_t u = 0;
+      if (lane == 0) u = atomicAdd(p.sched, 1u);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      const int it = u < uint32_t(p.n_items) ? int(u) : -1;  // unsigned: no index below 0
       if (tc::elect_one()) {
-        item_ring[k & 1] = it < p.n_items ? it : -1;
+        item_ring[k & 1] = it;
         tc::mbar_arrive(item_full + (k & 1));
       }
       __syncwarp();
-      if (it >= p.n_items) break;
+      if (it < 0) break;
       const Item I = decode_item<NH>(p, it);
       if (I.n_it == 0) continue;
       const int32_t* list = p.q_idx + int64_t(I.b) * p.cap + I.e0;

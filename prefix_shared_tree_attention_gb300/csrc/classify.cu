@@ -87,13 +87,13 @@ __global__ void __launch_bounds__(1024) csr_kernel(const uint8_t* __restrict__ c
     scan_s[line] += add;
     __syncthreads();
   }
+  if (b == 0 && dir == 0 && line < 16) sched[line] = 0;  // work counters of the attention kernels
   if (line >= n_blk) return;
   int32_t* ptr = (dir == 0 ? q_ptr : k_ptr) + int64_t(b) * (n_blk + 1);
   int32_t* idx = (dir == 0 ? q_idx : k_idx) + int64_t(b) * cap;
   int pos = scan_s[line] - cnt;
   ptr[line] = pos;
   if (line == n_blk - 1) ptr[n_blk] = scan_s[line];
-  if (b == 0 && dir == 0 && line < 16) sched[line] = 0;  // work counters of the attention kernels
   for (int o = 0; o < n_blk; ++o) {
     const uint8_t v = c[line * s_line + o * s_elem];
     if (v != TPA_BLOCK_EMPTY) idx[pos++] = 2 * o + (v == TPA_BLOCK_FULL ? 1 : 0);

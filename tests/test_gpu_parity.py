@@ -76,6 +76,37 @@ def test_classify_workloads(tpa, cid):
     _check_mask(tpa, pk, mask, cfg.max_tokens_per_mb, check_bits=cid in (1, 2))
 
 
+@pytest.mark.parametrize("T", [128, 384, 2560])
+def test_work_counters_rearmed(tpa, T):
+    """Classification zeroes all 16 work counters whatever the block count,
+    and every attention call leaves them at zero: a mask buffer that starts
+    as 0xFF bytes and is used for two forward+backward passes gives the
+    oracle's result both times."""
+    rng = np.random.default_rng(700 + T)
+    seqs = random_small_sequences(rng, 6, min(T, 400), 3, min_len=1)
+    pk = oracle.tree_pack(seqs, T)
+    tree = tpa.tree_pack(seqs, T)
+    dtree = tree.upload("cuda")
+    nbytes = int(tpa.lib().tpa_blockmask_bytes(tree.n_trees, T))
+    mask = tpa.BlockMask(tree.n_trees, T, "cuda", buf=torch.full((nbytes,), 255, dtype=torch.uint8, device="cuda"))
+    tpa.block_classify(dtree, out=mask)
+    assert torch.all(mask.arrays()["sched"] == 0)
+    B = tree.n_trees
+    (q, k, v, do), (qc, kc, vc, doc) = random_inputs(B, T, 4, 2, 64, T)
+    for _ in range(2):
+        o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+        dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do)
+        tpa.sync_status()
+        assert torch.all(mask.arrays()["sched"] == 0)
+        for b, t in enumerate(pk.trees):
+            O, _ = oracle.attn_forward(t, qc[b], kc[b], vc[b], t_pad=T)
+            dQ, dK, dV = oracle.attn_backward(t, qc[b], kc[b], vc[b], doc[b], t_pad=T)
+            assert_attn_close(o[b], O, f"O tree {b}")
+            assert_attn_close(dq[b], dQ, f"dQ tree {b}")
+            assert_attn_close(dk[b], dK, f"dK tree {b}")
+            assert_attn_close(dv[b], dV, f"dV tree {b}")
+
+
 # ---------------------------------------------------------------- attention, full oracle
 
 CASES = [
