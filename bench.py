@@ -242,7 +242,7 @@ def run_gpu(args, rank, world, local):
     lp_out = (torch.empty((B, T), dtype=torch.float32, device=dev), torch.empty((B, T), dtype=torch.float32, device=dev),
               torch.empty(N, dtype=torch.float32, device=dev), torch.empty(N, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream(dev)
-    n_launch_per_step = 2 + 1 + 2 + 2  # classify+csr, fwd, bwd pre+main (fp32 grads), rows+regather
+    n_launch_per_step = 3 + 1 + 3 + 2  # classify+csr+bit masks, fwd, bwd pre+KV+dQ, rows+regather
 
     def step(ev=None):
         if ev: ev[0].record(stream)
