@@ -12,17 +12,21 @@
 //      chunks of long key columns add into).
 //  (2) KV kernel: work items are (key tile, kv head, tree, chunk of up to 64
 //      steps of that key tile's column), a step being one (query head, query
-//      tile) pair of the per-key-block CSR.  Per step the MMA issuer runs
-//      S^T = K Q^T and dP^T = V dO^T; four compute warpgroups (thread r = key
-//      row r = TMEM lane r; warpgroup w = query columns [32w, 32w+32)) write
-//      P^T and dS^T back into TMEM as packed bf16, and the issuer runs
-//      dV += P^T dO and dK += dS^T Q with A read from TMEM.  A key only sees
-//      the query interval [j, E[j]], applied on PARTIAL tiles.
+//      tile) pair of the per-key-block CSR, run as two units of 64 queries.
+//      Per unit the MMA issuer runs S^T = K Q^T and dP^T = V dO^T; four compute
+//      warpgroups (thread r = key row r = TMEM lane r; warpgroup w = query
+//      columns of the unit) write P^T and dS^T back into TMEM as packed bf16,
+//      and the issuer runs dV += P^T dO and dK += dS^T Q with A read from
+//      TMEM.  Two units are in flight, one per pair of warpgroups (units of
+//      even parity to warpgroups 0-1, odd to 2-3), so one pair's TMEM round
+//      trips overlap the other pair's work and the MMAs of both.  A key only sees the query interval
+//      [j, E[j]], applied on PARTIAL tiles.
 //  (3) dQ kernel: work items are (query tile, query head, tree); it walks the
-//      query block's key tiles like the forward, recomputes S = Q K^T (double
-//      buffered in TMEM) and dP = dO V^T, forms dS = P (dP - D) with the
-//      forward's LSE and the partial-tile bit masks, writes dS as packed bf16
-//      into TMEM and accumulates dQ += dS K in TMEM; dQ is stored once.
+//      query block's key tiles like the forward, in units of 64 keys, three
+//      units in flight (taken alternately by two warpgroup pairs):
+//      S = Q K^T and dP = dO V^T, dS = P (dP - D) with the
+//      forward's LSE and the partial-tile bit masks, dS written as packed
+//      bf16 into TMEM, dQ += dS K accumulated in TMEM; dQ is stored once.
 // Both main kernels are persistent: one CTA per SM takes items from a counter
 // in the block-mask buffer, barrier phases run on across items, and the issuer
 // warps run converged with an elected lane issuing each copy, MMA and commit.
@@ -43,13 +47,13 @@ namespace {
 __device__ unsigned int g_status_bwd = 0;
 
 constexpr int kB = 128;
-constexpr uint32_t kChunk = 128 * 128;  // bytes of a 128-row x 64-col bf16 tile
+constexpr uint32_t kChunk = 128 * 128;    // bytes of a 128-row x 64-col bf16 tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kSmemMax = 232448;   // 227 KB opt-in per CTA
 constexpr int kNWG = 4;                    // compute warpgroups per CTA
-constexpr int kCW = kB / kNWG;             // columns per warpgroup (32)
 constexpr int kThreads = 128 * kNWG + 64;  // + TMA warp + MMA warp
 constexpr int kWTma = 4 * kNWG, kWMma = 4 * kNWG + 1;
+constexpr int kCW = kB / kNWG;             // query or key columns per warpgroup (32)
 constexpr int kKvChunk = 64;               // steps per KV work item (fp32 gradients)
 
 struct BwdParams {
@@ -67,7 +71,7 @@ struct BwdParams {
   const uint4* qmask;
   uint32_t* sched;      // work counters: [2..3] KV kernel, [4..5] dQ kernel
   int32_t t_pad, n_blk, cap, hq, hkv;
-  int32_t kv_chunk, kv_nchunk, kv_items, dq_items;
+  int32_t n_trees, kv_chunk, kv_nchunk, kv_items, dq_items;
   float scale, scale_log2;
 };
 
@@ -118,11 +122,6 @@ __device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16
   }
 }
 
-// Packed bf16 A operand written by the warpgroups: warpgroup w owns columns
-// [32w, 32w+32) of the region it read and writes its 32 K-values packed into
-// the first 16 of them.
-__device__ __forceinline__ uint32_t wg_a(uint32_t base, int k) { return base + 32 * (k >> 1) + 8 * (k & 1); }
-
 // Item fetch shared by the producers of both kernels: one lane takes the next
 // index from the counter, the elected lane publishes it.
 // Returns -1 once the items are used up.
@@ -152,23 +151,33 @@ __device__ __forceinline__ void rearm_counter(uint32_t* ctr) {
 }
 
 // =========================================================================== KV kernel
+//
+// A step is one (query head, 128-query tile) pair of a key tile's column.
+// TMEM: two 128-column regions X = [0, 128) and Y = [128, 256) and the dV, dK
+// accumulators in [256, 256+D) and [256+D, 256+2D).  Step t computes S^T(t)
+// into region A_t and dP^T(t) into the other region B_t, alternating with t
+// (A_t = X for even t).  Compute warpgroup w owns query columns [32w, 32w+32)
+// of both; it writes P^T(t) packed into the first 16 of its S^T columns and
+// dS^T(t) packed into the other 16, so B_t is free as soon as dP^T(t) has
+// been read.  The issuer then runs S^T(t+1) into B_t (= A_{t+1}) while dV(t)
+// and dK(t) read A_t, and dP^T(t+1) into A_t (= B_{t+1}) behind them.
 
 template <int D>
 struct KvCfg {
   static constexpr int NCH = D / 64;
-  static constexpr uint32_t TILE = NCH * kChunk;
+  static constexpr uint32_t TILE = NCH * kChunk;  // 128-row tile of K, V, Q or dO
   static constexpr int NS_FIT = int((kSmemMax - 1024 - 2 * TILE - 4096) / (2 * TILE + 1024));
-  static constexpr int NS = NS_FIT > 3 ? 3 : NS_FIT;  // Q/dO ring depth
+  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;  // Q/dO ring depth
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
   static constexpr uint32_t OFF_Q = OFF_V + TILE;
   static constexpr uint32_t OFF_DO = OFF_Q + NS * TILE;
-  static constexpr uint32_t OFF_LSE = OFF_DO + NS * TILE;   // NS x 128 fp32
-  static constexpr uint32_t OFF_DV = OFF_LSE + NS * kB * 4; // NS x 128 fp32
+  static constexpr uint32_t OFF_LSE = OFF_DO + NS * TILE;    // NS x 128 fp32
+  static constexpr uint32_t OFF_DV = OFF_LSE + NS * kB * 4;  // NS x 128 fp32
   static constexpr uint32_t OFF_BAR = OFF_DV + NS * kB * 4;
-  // kv_full, kv_empty, q_full[NS], q_empty[NS], s_full, dp_full, p_ready, ds_ready, acc_full,
-  // acc_free, drain, item_full[2], item_empty[2]
-  static constexpr int NBAR = 2 + 2 * NS + 7 + 4;
+  // kv_full, kv_empty, q_full[NS], q_empty[NS], s_full, dp_full, p_ready, dp_free, ds_ready,
+  // acc_full, acc_free, drain, item_full[2], item_empty[2]
+  static constexpr int NBAR = 2 + 2 * NS + 8 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;
   static_assert(NS >= 2, "shared memory budget");
@@ -183,14 +192,17 @@ struct KvItem {
 __device__ __forceinline__ KvItem decode_kv(const BwdParams& p, int it) {
   KvItem r;
   const int G = p.hq / p.hkv;
-  const int per_g = p.n_blk * p.kv_nchunk;
-  const int per_b = p.hkv * per_g;
-  r.b = it / per_b;
-  int rem = it - r.b * per_b;
-  r.g = rem / per_g;
-  rem -= r.g * per_g;
-  r.kb = rem / p.kv_nchunk;  // ascending key blocks: the longest columns first
-  const int ch = rem - r.kb * p.kv_nchunk;
+  // Chunk index slowest: first chunk 0 of every column, then chunk 1 of the
+  // columns that have one, and so on, so the empty (column, chunk) pairs
+  // gather at the end; within a chunk level ascending key blocks, the
+  // longest columns first.
+  const int per_ch = p.n_trees * p.hkv * p.n_blk;
+  const int ch = it / per_ch;
+  int rem = it - ch * per_ch;
+  r.b = rem / (p.hkv * p.n_blk);
+  rem -= r.b * (p.hkv * p.n_blk);
+  r.g = rem / p.n_blk;
+  r.kb = rem - r.g * p.n_blk;
   const int32_t* kp = p.k_ptr + r.b * (p.n_blk + 1);
   r.n_col = kp[r.kb + 1] - kp[r.kb];
   r.list = p.k_idx + int64_t(r.b) * p.cap + kp[r.kb];
@@ -198,6 +210,19 @@ __device__ __forceinline__ KvItem decode_kv(const BwdParams& p, int it) {
   const int total = G * r.n_col;
   r.n = total - r.s0 < p.kv_chunk ? total - r.s0 : p.kv_chunk;
   return r;
+}
+
+// Descriptor offset (>> 4) of the 16-column K slice k of a swizzled tile
+// whose 64-column chunks are `chunk` bytes apart (kChunk for 128 rows).
+__device__ __forceinline__ uint32_t kslice(int k, uint32_t chunk = kChunk) {
+  return ((k >> 2) * chunk + (k & 3) * 32) >> 4;
+}
+
+// TMEM column of the packed bf16 A operand for the 16-row K slice kk of a
+// region whose warpgroup w wrote its 32 values packed into columns
+// [32w + half, 32w + half + 16) (half = 0 for P, 16 for dS).
+__device__ __forceinline__ uint32_t packed_a(uint32_t region, int half, int kk) {
+  return region + 32 * (kk >> 1) + half + 8 * (kk & 1);
 }
 
 template <int D, bool F32OUT>
@@ -224,20 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = q_empty + NS;
   uint64_t* dp_full = s_full + 1;
   uint64_t* p_ready = s_full + 2;
-  uint64_t* ds_ready = s_full + 3;
-  uint64_t* acc_full = s_full + 4;
-  uint64_t* acc_free = s_full + 5;
-  uint64_t* drain = s_full + 6;
-  uint64_t* item_full = s_full + 7;   // [2]
-  uint64_t* item_empty = s_full + 9;  // [2]
+  uint64_t* dp_free = s_full + 3;
+  uint64_t* ds_ready = s_full + 4;
+  uint64_t* acc_full = s_full + 5;
+  uint64_t* acc_free = s_full + 6;
+  uint64_t* drain = s_full + 7;
+  uint64_t* item_full = s_full + 8;   // [2]
+  uint64_t* item_empty = s_full + 10;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // [2]
 
   const int warp = threadIdx.x >> 5;
   const int G = p.hq / p.hkv;
-  constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
+  constexpr uint32_t T_DV = 256, T_DK = 256 + D;
   constexpr int NCONS = 1 + 128 * kNWG;  // item consumers: MMA warp (elected lane) + compute threads
+  // region holding S^T of global step gs (dP^T goes to the other one)
+  auto reg_s = [](int gs) -> uint32_t { return (gs & 1) ? 128u : 0u; };
 
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
@@ -249,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(s_full, 1);
     tc::mbar_init(dp_full, 1);
     tc::mbar_init(p_ready, 128 * kNWG);
+    tc::mbar_init(dp_free, 128 * kNWG);
     tc::mbar_init(ds_ready, 128 * kNWG);
     tc::mbar_init(acc_full, 1);
     tc::mbar_init(acc_free, 128 * kNWG);
@@ -282,9 +311,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
-      const int it = fetch_item(p.sched + 2, p.kv_items, item_ring + (k & 1), item_full + (k & 1));
+      // Take indices until one has work (bf16 outputs also need the zero
+      // rows of key tiles no query sees); only that one is handed on.
+      int it = -1;
+      KvItem I;
+      for (;;) {
+        uint32_t u = 0;
+        if ((threadIdx.x & 31) == 0) u = atomicAdd(p.sched + 2, 1u);
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (u >= uint32_t(p.kv_items)) break;  // unsigned: no index below 0
+        I = decode_kv(p, int(u));
+        if (I.n > 0 || (!F32OUT && I.s0 == 0)) {
+          it = int(u);
+          break;
+        }
+      }
+      if (tc::elect_one()) {
+        item_ring[k & 1] = it;
+        tc::mbar_arrive(item_full + (k & 1));
+      }
+      __syncwarp();
       if (it < 0) break;
-      const KvItem I = decode_kv(p, it);
       if (I.n <= 0) continue;
       const int krow = I.b * p.t_pad + I.kb * kB;
       if (!(ok = wait_u(kv_empty, (nk & 1) ^ 1))) break;
@@ -294,9 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sV + c * kChunk, &tm_v, kv_full, c * 64, I.g, krow);
       }
       __syncwarp();
+      ++nk;
       for (int t = 0; t < I.n; ++t) {
-        const int gs = qs + t, st = gs % NS;
-        if (!(ok = wait_u(q_empty + st, ((gs / NS) & 1) ^ 1))) break;
+        const int st = qs % NS;
+        if (!(ok = wait_u(q_empty + st, ((qs / NS) & 1) ^ 1))) break;
         const int s = I.s0 + t;
         const int h = I.g * G + s / I.n_col;
         const int qb = I.list[s % I.n_col] >> 1;
@@ -312,9 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::bulk_load(sDv + st * kB, p.dvec + vec, kB * 4, q_full + st);
         }
         __syncwarp();
+        ++qs;
       }
-      qs += I.n;
-      ++nk;
     }
     if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
       volatile int never = 0;
@@ -325,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Per step: dV as soon as P^T is in TMEM, then S^T of the next step into the
-    // region P^T came from (in order behind dV), then dK once dS^T is in TMEM,
-    // then dP^T of the next step into the region dS^T came from.
+    // Per step t: S^T(t+1) into B_t once dP^T(t) has been read, dV(t) once
+    // P^T(t) is packed, dK(t) once dS^T(t) is packed, then dP^T(t+1) into A_t
+    // (in order behind dV(t) and dK(t), which read it).
     constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_kv = tc::idesc_bf16(128, D, false, true);
     const uint64_t dK_ = tc::smem_desc(tc::smem_u32(sK), 16, 1024);
@@ -336,25 +383,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dDOk = tc::smem_desc(tc::smem_u32(sDO), 16, 1024);      // dO as K-major B
     const uint64_t dQm = tc::smem_desc(tc::smem_u32(sQ), kChunk, 1024);    // Q as MN-major B
     const uint64_t dDOm = tc::smem_desc(tc::smem_u32(sDO), kChunk, 1024);  // dO as MN-major B
-    auto issue_s_dp = [&](int gs, bool s_only, bool dp_only) {  // S^T = K Q^T ; dP^T = V dO^T
+    auto issue_s = [&](int gs) -> bool {  // S^T(gs) = K Q^T into A_gs
+      if (!wait_u(q_full + gs % NS, (gs / NS) & 1)) return false;
+      tc::tc_fence_after();
       const uint32_t so = ((gs % NS) * TILE) >> 4;
       if (tc::elect_one()) {
-        if (!dp_only) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
-            tc::mma_ss(tmem + T_S, dK_ + off, dQk + so + off, idesc_s, k > 0);
-          }
-          tc::mma_commit(s_full);
-        }
-        if (!s_only) {
+        for (int k = 0; k < D / 16; ++k)
+          tc::mma_ss(tmem + reg_s(gs), dK_ + kslice(k), dQk + so + kslice(k), idesc_s, k > 0);
+        tc::mma_commit(s_full);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int gs) {  // dP^T(gs) = V dO^T into B_gs (after issue_s(gs) saw Q/dO land)
+      const uint32_t so = ((gs % NS) * TILE) >> 4;
+      if (tc::elect_one()) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
-            tc::mma_ss(tmem + T_DP, dV_ + off, dDOk + so + off, idesc_s, k > 0);
-          }
-          tc::mma_commit(dp_full);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          tc::mma_ss(tmem + reg_s(gs + 1), dV_ + kslice(k), dDOk + so + kslice(k), idesc_s, k > 0);
+        tc::mma_commit(dp_full);
       }
       __syncwarp();
     };
@@ -373,42 +421,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const KvItem I = decode_kv(p, it);
       const int n = I.n;
       if (n <= 0) continue;
-      if (!(ok = wait_u(kv_full, nk & 1) && wait_u(q_full + qs % NS, (qs / NS) & 1))) break;
+      if (!(ok = wait_u(kv_full, nk & 1))) break;
       tc::tc_fence_after();
-      issue_s_dp(qs, false, false);
+      if (!(ok = issue_s(qs))) break;
+      issue_dp(qs);
+      if (n == 1) commit(kv_empty);  // K and V are read by S^T and dP^T only
       for (int t = 0; ok && t < n; ++t) {
         const int gs = qs + t, st = gs % NS;
-        const bool more = t + 1 < n;
         const uint32_t so = (st * TILE) >> 4;
+        const uint32_t A = tmem + reg_s(gs);
         if (!(ok = wait_u(p_ready, gs & 1))) break;
         if (t == 0 && nk > 0 && !(ok = wait_u(acc_free, (nk - 1) & 1))) break;
+        // S^T(t+1) first: the next step's exponentials then overlap dV(t),
+        // dK(t) and dP^T(t+1).
+        if (t + 1 < n) {
+          if (!(ok = wait_u(dp_free, gs & 1))) break;
+          if (!(ok = issue_s(gs + 1))) break;
+        }
         tc::tc_fence_after();
         if (tc::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kB / 16; ++kk)  // dV += P^T dO, P^T packed bf16 in TMEM
-            mma_ts(tmem + T_DV, wg_a(tmem + T_S, kk), dDOm + so + ((kk * 2048) >> 4), idesc_kv,
+          for (int kk = 0; kk < kB / 16; ++kk)  // dV += P^T dO, P^T packed bf16 in A_t
+            mma_ts(tmem + T_DV, packed_a(A, 0, kk), dDOm + so + ((kk * 2048) >> 4), idesc_kv,
                    (t > 0 || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
-        if (more) {
-          if (!(ok = wait_u(q_full + (gs + 1) % NS, ((gs + 1) / NS) & 1))) break;
-          tc::tc_fence_after();
-          issue_s_dp(gs + 1, true, false);
-        }
         if (!(ok = wait_u(ds_ready, gs & 1))) break;
         tc::tc_fence_after();
         if (tc::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in TMEM
-            mma_ts(tmem + T_DK, wg_a(tmem + T_DP, kk), dQm + so + ((kk * 2048) >> 4), idesc_kv,
+          for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in A_t
+            mma_ts(tmem + T_DK, packed_a(A, 16, kk), dQm + so + ((kk * 2048) >> 4), idesc_kv,
                    (t > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(q_empty + st);
         }
         __syncwarp();
-        if (more) issue_s_dp(gs + 1, false, true);
+        if (t + 1 < n) {
+          issue_dp(gs + 1);
+          if (t + 2 == n) commit(kv_empty);
+        }
       }
       if (!ok) break;
-      commit(kv_empty);  // K, V reads done once these complete
       commit(acc_full);  // dK, dV complete
       qs += n;
       ++nk;
@@ -421,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < 4 * kNWG) {
     // ------------------------------------------------------------ compute warpgroups
-    const int w = warp >> 2;              // query columns [32w, 32w+32) of this warpgroup
+    const int w = warp >> 2;              // query columns [32w, 32w+32) of each step
     const int r = threadIdx.x & 127;      // key row = TMEM lane
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     constexpr int ESZ = F32OUT ? 4 : 2;
@@ -453,18 +506,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = I.kb * kB + r;  // key position owned by this thread
       const int n_tok = p.n_tokens[I.b];
       const int Ej = (j < n_tok) ? p.subtree_end[krow + r] : -1;
+      int entry = I.list[I.s0 % I.n_col];
       for (int t = 0; t < I.n; ++t) {
         const int gs = qs + t, st = gs % NS;
-        const int entry = I.list[(I.s0 + t) % I.n_col];
         const int qb = entry >> 1;
         const bool full = entry & 1;
+        if (t + 1 < I.n) entry = I.list[(I.s0 + t + 1) % I.n_col];
+        const uint32_t tA = tmem + lane_base + reg_s(gs) + kCW * w;      // S^T, then P^T | dS^T
+        const uint32_t tB = tmem + lane_base + reg_s(gs + 1) + kCW * w;  // dP^T
         if (!wait_u(q_full + st, (gs / NS) & 1) || !wait_u(s_full, gs & 1)) { ok = false; break; }
         tc::tc_fence_after();
         // ---- P^T = exp2(S * scale*log2e - LSE*log2e) on this group's 32 query columns
         float pf[kCW];
         {
           uint32_t sv[kCW];
-          tc::tmem_ld32(tmem + lane_base + T_S + kCW * w, sv);
+          tc::tmem_ld32(tA, sv);
           const float4* l4 = reinterpret_cast<const float4*>(sLSE + st * kB + kCW * w);
           tc::tmem_ld_wait();
           const int lo = j - (qb * kB + kCW * w);  // visible query columns: [lo, hi]
@@ -474,10 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 l = l4[c4];
             const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int c = 4 * c4 + u;
-              pf[c] = tc::ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[u] * kLog2e));
-            }
+            for (int e = 0; e < 4; ++e)
+              pf[4 * c4 + e] = tc::ex2(fmaf(__uint_as_float(sv[4 * c4 + e]), p.scale_log2, -lv[e] * kLog2e));
           }
           if (!full) {
 #pragma unroll
@@ -486,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint32_t pw[kCW / 2];
 #pragma unroll
-          for (int u = 0; u < kCW / 2; ++u) pw[u] = tc::pack_bf16(pf[2 * u], pf[2 * u + 1]);
-          tc::tmem_st16(tmem + lane_base + T_S + kCW * w, pw);  // over the first half of what was read
+          for (int e = 0; e < kCW / 2; ++e) pw[e] = tc::pack_bf16(pf[2 * e], pf[2 * e + 1]);
+          tc::tmem_st16(tA, pw);  // first half of this group's S^T columns
           tc::tmem_st_wait();
         }
         tc::tc_fence_before();
@@ -497,9 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_after();
         {
           uint32_t dpv[kCW];
-          tc::tmem_ld32(tmem + lane_base + T_DP + kCW * w, dpv);
-          const float4* d4 = reinterpret_cast<const float4*>(sDv + st * kB + kCW * w);
+          tc::tmem_ld32(tB, dpv);
           tc::tmem_ld_wait();
+          tc::tc_fence_before();
+          tc::mbar_arrive(dp_free);  // B_t may take S^T of the next step now
+          const float4* d4 = reinterpret_cast<const float4*>(sDv + st * kB + kCW * w);
           uint32_t dw[kCW / 2];
 #pragma unroll
           for (int c4 = 0; c4 < kCW / 4; ++c4) {
@@ -510,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dw[2 * c4 + 1] = tc::pack_bf16(pf[c + 2] * (__uint_as_float(dpv[c + 2]) - dd.z),
                                            pf[c + 3] * (__uint_as_float(dpv[c + 3]) - dd.w));
           }
-          tc::tmem_st16(tmem + lane_base + T_DP + kCW * w, dw);
+          tc::tmem_st16(tA + 16, dw);  // second half of this group's S^T columns
           tc::tmem_st_wait();
         }
         tc::tc_fence_before();
@@ -788,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K, dS packed bf16 in S buffer (tb+jj) % 2
-            mma_ts(tmem + T_DQ, wg_a(tmem + T_S0 + ((tb + jj) & 1) * 128, kk),
+            mma_ts(tmem + T_DQ, packed_a(tmem + T_S0 + ((tb + jj) & 1) * 128, 0, kk),
                    dKm + ((s * TILE) >> 4) + ((kk * 2048) >> 4), idesc_q, (jj > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(k_empty + s);
         }
@@ -1005,6 +1061,7 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   // one item per column.
   prm.kv_chunk = F32OUT ? kKvChunk : G * mask->n_blk;
   prm.kv_nchunk = (G * mask->n_blk + prm.kv_chunk - 1) / prm.kv_chunk;
+  prm.n_trees = tree->n_trees;
   prm.kv_items = tree->n_trees * hkv * mask->n_blk * prm.kv_nchunk;
   prm.dq_items = tree->n_trees * hq * mask->n_blk;
   prm.scale = scale;

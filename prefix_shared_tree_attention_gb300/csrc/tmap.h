@@ -30,15 +30,15 @@ inline EncodeTiledFn encode_fn() {
 }
 
 // Tensor [rows][heads][d] bf16, row-major.  A box is 64 head-dim elements
-// (128 bytes, the 128-byte swizzle span) x 1 head x 128 rows, landing in
-// shared memory as 128 swizzled rows of 128 bytes.
+// (128 bytes, the 128-byte swizzle span) x 1 head x `box_rows` rows (128 or
+// 64), landing in shared memory as `box_rows` swizzled rows of 128 bytes.
 inline bool make_rows_heads_d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t heads,
-                              uint64_t d) {
+                              uint64_t d, uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {d, heads, rows};
   const cuuint64_t strides[2] = {d * 2, heads * d * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t box[3] = {64, 1, box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
