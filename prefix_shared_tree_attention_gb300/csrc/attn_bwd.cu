@@ -22,11 +22,11 @@
 //      trips overlap the other pair's work and the MMAs of both.  A key only sees the query interval
 //      [j, E[j]], applied on PARTIAL tiles.
 //  (3) dQ kernel: work items are (query tile, query head, tree); it walks the
-//      query block's key tiles like the forward, in units of 64 keys, three
-//      units in flight (taken alternately by two warpgroup pairs):
-//      S = Q K^T and dP = dO V^T, dS = P (dP - D) with the
-//      forward's LSE and the partial-tile bit masks, dS written as packed
-//      bf16 into TMEM, dQ += dS K accumulated in TMEM; dQ is stored once.
+//      query block's key tiles like the forward, rotating S, dP and packed dS
+//      through three TMEM regions so the next tile's S and dP run while this
+//      tile's dS is formed: dS = P (dP - D) with the forward's LSE and the
+//      partial-tile bit masks, dQ += dS K accumulated in TMEM; dQ is stored
+//      once.
 // Both main kernels are persistent: one CTA per SM takes items from a counter
 // in the block-mask buffer, barrier phases run on across items, and the issuer
 // warps run converged with an elected lane issuing each copy, MMA and commit.
@@ -166,21 +166,24 @@ template <int D>
 struct KvCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = NCH * kChunk;  // 128-row tile of K, V, Q or dO
-  static constexpr int NS_FIT = int((kSmemMax - 1024 - 2 * TILE - 4096) / (2 * TILE + 1024));
-  static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;  // Q/dO ring depth
+  // Q ring one stage deeper than the dO ring: Q(t) feeds S^T(t), which is
+  // issued a step before dP^T(t).  LSE and D travel with dO.
+  static constexpr int NSQ = D == 128 ? 3 : 4;
+  static constexpr int NSD = D == 128 ? 2 : 3;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + TILE;
   static constexpr uint32_t OFF_Q = OFF_V + TILE;
-  static constexpr uint32_t OFF_DO = OFF_Q + NS * TILE;
-  static constexpr uint32_t OFF_LSE = OFF_DO + NS * TILE;    // NS x 128 fp32
-  static constexpr uint32_t OFF_DV = OFF_LSE + NS * kB * 4;  // NS x 128 fp32
-  static constexpr uint32_t OFF_BAR = OFF_DV + NS * kB * 4;
-  // kv_full, kv_empty, q_full[NS], q_empty[NS], s_full, dp_full, p_ready, dp_free, ds_ready,
-  // acc_full, acc_free, drain, item_full[2], item_empty[2]
-  static constexpr int NBAR = 2 + 2 * NS + 8 + 4;
+  static constexpr uint32_t OFF_DO = OFF_Q + NSQ * TILE;
+  static constexpr uint32_t OFF_LSE = OFF_DO + NSD * TILE;    // NSD x 128 fp32
+  static constexpr uint32_t OFF_DV = OFF_LSE + NSD * kB * 4;  // NSD x 128 fp32
+  static constexpr uint32_t OFF_BAR = OFF_DV + NSD * kB * 4;
+  // kv_full, kv_empty, q_full[NSQ], q_empty[NSQ], do_full[NSD], do_empty[NSD], s_full, dp_full,
+  // p_ready, dp_free, ds_ready, acc_full, acc_free, drain, item_full[2], item_empty[2]
+  static constexpr int NBAR = 2 + 2 * NSQ + 2 * NSD + 8 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;
-  static_assert(NS >= 2, "shared memory budget");
+  // No alignment slack: the kernel checks that dynamic shared memory starts
+  // 1024-byte aligned (the swizzled tiles need it).
+  static constexpr uint32_t BYTES = OFF_MISC + 32;
   static_assert(BYTES <= kSmemMax, "shared memory budget");
 };
 
@@ -231,10 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams p) {
   using C = KvCfg<D>;
-  constexpr int NCH = C::NCH, NS = C::NS;
+  constexpr int NCH = C::NCH, NSQ = C::NSQ, NSD = C::NSD;
   constexpr uint32_t TILE = C::TILE;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (tc::smem_u32(smem) & 1023u) {  // uniform over the CTA: every thread leaves
+    if (threadIdx.x == 0) atomicOr(&g_status_bwd, 2u);
+    return;
+  }
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sQ = smem + C::OFF_Q;
@@ -245,8 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bar;
   uint64_t* kv_empty = bar + 1;
   uint64_t* q_full = bar + 2;
-  uint64_t* q_empty = q_full + NS;
-  uint64_t* s_full = q_empty + NS;
+  uint64_t* q_empty = q_full + NSQ;
+  uint64_t* do_full = q_empty + NSQ;
+  uint64_t* do_empty = do_full + NSD;
+  uint64_t* s_full = do_empty + NSD;
   uint64_t* dp_full = s_full + 1;
   uint64_t* p_ready = s_full + 2;
   uint64_t* dp_free = s_full + 3;
@@ -270,9 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
     tc::mbar_init(kv_empty, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSQ; ++s) {
       tc::mbar_init(q_full + s, 1);
       tc::mbar_init(q_empty + s, 1);
+    }
+    for (int s = 0; s < NSD; ++s) {
+      tc::mbar_init(do_full + s, 1);
+      tc::mbar_init(do_empty + s, 1);
     }
     tc::mbar_init(s_full, 1);
     tc::mbar_init(dp_full, 1);
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tm_do);
     }
     __syncwarp();
-    int qs = 0, nk = 0;  // Q ring steps and K/V loads so far
+    int qs = 0, nk = 0, nq_half = 0;  // steps loaded, K/V loads, and a lone Q load in flight
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
@@ -342,32 +355,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       ++nk;
+      int entry = I.list[I.s0 % I.n_col];
       for (int t = 0; t < I.n; ++t) {
-        const int st = qs % NS;
-        if (!(ok = wait_u(q_empty + st, ((qs / NS) & 1) ^ 1))) break;
+        const int sq = qs % NSQ, sd = qs % NSD;
         const int s = I.s0 + t;
         const int h = I.g * G + s / I.n_col;
-        const int qb = I.list[s % I.n_col] >> 1;
+        const int qb = entry >> 1;
+        if (t + 1 < I.n) entry = I.list[(s + 1) % I.n_col];
+        const int qrow = I.b * p.t_pad + qb * kB;
+        const int64_t vec = (int64_t(I.b) * p.hq + h) * p.t_pad + qb * kB;
+        if (!(ok = wait_u(q_empty + sq, ((qs / NSQ) & 1) ^ 1))) break;
         if (tc::elect_one()) {
-          const int qrow = I.b * p.t_pad + qb * kB;
-          const int64_t vec = (int64_t(I.b) * p.hq + h) * p.t_pad + qb * kB;
-          tc::mbar_arrive_expect_tx(q_full + st, 2 * TILE + 2 * kB * 4);
+          tc::mbar_arrive_expect_tx(q_full + sq, TILE);
           for (int c = 0; c < NCH; ++c)
-            tc::tma_load_3d(sQ + st * TILE + c * kChunk, &tm_q, q_full + st, c * 64, h, qrow);
-          for (int c = 0; c < NCH; ++c)
-            tc::tma_load_3d(sDO + st * TILE + c * kChunk, &tm_do, q_full + st, c * 64, h, qrow);
-          tc::bulk_load(sLSE + st * kB, p.lse + vec, kB * 4, q_full + st);
-          tc::bulk_load(sDv + st * kB, p.dvec + vec, kB * 4, q_full + st);
+            tc::tma_load_3d(sQ + sq * TILE + c * kChunk, &tm_q, q_full + sq, c * 64, h, qrow);
         }
         __syncwarp();
+        nq_half = 1;  // this step's Q load is in flight, its dO load not yet
+        if (!(ok = wait_u(do_empty + sd, ((qs / NSD) & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          tc::mbar_arrive_expect_tx(do_full + sd, TILE + 2 * kB * 4);
+          for (int c = 0; c < NCH; ++c)
+            tc::tma_load_3d(sDO + sd * TILE + c * kChunk, &tm_do, do_full + sd, c * 64, h, qrow);
+          tc::bulk_load(sLSE + sd * kB, p.lse + vec, kB * 4, do_full + sd);
+          tc::bulk_load(sDv + sd * kB, p.dvec + vec, kB * 4, do_full + sd);
+        }
+        __syncwarp();
+        nq_half = 0;
         ++qs;
       }
     }
     if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
       volatile int never = 0;
       if (nk > 0) tc::mbar_wait(kv_full, (nk - 1) & 1, &never, &g_status_bwd, 100000000ull);
-      for (int j = (qs > NS ? qs - NS : 0); j < qs; ++j)
-        tc::mbar_wait(q_full + (j % NS), (j / NS) & 1, &never, &g_status_bwd, 100000000ull);
+      const int nq = qs + nq_half;  // Q loads issued
+      for (int j = (nq > NSQ ? nq - NSQ : 0); j < nq; ++j)
+        tc::mbar_wait(q_full + (j % NSQ), (j / NSQ) & 1, &never, &g_status_bwd, 100000000ull);
+      for (int j = (qs > NSD ? qs - NSD : 0); j < qs; ++j)
+        tc::mbar_wait(do_full + (j % NSD), (j / NSD) & 1, &never, &g_status_bwd, 100000000ull);
     }
     __syncwarp();
   } else if (warp == kWMma) {
@@ -384,9 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dQm = tc::smem_desc(tc::smem_u32(sQ), kChunk, 1024);    // Q as MN-major B
     const uint64_t dDOm = tc::smem_desc(tc::smem_u32(sDO), kChunk, 1024);  // dO as MN-major B
     auto issue_s = [&](int gs) -> bool {  // S^T(gs) = K Q^T into A_gs
-      if (!wait_u(q_full + gs % NS, (gs / NS) & 1)) return false;
+      if (!wait_u(q_full + gs % NSQ, (gs / NSQ) & 1)) return false;
       tc::tc_fence_after();
-      const uint32_t so = ((gs % NS) * TILE) >> 4;
+      const uint32_t so = ((gs % NSQ) * TILE) >> 4;
       if (tc::elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -396,8 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    auto issue_dp = [&](int gs) {  // dP^T(gs) = V dO^T into B_gs (after issue_s(gs) saw Q/dO land)
-      const uint32_t so = ((gs % NS) * TILE) >> 4;
+    auto issue_dp = [&](int gs) -> bool {  // dP^T(gs) = V dO^T into B_gs
+      if (!wait_u(do_full + gs % NSD, (gs / NSD) & 1)) return false;
+      tc::tc_fence_after();
+      const uint32_t so = ((gs % NSD) * TILE) >> 4;
       if (tc::elect_one()) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -405,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_commit(dp_full);
       }
       __syncwarp();
+      return true;
     };
     auto commit = [&](uint64_t* b_) {
       if (tc::elect_one()) tc::mma_commit(b_);
@@ -423,12 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n <= 0) continue;
       if (!(ok = wait_u(kv_full, nk & 1))) break;
       tc::tc_fence_after();
-      if (!(ok = issue_s(qs))) break;
-      issue_dp(qs);
+      if (!(ok = issue_s(qs) && issue_dp(qs))) break;
       if (n == 1) commit(kv_empty);  // K and V are read by S^T and dP^T only
       for (int t = 0; ok && t < n; ++t) {
-        const int gs = qs + t, st = gs % NS;
-        const uint32_t so = (st * TILE) >> 4;
+        const int gs = qs + t, sq = gs % NSQ, sd = gs % NSD;
+        const uint32_t soq = (sq * TILE) >> 4, sod = (sd * TILE) >> 4;
         const uint32_t A = tmem + reg_s(gs);
         if (!(ok = wait_u(p_ready, gs & 1))) break;
         if (t == 0 && nk > 0 && !(ok = wait_u(acc_free, (nk - 1) & 1))) break;
@@ -442,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kB / 16; ++kk)  // dV += P^T dO, P^T packed bf16 in A_t
-            mma_ts(tmem + T_DV, packed_a(A, 0, kk), dDOm + so + ((kk * 2048) >> 4), idesc_kv,
+            mma_ts(tmem + T_DV, packed_a(A, 0, kk), dDOm + sod + ((kk * 2048) >> 4), idesc_kv,
                    (t > 0 || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
@@ -451,13 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in A_t
-            mma_ts(tmem + T_DK, packed_a(A, 16, kk), dQm + so + ((kk * 2048) >> 4), idesc_kv,
+            mma_ts(tmem + T_DK, packed_a(A, 16, kk), dQm + soq + ((kk * 2048) >> 4), idesc_kv,
                    (t > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(q_empty + st);
+          tc::mma_commit(q_empty + sq);
+          tc::mma_commit(do_empty + sd);  // after dS^T(t): the compute threads are done with LSE, D
         }
         __syncwarp();
         if (t + 1 < n) {
-          issue_dp(gs + 1);
+          if (!(ok = issue_dp(gs + 1))) break;
           if (t + 2 == n) commit(kv_empty);
         }
       }
@@ -508,13 +536,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Ej = (j < n_tok) ? p.subtree_end[krow + r] : -1;
       int entry = I.list[I.s0 % I.n_col];
       for (int t = 0; t < I.n; ++t) {
-        const int gs = qs + t, st = gs % NS;
+        const int gs = qs + t, st = gs % NSD;  // LSE and D sit in the dO stage
         const int qb = entry >> 1;
         const bool full = entry & 1;
         if (t + 1 < I.n) entry = I.list[(I.s0 + t + 1) % I.n_col];
         const uint32_t tA = tmem + lane_base + reg_s(gs) + kCW * w;      // S^T, then P^T | dS^T
         const uint32_t tB = tmem + lane_base + reg_s(gs + 1) + kCW * w;  // dP^T
-        if (!wait_u(q_full + st, (gs / NS) & 1) || !wait_u(s_full, gs & 1)) { ok = false; break; }
+        if (!wait_u(do_full + st, (gs / NSD) & 1) || !wait_u(s_full, gs & 1)) { ok = false; break; }
         tc::tc_fence_after();
         // ---- P^T = exp2(S * scale*log2e - LSE*log2e) on this group's 32 query columns
         float pf[kCW];
@@ -600,23 +628,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // =========================================================================== dQ kernel
+//
+// A step is one key tile j of the query tile's row.  TMEM: three 128-column
+// regions R0..R2 and the dQ accumulator in [384, 384+D).  S(j) goes to
+// R[j%3] and dP(j) to R[(j+1)%3]; compute warpgroup w owns key columns
+// [32w, 32w+32) and writes dS(j) packed into the first 16 of its S columns.
+// R[(j+1)%3] is free once dP(j) has been read, so S(j+1) and dP(j+1) (into
+// R[(j+2)%3], whose dS(j-1) dQ(j-1) read before them) are issued then, ahead
+// of dQ(j); the next tile's exponentials overlap dQ(j) and dP(j+1).
 
 template <int D>
 struct DqCfg {
   static constexpr int NCH = D / 64;
-  static constexpr uint32_t TILE = NCH * kChunk;
-  static constexpr int NSK = 3;  // K ring (K(j) is read by S(j) and again by dQ(j))
-  static constexpr int NSV = D == 128 ? 1 : 2;
+  static constexpr uint32_t TILE = NCH * kChunk;  // 128-row tile of Q, dO, K or V
+  static constexpr int NSK = D == 128 ? 3 : 6;    // K(j) is read by S(j) and again by dQ(j)
+  static constexpr int NSV = D == 128 ? 2 : 4;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_DO = TILE;
   static constexpr uint32_t OFF_K = 2 * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
   static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
-  // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], dp_full,
-  // dp_free, ds_ready, dq_final, dq_free, drain, item_full[2], item_empty[2]
+  // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, dp_full,
+  // dp_free, ds_ready[2], dq_final, dq_free, drain, item_full[2], item_empty[2]
   static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 8 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;
+  static constexpr uint32_t BYTES = OFF_MISC + 32;  // base checked 1024-byte aligned
   static_assert(BYTES <= kSmemMax, "shared memory budget");
 };
 
@@ -639,6 +675,8 @@ __device__ __forceinline__ DqItem decode_dq(const BwdParams& p, int it) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t rot3(int j) { return uint32_t(j % 3) * 128u; }
+
 template <int D, bool F32OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -647,8 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = DqCfg<D>;
   constexpr int NCH = C::NCH, NSK = C::NSK, NSV = C::NSV;
   constexpr uint32_t TILE = C::TILE;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (tc::smem_u32(smem) & 1023u) {  // uniform over the CTA: every thread leaves
+    if (threadIdx.x == 0) atomicOr(&g_status_bwd, 2u);
+    return;
+  }
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sDO = smem + C::OFF_DO;
   uint8_t* sK = smem + C::OFF_K;
@@ -660,10 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + NSK;
   uint64_t* v_full = k_empty + NSK;
   uint64_t* v_empty = v_full + NSV;
-  uint64_t* s_full = v_empty + NSV;  // [2]
-  uint64_t* dp_full = s_full + 2;
-  uint64_t* dp_free = s_full + 3;
-  uint64_t* ds_ready = s_full + 4;
+  uint64_t* s_full = v_empty + NSV;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* dp_free = s_full + 2;
+  uint64_t* ds_ready = s_full + 3;  // [2]: a fast thread may arrive for tile j+1 early
   uint64_t* dq_final = s_full + 5;
   uint64_t* dq_free = s_full + 6;
   uint64_t* drain = s_full + 7;
@@ -675,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int G = p.hq / p.hkv;
-  constexpr uint32_t T_S0 = 0, T_DP = 256, T_DQ = 384;
+  constexpr uint32_t T_DQ = 384;
   constexpr int NCONS = 1 + 128 * kNWG;
 
   if (threadIdx.x == 0) {
@@ -690,10 +732,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(v_empty + s, 1);
     }
     tc::mbar_init(s_full, 1);
-    tc::mbar_init(s_full + 1, 1);
     tc::mbar_init(dp_full, 1);
     tc::mbar_init(dp_free, 128 * kNWG);
     tc::mbar_init(ds_ready, 128 * kNWG);
+    tc::mbar_init(ds_ready + 1, 128 * kNWG);
     tc::mbar_init(dq_final, 1);
     tc::mbar_init(dq_free, 128 * kNWG);
     tc::mbar_init(drain, 1);
@@ -722,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tm_do);
     }
     __syncwarp();
-    int kt = 0, vt = 0, nq = 0;
+    int gk = 0, gv = 0, nq = 0;  // K tiles, V tiles and Q tiles loaded so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
@@ -739,40 +781,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sDO + c * kChunk, &tm_do, q_full, c * 64, I.h, row0);
       }
       __syncwarp();
-      // Use order: K(0), K(1), V(0), K(2), V(1), ...: K runs ahead of V.
-      int kj = 0, vj = 0;
-      while (kj < I.n || vj < I.n) {
-        const bool do_k = kj < I.n && kj <= vj + 1;
-        const int jj = do_k ? kj : vj;
-        const int krow = I.b * p.t_pad + (I.list[jj] >> 1) * kB;
-        const int ns = do_k ? NSK : NSV;
-        const int gx = (do_k ? kt : vt) + jj, s = gx % ns;
-        if (!(ok = wait_u((do_k ? k_empty : v_empty) + s, ((gx / ns) & 1) ^ 1))) break;
+      ++nq;
+      int entry = I.list[0];
+      for (int j = 0; ok && j < I.n; ++j) {
+        const int krow = I.b * p.t_pad + (entry >> 1) * kB;
+        if (j + 1 < I.n) entry = I.list[j + 1];
+        const int sk = gk % NSK;
+        if (!(ok = wait_u(k_empty + sk, ((gk / NSK) & 1) ^ 1))) break;
         if (tc::elect_one()) {
-          uint64_t* fb = (do_k ? k_full : v_full) + s;
-          uint8_t* dst = (do_k ? sK : sV) + s * TILE;
-          tc::mbar_arrive_expect_tx(fb, TILE);
-          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(dst + c * kChunk, do_k ? &tm_k : &tm_v, fb, c * 64, g, krow);
+          tc::mbar_arrive_expect_tx(k_full + sk, TILE);
+          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sK + sk * TILE + c * kChunk, &tm_k, k_full + sk, c * 64, g, krow);
         }
         __syncwarp();
-        if (do_k) ++kj; else ++vj;
+        ++gk;
+        const int sv = gv % NSV;
+        if (!(ok = wait_u(v_empty + sv, ((gv / NSV) & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          tc::mbar_arrive_expect_tx(v_full + sv, TILE);
+          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sV + sv * TILE + c * kChunk, &tm_v, v_full + sv, c * 64, g, krow);
+        }
+        __syncwarp();
+        ++gv;
       }
-      kt += kj;
-      vt += vj;
-      ++nq;
     }
-    if (*abort_flag && tc::elect_one()) {
+    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
       volatile int never = 0;
-      for (int jj = (kt > NSK ? kt - NSK : 0); jj < kt; ++jj)
+      if (nq > 0) tc::mbar_wait(q_full, (nq - 1) & 1, &never, &g_status_bwd, 100000000ull);
+      for (int jj = (gk > NSK ? gk - NSK : 0); jj < gk; ++jj)
         tc::mbar_wait(k_full + (jj % NSK), (jj / NSK) & 1, &never, &g_status_bwd, 100000000ull);
-      for (int jj = (vt > NSV ? vt - NSV : 0); jj < vt; ++jj)
+      for (int jj = (gv > NSV ? gv - NSV : 0); jj < gv; ++jj)
         tc::mbar_wait(v_full + (jj % NSV), (jj / NSV) & 1, &never, &g_status_bwd, 100000000ull);
     }
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Per key tile j: dP(j+1) as soon as dP(j) has been read, dQ(j) once dS(j)
-    // is in TMEM, then S(j+2) into the buffer dS(j) came from.
     constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_q = tc::idesc_bf16(128, D, false, true);
     const uint64_t dQ_ = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
@@ -780,34 +822,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKk = tc::smem_desc(tc::smem_u32(sK), 16, 1024);      // K as K-major B
     const uint64_t dKm = tc::smem_desc(tc::smem_u32(sK), kChunk, 1024);  // K as MN-major B
     const uint64_t dV_ = tc::smem_desc(tc::smem_u32(sV), 16, 1024);
-    int kt = 0, vt = 0, tb = 0, nq = 0;
-    auto issue_s = [&](int jj) -> bool {  // S(jj) = Q K^T into buffer (tb + jj) % 2
-      const int gk = kt + jj, s = gk % NSK, buf = (tb + jj) & 1;
-      if (!wait_u(k_full + s, (gk / NSK) & 1)) return false;
+    auto issue_sdp = [&](int gt) -> bool {  // S(gt) = Q K^T into R[gt%3]; dP(gt) = dO V^T into R[(gt+1)%3]
+      const int sk = gt % NSK, sv = gt % NSV;
+      if (!wait_u(k_full + sk, (gt / NSK) & 1)) return false;
       tc::tc_fence_after();
       if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
-          tc::mma_ss(tmem + T_S0 + buf * 128, dQ_ + off, dKk + ((s * TILE) >> 4) + off, idesc_s, k > 0);
-        }
-        tc::mma_commit(s_full + buf);
+        for (int k = 0; k < D / 16; ++k)
+          tc::mma_ss(tmem + rot3(gt), dQ_ + kslice(k), dKk + ((sk * TILE) >> 4) + kslice(k), idesc_s, k > 0);
+        tc::mma_commit(s_full);
       }
       __syncwarp();
-      return true;
-    };
-    auto issue_dp = [&](int jj) -> bool {  // dP(jj) = dO V^T
-      const int gv = vt + jj, s = gv % NSV;
-      if (!wait_u(v_full + s, (gv / NSV) & 1)) return false;
+      if (!wait_u(v_full + sv, (gt / NSV) & 1)) return false;
       tc::tc_fence_after();
       if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
-          tc::mma_ss(tmem + T_DP, dDO_ + off, dV_ + ((s * TILE) >> 4) + off, idesc_s, k > 0);
-        }
+        for (int k = 0; k < D / 16; ++k)
+          tc::mma_ss(tmem + rot3(gt + 1), dDO_ + kslice(k), dV_ + ((sv * TILE) >> 4) + kslice(k), idesc_s, k > 0);
         tc::mma_commit(dp_full);
-        tc::mma_commit(v_empty + s);
+        tc::mma_commit(v_empty + sv);
       }
       __syncwarp();
       return true;
@@ -816,6 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tc::elect_one()) tc::mma_commit(b_);
       __syncwarp();
     };
+    int gt = 0, nq = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
@@ -827,35 +861,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = I.n;
       if (n == 0) continue;
       if (!(ok = wait_u(q_full, nq & 1))) break;
-      ok = issue_s(0);
-      if (ok && n > 1) ok = issue_s(1);
-      ok = ok && issue_dp(0);
-      if (ok && n == 1) commit(q_empty);  // Q and dO have been read by every MMA issued
-      for (int jj = 0; ok && jj < n; ++jj) {
-        if (jj + 1 < n) {
-          if (!(ok = wait_u(dp_free, (tb + jj) & 1))) break;
-          if (!(ok = issue_dp(jj + 1))) break;
-          if (jj + 2 == n) commit(q_empty);  // the item's last S and last dP are issued
+      if (!(ok = issue_sdp(gt))) break;
+      if (n == 1) commit(q_empty);  // Q and dO are read by S and dP only
+      for (int j = 0; ok && j < n; ++j) {
+        const int g = gt + j, sk = g % NSK;
+        if (j + 1 < n) {  // the next tile's S and dP once dP(j) has been read
+          if (!(ok = wait_u(dp_free, g & 1))) break;
+          if (!(ok = issue_sdp(g + 1))) break;
+          if (j + 2 == n) commit(q_empty);
         }
-        if (!(ok = wait_u(ds_ready, (tb + jj) & 1))) break;
-        if (jj == 0 && nq > 0 && !(ok = wait_u(dq_free, (nq - 1) & 1))) break;
+        if (!(ok = wait_u(ds_ready + (g & 1), (g >> 1) & 1))) break;
+        if (j == 0 && nq > 0 && !(ok = wait_u(dq_free, (nq - 1) & 1))) break;
         tc::tc_fence_after();
-        const int gk = kt + jj, s = gk % NSK;
         if (tc::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K, dS packed bf16 in S buffer (tb+jj) % 2
-            mma_ts(tmem + T_DQ, packed_a(tmem + T_S0 + ((tb + jj) & 1) * 128, 0, kk),
-                   dKm + ((s * TILE) >> 4) + ((kk * 2048) >> 4), idesc_q, (jj > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(k_empty + s);
+          for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K, dS packed bf16 in R[g%3]
+            mma_ts(tmem + T_DQ, packed_a(tmem + rot3(g), 0, kk), dKm + ((sk * TILE) >> 4) + ((kk * 2048) >> 4),
+                   idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(k_empty + sk);
         }
         __syncwarp();
-        if (jj + 2 < n && !(ok = issue_s(jj + 2))) break;  // the buffer dS(jj) came from
       }
       if (!ok) break;
       commit(dq_final);
-      kt += n;
-      vt += n;
-      tb += n;
+      gt += n;
       ++nq;
     }
     if (*abort_flag && tc::elect_one()) {
@@ -866,12 +895,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < 4 * kNWG) {
     // ------------------------------------------------------------ compute warpgroups
-    const int w = warp >> 2;          // key columns [32w, 32w+32) of this warpgroup
+    const int w = warp >> 2;          // key columns [32w, 32w+32) of each tile
     const int r = threadIdx.x & 127;  // query row = TMEM lane
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     constexpr int ESZ = F32OUT ? 4 : 2;
     constexpr int DW = D / kNWG;
-    int tb = 0, nq = 0;
+    int gt = 0, nq = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!wait_u(item_full + (k & 1), (k >> 1) & 1)) break;
@@ -894,21 +923,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(I.b) * p.cap + I.e0) * kB + r) + w;
       int entry = I.list[0];
       uint32_t mk = (entry & 1) ? 0u : qmask_row[0];
-      for (int jj = 0; jj < I.n; ++jj) {
+      for (int j = 0; j < I.n; ++j) {
+        const int g = gt + j;
         const bool full = entry & 1;
         const uint32_t mcur = mk;  // this group's 32 key columns
-        if (jj + 1 < I.n) {
-          entry = I.list[jj + 1];
-          if (!(entry & 1)) mk = qmask_row[int64_t(jj + 1) * kB * 4];
+        if (j + 1 < I.n) {
+          entry = I.list[j + 1];
+          if (!(entry & 1)) mk = qmask_row[int64_t(j + 1) * kB * 4];
         }
-        const int gt = tb + jj;
-        const uint32_t tS = tmem + lane_base + T_S0 + (gt & 1) * 128;
-        if (!wait_u(s_full + (gt & 1), (gt >> 1) & 1)) { ok = false; break; }
+        const uint32_t tS = tmem + lane_base + rot3(g) + kCW * w;
+        if (!wait_u(s_full, g & 1)) { ok = false; break; }
         tc::tc_fence_after();
         float pf[kCW];
         {
           uint32_t sv[kCW];
-          tc::tmem_ld32(tS + kCW * w, sv);
+          tc::tmem_ld32(tS, sv);
           tc::tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < kCW; ++c) pf[c] = tc::ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, nlse2));
@@ -918,24 +947,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!((mcur >> c) & 1u)) pf[c] = 0.f;
           }
         }
-        if (!wait_u(dp_full, gt & 1)) { ok = false; break; }
+        if (!wait_u(dp_full, g & 1)) { ok = false; break; }
         tc::tc_fence_after();
         {
           uint32_t dpv[kCW];
-          tc::tmem_ld32(tmem + lane_base + T_DP + kCW * w, dpv);
+          tc::tmem_ld32(tmem + lane_base + rot3(g + 1) + kCW * w, dpv);
           tc::tmem_ld_wait();
           tc::tc_fence_before();
-          tc::mbar_arrive(dp_free);  // the dP region may be overwritten now
+          tc::mbar_arrive(dp_free);  // R[(g+1)%3] may take S of the next tile now
           uint32_t dw[kCW / 2];
 #pragma unroll
-          for (int u = 0; u < kCW / 2; ++u)
-            dw[u] = tc::pack_bf16(pf[2 * u] * (__uint_as_float(dpv[2 * u]) - drow),
-                                  pf[2 * u + 1] * (__uint_as_float(dpv[2 * u + 1]) - drow));
-          tc::tmem_st16(tS + kCW * w, dw);  // dS over the first half of this group's S columns
+          for (int e = 0; e < kCW / 2; ++e)
+            dw[e] = tc::pack_bf16(pf[2 * e] * (__uint_as_float(dpv[2 * e]) - drow),
+                                  pf[2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - drow));
+          tc::tmem_st16(tS, dw);  // dS over the first half of this group's S columns
           tc::tmem_st_wait();
         }
         tc::tc_fence_before();
-        tc::mbar_arrive(ds_ready);
+        tc::mbar_arrive(ds_ready + (g & 1));
       }
       if (!ok || !wait_u(dq_final, nq & 1)) { ok = false; break; }
       tc::tc_fence_after();
@@ -948,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tc_fence_before();
       tc::mbar_arrive(dq_free);
-      tb += I.n;
+      gt += I.n;
       ++nq;
     }
   }
