@@ -8,8 +8,9 @@
 // with dK/dV summed over the query heads of each key/value head.
 //
 // Three kernels, no atomics on the hot loop:
-//  (1) preprocess: D = rowsum(dO * O) in fp32 (and zeroed fp32 dK/dV, which
-//      chunks of long key columns add into).
+//  (1) preprocess: D = rowsum(dO * O) in fp32 (and zeroed fp32 dK/dV rows of
+//      the key tiles whose long column is split into several items that add
+//      into them).
 //  (2) KV kernel: work items are (key tile, kv head, tree, chunk of up to 64
 //      steps of that key tile's column), a step being one (query head, query
 //      tile) pair of the per-key-block CSR, run as two units of 64 queries.
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* dk_row = static_cast<uint8_t*>(p.dk) + off;
       uint8_t* dv_row = static_cast<uint8_t*>(p.dv) + off;
       if (I.n <= 0) {
-        // a key tile no query sees: zero rows (fp32 outputs were zeroed by the preprocess)
+        // a key tile no query sees: zero rows (the preprocess zeroed fp32 outputs)
         if (!F32OUT && I.s0 == 0) {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -989,46 +990,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   rearm_counter(p.sched + 4);
 }
 
-// D[b, h, i] = sum_d dO * O (fp32) for real rows, 0 for pad rows; one warp per
-// (b, i, h) row.  With fp32 gradients it also zeroes dK and dV, which the
-// chunks of long key columns add into.
+// D[b, h, i] = sum_d dO * O (fp32) for real rows, 0 for pad rows.  The
+// [B*T*Hq, D] bf16 rows of O and dO are read with 16-byte loads, four per
+// lane in flight: a warp covers 128 * 32 / D rows per pass, D / 8 lanes per
+// row, and sums each row with shuffles.  With fp32 gradients it also zeroes
+// the dK and dV rows of the key tiles whose column is split into several
+// work items of the KV kernel (they add into those rows) and of the key tiles
+// no query sees (no item visits them); every other row is written whole by
+// its single item.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
-                                                      const __nv_bfloat16* __restrict__ dout,
-                                                      const int32_t* __restrict__ n_tokens, int32_t t_pad,
-                                                      int32_t hq, int64_t n_rows, float* __restrict__ dvec,
-                                                      float4* __restrict__ zero_a, float4* __restrict__ zero_b,
-                                                      int64_t n_zero4) {
+                                                     const __nv_bfloat16* __restrict__ dout,
+                                                     const int32_t* __restrict__ n_tokens, int32_t t_pad,
+                                                     int32_t hq, int64_t n_rows, float* __restrict__ dvec,
+                                                     float4* __restrict__ dk, float4* __restrict__ dv,
+                                                     const int32_t* __restrict__ k_ptr, int32_t n_trees,
+                                                     int32_t n_blk, int32_t hkv, int32_t group,
+                                                     int32_t kv_chunk) {
+  constexpr int LPR = D / 8;        // lanes per row (16 bytes each)
+  constexpr int RPL = 32 / LPR;     // rows per warp load
+  constexpr int RPW = 4 * RPL;      // rows per warp pass
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < n_rows; row += warps) {
-    const int h = int(row % hq);
-    const int64_t bt = row / hq;
-    const int b = int(bt / t_pad), i = int(bt % t_pad);
-    float s = 0.f;
-    if (i < n_tokens[b]) {
-      constexpr int PER = D / 32;  // elements per lane: one 8- or 4-byte load of each
-      const __nv_bfloat16* a = o + row * D + lane * PER;
-      const __nv_bfloat16* c = dout + row * D + lane * PER;
-      if (PER == 4) {
-        const uint2 va = *reinterpret_cast<const uint2*>(a), vc = *reinterpret_cast<const uint2*>(c);
-        s = __uint_as_float(va.x << 16) * __uint_as_float(vc.x << 16) +
-            __uint_as_float(va.x & 0xffff0000u) * __uint_as_float(vc.x & 0xffff0000u) +
-            __uint_as_float(va.y << 16) * __uint_as_float(vc.y << 16) +
-            __uint_as_float(va.y & 0xffff0000u) * __uint_as_float(vc.y & 0xffff0000u);
-      } else {
+  const int64_t n_pass = (n_rows + RPW - 1) / RPW;
+  for (int64_t ps = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; ps < n_pass; ps += warps) {
+    uint4 va[4], vc[4];
+    int64_t row[4];
 #pragma unroll
-        for (int e = 0; e < PER; ++e) s += __bfloat162float(a[e]) * __bfloat162float(c[e]);
+    for (int k = 0; k < 4; ++k) {
+      row[k] = ps * RPW + k * RPL + lane / LPR;
+      va[k] = make_uint4(0, 0, 0, 0);
+      vc[k] = va[k];
+      if (row[k] < n_rows) {
+        va[k] = reinterpret_cast<const uint4*>(o + row[k] * D)[lane % LPR];
+        vc[k] = reinterpret_cast<const uint4*>(dout + row[k] * D)[lane % LPR];
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     }
-    if (lane == 0) dvec[(int64_t(b) * hq + h) * t_pad + i] = s;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t a[4] = {va[k].x, va[k].y, va[k].z, va[k].w};
+      const uint32_t c[4] = {vc[k].x, vc[k].y, vc[k].z, vc[k].w};
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        s += __uint_as_float(a[e] << 16) * __uint_as_float(c[e] << 16) +
+             __uint_as_float(a[e] & 0xffff0000u) * __uint_as_float(c[e] & 0xffff0000u);
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (lane % LPR == 0 && row[k] < n_rows) {
+        const int h = int(row[k] % hq);
+        const int64_t bt = row[k] / hq;
+        const int b = int(bt / t_pad), i = int(bt % t_pad);
+        dvec[(int64_t(b) * hq + h) * t_pad + i] = (i < n_tokens[b]) ? s : 0.f;
+      }
+    }
   }
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < n_zero4; k += int64_t(gridDim.x) * blockDim.x) {
-    zero_a[k] = z;
-    zero_b[k] = z;
+  if (dk == nullptr) return;
+  // zero the rows of split key columns: one (tree, key tile) unit per block pass
+  const int64_t per_tile4 = int64_t(kB) * hkv * D / 4;  // float4s of one key tile's rows
+  for (int u = blockIdx.x; u < n_trees * n_blk; u += gridDim.x) {
+    const int b = u / n_blk, kb = u % n_blk;
+    const int32_t* kp = k_ptr + b * (n_blk + 1);
+    const int n_col = kp[kb + 1] - kp[kb];
+    if (n_col > 0 && group * n_col <= kv_chunk) continue;  // written whole by its one item
+    const int64_t base = (int64_t(b) * t_pad + int64_t(kb) * kB) * hkv * D / 4;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t x = threadIdx.x; x < per_tile4; x += blockDim.x) {
+      dk[base + x] = z;
+      dv[base + x] = z;
+    }
   }
 }
 
@@ -1056,10 +1086,14 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   const int64_t rows = int64_t(tree->n_trees) * tree->t_pad;
   float* dvec = static_cast<float*>(ws);  // workspace: D [B, Hq, T] fp32
   const int64_t n_rows = rows * hq;
-  const int64_t n_zero4 = F32OUT ? rows * hkv * D / 4 : 0;
-  bwd_pre_kernel<D><<<grid_for(n_rows * 32, 256), 256, 0, st>>>(
+  const int G = hq / hkv;
+  // fp32 gradients: long key columns are split into items of kKvChunk steps
+  // that add into zeroed rows; bf16 gradients: one item per column
+  const int kv_chunk = F32OUT ? kKvChunk : G * mask->n_blk;
+  bwd_pre_kernel<D><<<num_sms() * 8, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), tree->n_tokens,
-      tree->t_pad, hq, n_rows, dvec, static_cast<float4*>(dk), static_cast<float4*>(dv), n_zero4);
+      tree->t_pad, hq, n_rows, dvec, F32OUT ? static_cast<float4*>(dk) : nullptr,
+      F32OUT ? static_cast<float4*>(dv) : nullptr, mask->k_ptr, tree->n_trees, mask->n_blk, hkv, G, kv_chunk);
   TPA_CUDA_TRY(cudaGetLastError());
 
   CUtensorMap tq, tk, tv, tdo;
@@ -1085,10 +1119,7 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.cap = mask->cap;
   prm.hq = hq;
   prm.hkv = hkv;
-  const int G = hq / hkv;
-  // Chunks of long key columns add into zeroed fp32 rows; bf16 outputs keep
-  // one item per column.
-  prm.kv_chunk = F32OUT ? kKvChunk : G * mask->n_blk;
+  prm.kv_chunk = kv_chunk;
   prm.kv_nchunk = (G * mask->n_blk + prm.kv_chunk - 1) / prm.kv_chunk;
   prm.n_trees = tree->n_trees;
   prm.kv_items = tree->n_trees * hkv * mask->n_blk * prm.kv_nchunk;
