@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Per step t: S^T(t+1) into B_t once dP^T(t) has been read, dV(t) once
-    // P^T(t) is packed, dK(t) once dS^T(t) is packed, then dP^T(t+1) into A_t
+    // Per step t: dV(t) once P^T(t) is packed, S^T(t+1) into B_t once dP^T(t)
+    // has been read, dK(t) once dS^T(t) is packed, then dP^T(t+1) into A_t
     // (in order behind dV(t) and dK(t), which read it).
     constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_kv = tc::idesc_bf16(128, D, false, true);
@@ -460,12 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t A = tmem + reg_s(gs);
         if (!(ok = wait_u(p_ready, gs & 1))) break;
         if (t == 0 && nk > 0 && !(ok = wait_u(acc_free, (nk - 1) & 1))) break;
-        // S^T(t+1) first: the next step's exponentials then overlap dV(t),
-        // dK(t) and dP^T(t+1).
-        if (t + 1 < n) {
-          if (!(ok = wait_u(dp_free, gs & 1))) break;
-          if (!(ok = issue_s(gs + 1))) break;
-        }
         tc::tc_fence_after();
         if (tc::elect_one()) {
 #pragma unroll
@@ -474,6 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (t > 0 || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
+        // dV(t) keeps the tensor pipe busy while dP^T(t) is read out of B_t
+        if (t + 1 < n) {
+          if (!(ok = wait_u(dp_free, gs & 1))) break;
+          if (!(ok = issue_s(gs + 1))) break;
+        }
         if (!(ok = wait_u(ds_ready, gs & 1))) break;
         tc::tc_fence_after();
         if (tc::elect_one()) {
