@@ -53,6 +53,40 @@ def _peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+# Per-launch DRAM traffic comes from the ncu summaries under profiles/: each
+# names the source file it was captured from and that file's sha256 prefix,
+# the tree tokens of the captured case, and "DRAM traffic (read + write) of
+# this launch: X GB".  A summary counts only while the source is unchanged;
+# attention traffic scales with the tree tokens processed (every Q, K, V, O,
+# dO and gradient row is read or written a fixed number of times).
+PROFILES = {
+    "tpa_tree_attn_fwd": ["attn_fwd_grpo_3trees_ncu_full.md"],
+    "tpa_tree_attn_bwd": ["bwd_pre_grpo_3trees_ncu_full.md", "attn_bwd_kv_grpo_3trees_ncu_full.md",
+                          "attn_bwd_dq_grpo_3trees_ncu_full.md"],
+}
+
+
+def _profile_traffic(entry: str, tree_tokens: int):
+    import hashlib
+    import re
+    total = 0.0
+    for name in PROFILES.get(entry, []):
+        path = os.path.join(ROOT, "profiles", name)
+        if not os.path.exists(path):
+            return None
+        text = open(path).read()
+        src = re.search(r"Source: `([^`]+)` sha256 prefix ([0-9a-f]+)", text)
+        gb = re.search(r"DRAM traffic \(read \+ write\) of this launch: ([0-9.]+) GB", text)
+        toks = re.search(r"\(([0-9]+) tree tokens", text)
+        if not (src and gb and toks):
+            return None
+        with open(os.path.join(ROOT, src.group(1)), "rb") as f:
+            if not hashlib.sha256(f.read()).hexdigest().startswith(src.group(2)):
+                return None  # the kernel changed since the counters were taken
+        total += float(gb.group(1)) * 1e9 * tree_tokens / int(toks.group(1))
+    return total if total > 0 else None
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -356,6 +390,9 @@ def run_gpu(args, rank, world, local):
     else:
         roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": peak_sus, "unit": "TFLOP/s",
                 "frac": fwd_tflops / peak_sus, "traffic": None}
+    if dominant != "tpa_tree_logprobs_entropy":
+        roof["traffic"] = _profile_traffic(dominant, rows)
+        roof["traffic_unit"] = "bytes per launch (ncu DRAM read + write, scaled by tree tokens)"
     roof.update({"kernel": dominant, "peak_kind": f"{peak_kind} bf16 sustained" if roof["unit"] == "TFLOP/s"
                  else f"{peak_kind} HBM copy", "algorithmic_per_launch":
                  (10.0 * pairs * d * Hq if dominant == "tpa_tree_attn_bwd" else

@@ -196,17 +196,18 @@ struct KvItem {
 __device__ __forceinline__ KvItem decode_kv(const BwdParams& p, int it) {
   KvItem r;
   const int G = p.hq / p.hkv;
-  // Chunk index slowest: first chunk 0 of every column, then chunk 1 of the
-  // columns that have one, and so on, so the empty (column, chunk) pairs
-  // gather at the end; within a chunk level ascending key blocks, the
-  // longest columns first.
-  const int per_ch = p.n_trees * p.hkv * p.n_blk;
-  const int ch = it / per_ch;
-  int rem = it - ch * per_ch;
-  r.b = rem / (p.hkv * p.n_blk);
-  rem -= r.b * (p.hkv * p.n_blk);
-  r.g = rem / p.n_blk;
-  r.kb = rem - r.g * p.n_blk;
+  // (tree, kv head) slowest so the Q/dO tiles of one head group stay in L2
+  // while its columns run; ascending key blocks (the longest columns first);
+  // the chunk fastest.  Chunks past a column's end are empty and skipped by
+  // the producer.
+  const int per_g = p.n_blk * p.kv_nchunk;
+  const int per_b = p.hkv * per_g;
+  r.b = it / per_b;
+  int rem = it - r.b * per_b;
+  r.g = rem / per_g;
+  rem -= r.g * per_g;
+  r.kb = rem / p.kv_nchunk;
+  const int ch = rem - r.kb * p.kv_nchunk;
   const int32_t* kp = p.k_ptr + r.b * (p.n_blk + 1);
   r.n_col = kp[r.kb + 1] - kp[r.kb];
   r.list = p.k_idx + int64_t(r.b) * p.cap + kp[r.kb];
