@@ -398,6 +398,22 @@ def run_gpu(args, rank, world, local):
                  (10.0 * pairs * d * Hq if dominant == "tpa_tree_attn_bwd" else
                   flops_fwd if dominant == "tpa_tree_attn_fwd" else lp_bytes)})
 
+    # Micro-batch / rank balancing (host): the blog post's experiment shape —
+    # the workload's sequences split over 4 ranks with unbounded capacity —
+    # FFD against KK spread, and the cost of one call.
+    bal = None
+    if rank == 0:
+        lens = [len(s_) for s_ in seqs]
+        bal = {"items": len(lens), "groups": 4}
+        for algo in ("ffd", "kk"):
+            t0 = time.perf_counter()
+            for _ in range(20):
+                g_, ng_, used_ = tpa.balance(lens, 10**12, 4, 1, algo)
+            bal[f"{algo}_us_per_call"] = (time.perf_counter() - t0) / 20 * 1e6
+            bal[f"{algo}_spread"] = tpa.packing_metrics(lens, g_, ng_, 10**12)["spread"]
+        bal["kk_improvement_pct"] = (100.0 * (bal["ffd_spread"] - bal["kk_spread"]) / bal["ffd_spread"]
+                                     if bal["ffd_spread"] else 0.0)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
         r = cpu_oracle_run(1, 0, args.oracle_pairs)
@@ -418,7 +434,7 @@ def run_gpu(args, rank, world, local):
         "attn_fwd_bwd_tflops": attn_tflops, "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
         "logprobs_gbs": lp_gbs, "logprobs_frac_hbm": lp_gbs / peaks["hbm_gbs"],
         "roofline": roof, "clocks": clocks, "gpu_launches": n_launch_per_step * args.steps,
-        "e2e": e2e, "cpu_baseline": cpu,
+        "e2e": e2e, "cpu_baseline": cpu, "balance": bal,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -142,6 +142,65 @@ int tpa_tree_upload(const tpa_tree* tree, void* dev_blob, uint64_t dev_bytes, vo
 void tpa_tree_free(tpa_tree* tree);
 
 /* ------------------------------------------------------------------------ */
+/* Micro-batch / rank balancing: blog post "AReaL 序列打包算法 FFD 与 KK"
+ * (FFD and KK sections, packing metrics).  Items with positive integer
+ * weights — packed trees (weight = tree tokens or ancestor pairs) or
+ * sequences (weight = length) — are split into groups: micro-batches of at
+ * most `capacity`, or data-parallel ranks (a capacity larger than the total
+ * makes the split purely about balance).  Host only; thread-safe.           */
+/* ------------------------------------------------------------------------ */
+
+enum { TPA_BALANCE_FFD = 0, TPA_BALANCE_KK = 1 };
+
+/*
+ * tpa_balance
+ *   weights [n] int64 > 0, each <= capacity (host)
+ *   capacity > 0: largest group weight
+ *   min_groups >= 1, groups_divisor >= 1: the group count is >= min_groups
+ *     and a multiple of groups_divisor
+ *   algorithm TPA_BALANCE_FFD: items heaviest first (equal weights in input
+ *     order); while fewer than min_groups groups exist an item opens a group,
+ *     otherwise it joins the lightest group with room (equal loads: the
+ *     earliest group), or opens a group when none has room; a group count
+ *     that misses the rules raises min_groups to the next multiple of the
+ *     divisor and the allocation is redone.  Groups are numbered in
+ *     creation order.
+ *   algorithm TPA_BALANCE_KK: k = max(min_groups, ceil(total / capacity))
+ *     rounded up to the divisor; each item starts as a k-set partial
+ *     partition; the two partitions of largest spread (max - min set sum;
+ *     equal spreads: the older first) are merged by joining the i-th largest
+ *     set of the first with the i-th smallest set of the second, until one
+ *     remains.  Groups are numbered by final sum, heaviest first.  If a group
+ *     exceeds the capacity the FFD result is returned instead.
+ *   group_of [n] int32 (written): group of each item
+ *   n_groups (written): number of groups
+ *   algorithm_used (written if not NULL): the algorithm whose result this is
+ * Errors: TPA_ERR_INVALID_ARG (null pointer, n < 1, non-positive argument or
+ * weight, unknown algorithm, more groups required than items),
+ * TPA_ERR_SEQ_TOO_LONG (a weight above the capacity), TPA_ERR_NO_MEMORY.
+ */
+int tpa_balance(const int64_t* weights, int32_t n, int64_t capacity, int32_t min_groups,
+                int32_t groups_divisor, int32_t algorithm, int32_t* group_of, int32_t* n_groups,
+                int32_t* algorithm_used);
+
+/* Packing metrics of a grouping (the post's quality measures): group loads
+ * L_g = sum of the weights in g; spread = max - min; mean = total / groups;
+ * std_dev = population standard deviation of the loads; cv = std_dev / mean;
+ * imbalance_ratio = max / mean; utilization = total / (groups * capacity);
+ * wasted = groups * capacity - total (padding if every group is filled to
+ * the capacity).  A group with no item has load 0. */
+typedef struct {
+  int32_t n_groups, pad_;
+  int64_t total, max_load, min_load, spread, wasted;
+  double mean, std_dev, cv, imbalance_ratio, utilization;
+} tpa_packing_metrics_t;
+
+/* Errors: TPA_ERR_INVALID_ARG (null pointer, n < 1, n_groups < 1, capacity
+ * < 1, a group index outside [0, n_groups)), TPA_ERR_NO_MEMORY. */
+int tpa_packing_metrics(const int64_t* weights, int32_t n, const int32_t* group_of, int32_t n_groups,
+                        int64_t capacity, tpa_packing_metrics_t* out);
+
+/* ------------------------------------------------------------------------ */
 /* Block classification: tree training page, §树构建过程 step 4 (mask
  * generation) and §注意力机制 (block mask, BLOCK_SIZE 128, empty blocks are
  * skipped).  A 128x128 tile (query block qb, key block kb) is EMPTY when no

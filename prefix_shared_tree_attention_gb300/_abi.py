@@ -15,6 +15,7 @@ STATUS = {
 BLOCK_SIZE = 128
 LOGITS_COMPACT, LOGITS_PADDED = 0, 1
 GRAD_F32, GRAD_BF16 = 0, 1
+BALANCE_FFD, BALANCE_KK = 0, 1
 
 _i32p = C.POINTER(C.c_int32)
 _i64p = C.POINTER(C.c_int64)
@@ -47,6 +48,15 @@ class BlockMaskView(C.Structure):
     ]
 
 
+class PackingMetrics(C.Structure):
+    _fields_ = [
+        ("n_groups", C.c_int32), ("pad_", C.c_int32), ("total", C.c_int64), ("max_load", C.c_int64),
+        ("min_load", C.c_int64), ("spread", C.c_int64), ("wasted", C.c_int64), ("mean", C.c_double),
+        ("std_dev", C.c_double), ("cv", C.c_double), ("imbalance_ratio", C.c_double),
+        ("utilization", C.c_double),
+    ]
+
+
 # name -> (restype, argtypes); every symbol declared in include/tpa.h
 PROTOTYPES = {
     "tpa_tree_pack": (C.c_int, [_i32p, _i64p, C.c_int32, C.c_int32, C.POINTER(C.c_void_p)]),
@@ -55,6 +65,10 @@ PROTOTYPES = {
     "tpa_tree_make_view": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(TreeView)]),
     "tpa_tree_upload": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint64, C.c_void_p]),
     "tpa_tree_free": (None, [C.c_void_p]),
+    "tpa_balance": (C.c_int, [_i64p, C.c_int32, C.c_int64, C.c_int32, C.c_int32, C.c_int32, _i32p, _i32p,
+                              _i32p]),
+    "tpa_packing_metrics": (C.c_int, [_i64p, C.c_int32, _i32p, C.c_int32, C.c_int64,
+                                      C.POINTER(PackingMetrics)]),
     "tpa_blockmask_bytes": (C.c_uint64, [C.c_int32, C.c_int32]),
     "tpa_blockmask_make_view": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(BlockMaskView)]),
     "tpa_block_classify": (C.c_int, [C.POINTER(TreeView), C.POINTER(BlockMaskView), C.c_void_p]),

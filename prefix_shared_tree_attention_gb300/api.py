@@ -9,8 +9,8 @@ from typing import Sequence
 import numpy as np
 import torch
 
-from ._abi import (GRAD_BF16, GRAD_F32, LOGITS_COMPACT, LOGITS_PADDED, BlockMaskView, TreeInfo, TreeView,
-                   check, lib)
+from ._abi import (BALANCE_FFD, BALANCE_KK, GRAD_BF16, GRAD_F32, LOGITS_COMPACT, LOGITS_PADDED, BlockMaskView,
+                   PackingMetrics, TreeInfo, TreeView, check, lib)
 
 
 def _stream_ptr(stream) -> int:
@@ -164,6 +164,34 @@ def tree_pack(seqs: Sequence[Sequence[int]] | None = None, max_tokens_per_mb: in
     check("tpa_tree_pack", lib().tpa_tree_pack(tok_p, offsets.ctypes.data_as(C.POINTER(C.c_int64)), n,
                                                int(max_tokens_per_mb), C.byref(h)))
     return Tree(h)
+
+
+def balance(weights: Sequence[int], capacity: int, min_groups: int = 1, groups_divisor: int = 1,
+            algorithm: str = "ffd") -> tuple[np.ndarray, int, str]:
+    """Split weighted items into groups (tpa_balance): returns (group of each
+    item, number of groups, algorithm whose result it is)."""
+    w = np.ascontiguousarray(np.asarray(weights, dtype=np.int64))
+    if algorithm not in ("ffd", "kk"):
+        raise ValueError(f"unknown balancing algorithm {algorithm!r}; choose 'ffd' or 'kk'")
+    algo = BALANCE_FFD if algorithm == "ffd" else BALANCE_KK
+    out = np.empty(len(w), dtype=np.int32)
+    ng, used = C.c_int32(0), C.c_int32(0)
+    check("tpa_balance", lib().tpa_balance(w.ctypes.data_as(C.POINTER(C.c_int64)), len(w), int(capacity),
+                                           int(min_groups), int(groups_divisor), algo,
+                                           out.ctypes.data_as(C.POINTER(C.c_int32)), C.byref(ng),
+                                           C.byref(used)))
+    return out, ng.value, "kk" if used.value == BALANCE_KK else "ffd"
+
+
+def packing_metrics(weights: Sequence[int], group_of: Sequence[int], n_groups: int, capacity: int) -> dict:
+    """The packing metrics of a grouping (tpa_packing_metrics) as a dict."""
+    w = np.ascontiguousarray(np.asarray(weights, dtype=np.int64))
+    g = np.ascontiguousarray(np.asarray(group_of, dtype=np.int32))
+    m = PackingMetrics()
+    check("tpa_packing_metrics", lib().tpa_packing_metrics(w.ctypes.data_as(C.POINTER(C.c_int64)), len(w),
+                                                           g.ctypes.data_as(C.POINTER(C.c_int32)), int(n_groups),
+                                                           int(capacity), C.byref(m)))
+    return {f: getattr(m, f) for f, _ in PackingMetrics._fields_ if f != "pad_"}
 
 
 def block_classify(dtree: DeviceTree, stream=None, out: BlockMask | None = None) -> BlockMask:
