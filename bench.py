@@ -321,6 +321,29 @@ def run_gpu(args, rank, world, local):
     ms_step = total_ms / args.steps
     clocks = clk.summary()
 
+    # ------------------------------------------------ dense ancestor-mask export (Megatron-style mask)
+    # Not part of the step: the export a dense-mask consumer would run once
+    # per micro-batch, timed alone on the same trees; bound by HBM writes.
+    dmask = None
+    if args.only in ("all", "attn"):
+        dmask = {}
+        for fmt in ("u8", "bits"):
+            buf = tpa.dense_mask(dtree, fmt)
+            for _ in range(3):
+                tpa.dense_mask(dtree, fmt, out=buf)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 10
+            e0.record(stream)
+            for _ in range(reps):
+                tpa.dense_mask(dtree, fmt, out=buf)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / reps
+            nbytes = buf.numel() * buf.element_size()
+            dmask[fmt] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9}
+            del buf
+        tpa.sync_status()
+
     # ------------------------------------------------ end to end from host buffers
     e2e = None
     if not args.no_e2e and args.only == "all":
@@ -435,6 +458,10 @@ def run_gpu(args, rank, world, local):
         "logprobs_gbs": lp_gbs, "logprobs_frac_hbm": lp_gbs / peaks["hbm_gbs"],
         "roofline": roof, "clocks": clocks, "gpu_launches": n_launch_per_step * args.steps,
         "e2e": e2e, "cpu_baseline": cpu, "balance": bal,
+        "dense_mask": None if dmask is None else {
+            **dmask, "frac_hbm_u8": dmask["u8"]["gbs"] / peaks["hbm_gbs"],
+            "note": "write-only export of the [B, T, T] ancestor mask (u8) and its bit-packed form; "
+                    "fraction against the measured copy bandwidth"},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

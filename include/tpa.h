@@ -241,6 +241,35 @@ int tpa_blockmask_make_view(void* base, int32_t n_trees, int32_t t_pad, tpa_bloc
 int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask_view* mask, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Dense ancestor mask: tree training page, §Megatron 引擎 (for gradient
+ * checkpointing the Megatron engine passes a dense attention-mask tensor
+ * instead of a BlockMask, since save_for_backward() serialises only
+ * tensors).  M[b][i][j] = 1 iff key j is visible to query i, j <= i <= E[j];
+ * pad rows and pad columns are 0.                                           */
+/* ------------------------------------------------------------------------ */
+
+enum { TPA_MASK_U8 = 0, TPA_MASK_BITS = 1 };
+
+/* Bytes of a dense mask: B * T_pad^2 (TPA_MASK_U8) or B * T_pad^2 / 8
+ * (TPA_MASK_BITS); 0 on invalid arguments. */
+uint64_t tpa_dense_mask_bytes(int32_t n_trees, int32_t t_pad, int32_t format);
+
+/*
+ * tpa_dense_mask — write the dense mask of every tree.
+ *   tree     view of the DEVICE blob
+ *   out      device buffer of tpa_dense_mask_bytes() bytes, 16-byte aligned:
+ *            TPA_MASK_U8   [B, T_pad, T_pad] uint8, out[b][i][j] = M[b][i][j]
+ *            TPA_MASK_BITS [B, T_pad, T_pad / 32] uint32, bit (j % 32) of word
+ *                          j / 32 of row i = M[b][i][j]
+ *   invert   0: 1 marks a visible pair; 1: the complement (1 marks a removed
+ *            pair, the convention of boolean masks whose True blocks attention)
+ * One kernel on `stream`, bound by HBM writes.  Errors: TPA_ERR_INVALID_ARG,
+ * TPA_ERR_BUFFER_TOO_SMALL, TPA_ERR_CUDA.
+ */
+int tpa_dense_mask(const tpa_tree_view* tree, void* out, uint64_t out_bytes, int32_t format, int32_t invert,
+                   void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Tree attention (tree training page, §树构建过程 mask caption and
  * §注意力机制): for query position i of tree b and query head h,
  *   O_i = sum_{j: j <= i <= E[j]} softmax_j(scale * q_i . k_j) v_j

@@ -8,6 +8,7 @@ the C names without the ``tpa_`` prefix:
     tree = tree_pack(seqs, max_tokens_per_mb)           # host trie packer
     dtree = tree.upload(device)                         # metadata -> HBM
     mask = block_classify(dtree)                        # 128x128 tile classes + CSR
+    dense = dense_mask(dtree)                           # [B, T, T] ancestor mask (Megatron-style)
     o, lse = tree_attn_fwd(dtree, mask, q, k, v)
     dq, dk, dv = tree_attn_bwd(dtree, mask, q, k, v, o, lse, dout)
     pos_logp, pos_ent, seq_logp, seq_ent = tree_logprobs_entropy(dtree, logits)
@@ -16,6 +17,7 @@ the C names without the ``tpa_`` prefix:
 """
 from ._abi import BLOCK_SIZE, LOGITS_COMPACT, LOGITS_PADDED, STATUS, TpaError, lib  # noqa: F401
 from .api import (  # noqa: F401
-    BlockMask, DeviceTree, Tree, balance, block_classify, device_check, packing_metrics, sync_status, tree_attn_bwd,
+    BlockMask, DeviceTree, Tree, balance, block_classify, dense_mask, device_check, packing_metrics, sync_status,
+    tree_attn_bwd,
     tree_attn_bwd_workspace_bytes, tree_attn_fwd, tree_logprobs_entropy, tree_pack,
 )

@@ -16,6 +16,7 @@ BLOCK_SIZE = 128
 LOGITS_COMPACT, LOGITS_PADDED = 0, 1
 GRAD_F32, GRAD_BF16 = 0, 1
 BALANCE_FFD, BALANCE_KK = 0, 1
+MASK_U8, MASK_BITS = 0, 1
 
 _i32p = C.POINTER(C.c_int32)
 _i64p = C.POINTER(C.c_int64)
@@ -69,6 +70,8 @@ PROTOTYPES = {
                               _i32p]),
     "tpa_packing_metrics": (C.c_int, [_i64p, C.c_int32, _i32p, C.c_int32, C.c_int64,
                                       C.POINTER(PackingMetrics)]),
+    "tpa_dense_mask_bytes": (C.c_uint64, [C.c_int32, C.c_int32, C.c_int32]),
+    "tpa_dense_mask": (C.c_int, [C.POINTER(TreeView), C.c_void_p, C.c_uint64, C.c_int32, C.c_int32, C.c_void_p]),
     "tpa_blockmask_bytes": (C.c_uint64, [C.c_int32, C.c_int32]),
     "tpa_blockmask_make_view": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.POINTER(BlockMaskView)]),
     "tpa_block_classify": (C.c_int, [C.POINTER(TreeView), C.POINTER(BlockMaskView), C.c_void_p]),

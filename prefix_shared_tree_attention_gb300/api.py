@@ -9,8 +9,8 @@ from typing import Sequence
 import numpy as np
 import torch
 
-from ._abi import (BALANCE_FFD, BALANCE_KK, GRAD_BF16, GRAD_F32, LOGITS_COMPACT, LOGITS_PADDED, BlockMaskView,
-                   PackingMetrics, TreeInfo, TreeView, check, lib)
+from ._abi import (BALANCE_FFD, BALANCE_KK, GRAD_BF16, GRAD_F32, LOGITS_COMPACT, LOGITS_PADDED, MASK_BITS,
+                   MASK_U8, BlockMaskView, PackingMetrics, TreeInfo, TreeView, check, lib)
 
 
 def _stream_ptr(stream) -> int:
@@ -192,6 +192,24 @@ def packing_metrics(weights: Sequence[int], group_of: Sequence[int], n_groups: i
                                                            g.ctypes.data_as(C.POINTER(C.c_int32)), int(n_groups),
                                                            int(capacity), C.byref(m)))
     return {f: getattr(m, f) for f, _ in PackingMetrics._fields_ if f != "pad_"}
+
+
+def dense_mask(dtree: DeviceTree, fmt: str = "u8", invert: bool = False, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """Dense ancestor mask of every tree (tpa_dense_mask): uint8 [B, T, T]
+    for fmt "u8", or int32 words [B, T, T/32] (bit j%32 of word j/32) for
+    fmt "bits"; 1 marks a visible pair, or a removed pair with invert."""
+    if fmt not in ("u8", "bits"):
+        raise ValueError(f"unknown mask format {fmt!r}; choose 'u8' or 'bits'")
+    B, T = dtree.info.n_trees, dtree.info.t_pad
+    code = MASK_U8 if fmt == "u8" else MASK_BITS
+    if out is None:
+        out = (torch.empty((B, T, T), dtype=torch.uint8, device=dtree.device) if fmt == "u8" else
+               torch.empty((B, T, T // 32), dtype=torch.int32, device=dtree.device))
+    nbytes = out.numel() * out.element_size()
+    check("tpa_dense_mask", lib().tpa_dense_mask(C.byref(dtree.view), out.data_ptr(), nbytes, code,
+                                                 1 if invert else 0, _stream_ptr(stream)))
+    return out
 
 
 def block_classify(dtree: DeviceTree, stream=None, out: BlockMask | None = None) -> BlockMask:

@@ -1,0 +1,127 @@
+// Dense ancestor-mask export (tree training page, §Megatron 引擎: for
+// compatibility with gradient checkpointing the Megatron engine passes a
+// dense attention-mask tensor instead of a BlockMask object, because
+// save_for_backward() serialises only tensors).
+//
+// M[b][i][j] = 1 iff key j is visible to query i of tree b, i.e. j is i or
+// an ancestor of i: j <= i <= E[j] with E the subtree end of j's node
+// (§树构建过程 mask caption); pad rows and pad columns are 0.  With the
+// visible length len_j = E[j] - j + 1 (0 at pad keys, whose E is -1) the test
+// is one unsigned compare: (unsigned)(i - j) < (unsigned)len_j.
+//
+// Layouts: TPA_MASK_U8 [B, T, T] bytes; TPA_MASK_BITS [B, T, T/32] uint32
+// words, bit (j & 31) of word j >> 5.  `invert` writes the complement (1 =
+// pair removed), the convention of boolean attention masks whose True entries
+// block attention.
+//
+// The export is bound by HBM writes.  A CTA takes kRows query rows and a
+// chunk of keys; each thread keeps len_j of its keys in registers (E is read
+// once per CTA) and writes 16 bytes (U8: 16 keys) or 4 bytes (BITS: 32 keys)
+// per row, the writes of a warp to one row being contiguous.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kThreadsDm = 256;
+constexpr int kRows = 64;  // query rows per CTA
+
+__global__ void __launch_bounds__(kThreadsDm) dense_mask_u8_kernel(const int32_t* __restrict__ subtree_end,
+                                                                  int32_t t_pad, uint8_t* __restrict__ out,
+                                                                  uint32_t invert) {
+  const int b = blockIdx.z;
+  const int j0 = (blockIdx.x * kThreadsDm + threadIdx.x) * 16;
+  if (j0 >= t_pad) return;
+  const int32_t* e = subtree_end + int64_t(b) * t_pad + j0;
+  uint32_t len[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int4 v = reinterpret_cast<const int4*>(e)[q];
+    const int ev[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = j0 + 4 * q + c;
+      len[4 * q + c] = ev[c] >= j ? uint32_t(ev[c] - j + 1) : 0u;
+    }
+  }
+  const uint32_t inv = invert ? 0x01010101u : 0u;
+  uint8_t* dst = out + (int64_t(b) * t_pad + int64_t(blockIdx.y) * kRows) * t_pad + j0;
+  for (int r = 0; r < kRows; ++r) {
+    const int i = blockIdx.y * kRows + r;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) x |= uint32_t(uint32_t(i - (j0 + 4 * q + c)) < len[4 * q + c]) << (8 * c);
+      w[q] = x ^ inv;
+    }
+    *reinterpret_cast<uint4*>(dst + int64_t(r) * t_pad) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsDm) dense_mask_bits_kernel(const int32_t* __restrict__ subtree_end,
+                                                                    int32_t t_pad, uint32_t* __restrict__ out,
+                                                                    uint32_t invert) {
+  const int b = blockIdx.z;
+  const int word = blockIdx.x * kThreadsDm + threadIdx.x;
+  const int j0 = word * 32;
+  if (j0 >= t_pad) return;
+  const int32_t* e = subtree_end + int64_t(b) * t_pad + j0;
+  uint32_t len[32];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int4 v = reinterpret_cast<const int4*>(e)[q];
+    const int ev[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = j0 + 4 * q + c;
+      len[4 * q + c] = ev[c] >= j ? uint32_t(ev[c] - j + 1) : 0u;
+    }
+  }
+  const uint32_t inv = invert ? 0xffffffffu : 0u;
+  const int words = t_pad / 32;
+  uint32_t* dst = out + (int64_t(b) * t_pad + int64_t(blockIdx.y) * kRows) * words + word;
+  for (int r = 0; r < kRows; ++r) {
+    const int i = blockIdx.y * kRows + r;
+    uint32_t x = 0;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) x |= uint32_t(uint32_t(i - (j0 + c)) < len[c]) << c;
+    dst[int64_t(r) * words] = x ^ inv;
+  }
+}
+
+}  // namespace
+
+extern "C" uint64_t tpa_dense_mask_bytes(int32_t n_trees, int32_t t_pad, int32_t format) {
+  if (n_trees < 1 || t_pad < 1 || t_pad % TPA_BLOCK_SIZE != 0) return 0;
+  const uint64_t cells = uint64_t(n_trees) * uint64_t(t_pad) * uint64_t(t_pad);
+  if (format == TPA_MASK_U8) return cells;
+  if (format == TPA_MASK_BITS) return cells / 8;
+  return 0;
+}
+
+extern "C" int tpa_dense_mask(const tpa_tree_view* tree, void* out, uint64_t out_bytes, int32_t format,
+                              int32_t invert, void* stream) {
+  if (!tree || !out || !tree->subtree_end || tree->n_trees < 1 || tree->n_trees > 65535 || tree->t_pad < 1 ||
+      tree->t_pad % TPA_BLOCK_SIZE != 0)
+    return TPA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 15) return TPA_ERR_INVALID_ARG;
+  const uint64_t need = tpa_dense_mask_bytes(tree->n_trees, tree->t_pad, format);
+  if (need == 0) return TPA_ERR_INVALID_ARG;
+  if (out_bytes < need) return TPA_ERR_BUFFER_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int t = tree->t_pad;
+  const uint32_t inv = invert ? 1u : 0u;
+  if (format == TPA_MASK_U8) {
+    const dim3 grid((t / 16 + kThreadsDm - 1) / kThreadsDm, t / kRows, tree->n_trees);
+    dense_mask_u8_kernel<<<grid, kThreadsDm, 0, st>>>(tree->subtree_end, t, static_cast<uint8_t*>(out), inv);
+  } else {
+    const dim3 grid((t / 32 + kThreadsDm - 1) / kThreadsDm, t / kRows, tree->n_trees);
+    dense_mask_bits_kernel<<<grid, kThreadsDm, 0, st>>>(tree->subtree_end, t, static_cast<uint32_t*>(out), inv);
+  }
+  TPA_CUDA_TRY(cudaGetLastError());
+  return TPA_OK;
+}
