@@ -436,6 +436,25 @@ def run_gpu(args, rank, world, local):
             bal[f"{algo}_spread"] = tpa.packing_metrics(lens, g_, ng_, 10**12)["spread"]
         bal["kk_improvement_pct"] = (100.0 * (bal["ffd_spread"] - bal["kk_spread"]) / bal["ffd_spread"]
                                      if bal["ffd_spread"] else 0.0)
+        # host steps 1-3 of tree building on the workload as a right-padded batch
+        L = max(lens)
+        ids = np.zeros((len(seqs), L), dtype=np.int32)
+        am = np.zeros((len(seqs), L), dtype=np.uint8)
+        for r_, s_ in enumerate(seqs):
+            ids[r_, :len(s_)] = s_
+            am[r_, :len(s_)] = 1
+        t0 = time.perf_counter()
+        for _ in range(5):
+            tpa.extract_sequences(ids, am)
+        t1 = time.perf_counter()
+        for _ in range(5):
+            tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
+        t2 = time.perf_counter()
+        for _ in range(5):
+            tpa.tree_pack_padded(ids, am, T)
+        t3 = time.perf_counter()
+        bal["host_ms"] = {"extract": (t1 - t0) / 5 * 1e3, "pack": (t2 - t1) / 5 * 1e3,
+                          "pack_padded": (t3 - t2) / 5 * 1e3, "padded_batch": list(ids.shape)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":

@@ -120,6 +120,29 @@ typedef struct {
 int tpa_tree_pack(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
                   int32_t max_tokens_per_mb, tpa_tree** out);
 
+/*
+ * tpa_extract_sequences — step 1 of §树构建过程 (提取序列): the real tokens of
+ * each row of a padded batch are the input_ids entries whose attention_mask
+ * entry is non-zero, in column order (left or right padding and interior
+ * gaps alike).
+ *   input_ids      [n_rows, row_len] int32 (host)
+ *   attention_mask [n_rows, row_len] uint8, 0 = padding (host)
+ *   tokens_out     host buffer of n_rows * row_len int32 (the first
+ *                  offsets_out[n_rows] entries are written)
+ *   offsets_out    [n_rows+1] int64 (written): row r is tokens
+ *                  [offsets_out[r], offsets_out[r+1]) — the input format of
+ *                  tpa_tree_pack.  A row without tokens gives an empty range.
+ * Errors: TPA_ERR_INVALID_ARG.  Host only; thread-safe.
+ */
+int tpa_extract_sequences(const int32_t* input_ids, const uint8_t* attention_mask, int32_t n_rows,
+                          int32_t row_len, int32_t* tokens_out, int64_t* offsets_out);
+
+/* tpa_tree_pack on the sequences tpa_extract_sequences reads from a padded
+ * batch (steps 1-3 of §树构建过程 in one call).  Arguments and errors as the
+ * two calls; a row without tokens is TPA_ERR_EMPTY_SEQUENCE. */
+int tpa_tree_pack_padded(const int32_t* input_ids, const uint8_t* attention_mask, int32_t n_rows,
+                         int32_t row_len, int32_t max_tokens_per_mb, tpa_tree** out);
+
 /* Sizes and counts of a packed tree set.  Errors: TPA_ERR_INVALID_ARG. */
 int tpa_tree_get_info(const tpa_tree* tree, tpa_tree_info* info);
 

@@ -6,6 +6,7 @@ packer on the host, CUDA kernels for sm_103a on the device). Functions keep
 the C names without the ``tpa_`` prefix:
 
     tree = tree_pack(seqs, max_tokens_per_mb)           # host trie packer
+    tree = tree_pack_padded(input_ids, attention_mask, max_tokens_per_mb)  # from a padded batch
     dtree = tree.upload(device)                         # metadata -> HBM
     mask = block_classify(dtree)                        # 128x128 tile classes + CSR
     dense = dense_mask(dtree)                           # [B, T, T] ancestor mask (Megatron-style)
@@ -17,7 +18,7 @@ the C names without the ``tpa_`` prefix:
 """
 from ._abi import BLOCK_SIZE, LOGITS_COMPACT, LOGITS_PADDED, STATUS, TpaError, lib  # noqa: F401
 from .api import (  # noqa: F401
-    BlockMask, DeviceTree, Tree, balance, block_classify, dense_mask, device_check, packing_metrics, sync_status,
-    tree_attn_bwd,
+    BlockMask, DeviceTree, Tree, balance, block_classify, dense_mask, device_check, extract_sequences,
+    packing_metrics, sync_status, tree_attn_bwd, tree_pack_padded,
     tree_attn_bwd_workspace_bytes, tree_attn_fwd, tree_logprobs_entropy, tree_pack,
 )

@@ -61,6 +61,9 @@ class PackingMetrics(C.Structure):
 # name -> (restype, argtypes); every symbol declared in include/tpa.h
 PROTOTYPES = {
     "tpa_tree_pack": (C.c_int, [_i32p, _i64p, C.c_int32, C.c_int32, C.POINTER(C.c_void_p)]),
+    "tpa_extract_sequences": (C.c_int, [_i32p, C.POINTER(C.c_uint8), C.c_int32, C.c_int32, _i32p, _i64p]),
+    "tpa_tree_pack_padded": (C.c_int, [_i32p, C.POINTER(C.c_uint8), C.c_int32, C.c_int32, C.c_int32,
+                                       C.POINTER(C.c_void_p)]),
     "tpa_tree_get_info": (C.c_int, [C.c_void_p, C.POINTER(TreeInfo)]),
     "tpa_tree_host_blob": (C.c_void_p, [C.c_void_p]),
     "tpa_tree_make_view": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(TreeView)]),

@@ -166,6 +166,37 @@ def tree_pack(seqs: Sequence[Sequence[int]] | None = None, max_tokens_per_mb: in
     return Tree(h)
 
 
+def _padded(input_ids, attention_mask):
+    ids = np.ascontiguousarray(np.asarray(input_ids), dtype=np.int32)
+    msk = np.ascontiguousarray(np.asarray(attention_mask) != 0, dtype=np.uint8)
+    if ids.ndim != 2 or ids.shape != msk.shape:
+        raise ValueError("input_ids and attention_mask must be 2-D arrays of one shape")
+    return ids, msk
+
+
+def extract_sequences(input_ids, attention_mask) -> tuple[np.ndarray, np.ndarray]:
+    """Real tokens of a padded batch (tpa_extract_sequences): flat int32
+    tokens and int64 offsets, the input format of ``tree_pack``."""
+    ids, msk = _padded(input_ids, attention_mask)
+    n, L = ids.shape
+    tokens = np.empty(n * L, dtype=np.int32)
+    offsets = np.empty(n + 1, dtype=np.int64)
+    check("tpa_extract_sequences", lib().tpa_extract_sequences(
+        ids.ctypes.data_as(C.POINTER(C.c_int32)), msk.ctypes.data_as(C.POINTER(C.c_uint8)), n, L,
+        tokens.ctypes.data_as(C.POINTER(C.c_int32)), offsets.ctypes.data_as(C.POINTER(C.c_int64))))
+    return tokens[:int(offsets[-1])], offsets
+
+
+def tree_pack_padded(input_ids, attention_mask, max_tokens_per_mb: int = 8192) -> Tree:
+    """Extract the real tokens of a padded batch and pack them (tpa_tree_pack_padded)."""
+    ids, msk = _padded(input_ids, attention_mask)
+    h = C.c_void_p()
+    check("tpa_tree_pack_padded", lib().tpa_tree_pack_padded(
+        ids.ctypes.data_as(C.POINTER(C.c_int32)), msk.ctypes.data_as(C.POINTER(C.c_uint8)), ids.shape[0],
+        ids.shape[1], int(max_tokens_per_mb), C.byref(h)))
+    return Tree(h)
+
+
 def balance(weights: Sequence[int], capacity: int, min_groups: int = 1, groups_divisor: int = 1,
             algorithm: str = "ffd") -> tuple[np.ndarray, int, str]:
     """Split weighted items into groups (tpa_balance): returns (group of each

@@ -355,6 +355,42 @@ int tpa_tree_pack(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_s
   }
 }
 
+// Step 1 of §树构建过程 (提取序列): the real tokens of a padded row are its
+// input_ids entries whose attention_mask entry is non-zero, in column order
+// (left padding, right padding and interior gaps alike).
+int tpa_extract_sequences(const int32_t* input_ids, const uint8_t* attention_mask, int32_t n_rows,
+                          int32_t row_len, int32_t* tokens_out, int64_t* offsets_out) {
+  if (!input_ids || !attention_mask || !tokens_out || !offsets_out || n_rows < 1 || row_len < 1)
+    return TPA_ERR_INVALID_ARG;
+  int64_t n = 0;
+  offsets_out[0] = 0;
+  for (int32_t r = 0; r < n_rows; ++r) {
+    const int64_t base = int64_t(r) * row_len;
+    for (int32_t c = 0; c < row_len; ++c)
+      if (attention_mask[base + c] != 0) tokens_out[n++] = input_ids[base + c];
+    offsets_out[r + 1] = n;
+  }
+  return TPA_OK;
+}
+
+int tpa_tree_pack_padded(const int32_t* input_ids, const uint8_t* attention_mask, int32_t n_rows,
+                         int32_t row_len, int32_t max_tokens_per_mb, tpa_tree** out) {
+  if (out) *out = nullptr;
+  if (!input_ids || !attention_mask || !out || n_rows < 1 || row_len < 1) return TPA_ERR_INVALID_ARG;
+  try {
+    std::vector<int32_t> tokens(size_t(n_rows) * size_t(row_len));
+    std::vector<int64_t> offsets(size_t(n_rows) + 1);
+    const int rc = tpa_extract_sequences(input_ids, attention_mask, n_rows, row_len, tokens.data(),
+                                         offsets.data());
+    if (rc != TPA_OK) return rc;
+    return pack_impl(tokens.data(), offsets.data(), n_rows, max_tokens_per_mb, out);
+  } catch (const std::bad_alloc&) {
+    return TPA_ERR_NO_MEMORY;
+  } catch (...) {
+    return TPA_ERR_INVALID_ARG;
+  }
+}
+
 int tpa_tree_get_info(const tpa_tree* tree, tpa_tree_info* info) {
   if (!tree || !info) return TPA_ERR_INVALID_ARG;
   *info = tree->info;
