@@ -15,6 +15,8 @@ method computes, written from the AReaL "树训练" (tree training) page:
                   backward, computed node by node over each node's root path.
 * ``logprobs``  — fp64 per-sequence log-probabilities and entropies gathered
                   from the packed tree rows (§对数概率计算).
+* ``lm_head``   — fp64 logits rows from hidden states and the LM-head
+                  weight, for the fused LM-head log-prob path.
 * ``extract``   — step 1 of tree building: real tokens of padded rows from
                   ``input_ids`` and ``attention_mask``.
 * ``balance``   — FFD and KK allocation of weighted items (trees or
@@ -37,3 +39,4 @@ from .attention import attn_forward, attn_backward  # noqa: F401
 from .logprobs import sequence_logprobs_entropy, position_logprobs_entropy  # noqa: F401
 from .balance import ffd_allocate, kk_allocate, packing_metrics, BalanceError  # noqa: F401
 from .extract import extract_sequences  # noqa: F401
+from .lm_head import LazyLogits  # noqa: F401
