@@ -235,7 +235,8 @@ def run_gpu(args, rank, world, local):
     import torch.distributed as dist
 
     import prefix_shared_tree_attention_gb300 as tpa
-    from synth import CONFIGS, flatten_sequences, make_dout, make_logits, make_qkv, make_sequences
+    from synth import (CONFIGS, flatten_sequences, make_dout, make_hidden, make_lm_weight, make_logits, make_qkv,
+                       make_sequences)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -343,6 +344,47 @@ def run_gpu(args, rank, world, local):
             dmask[fmt] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9}
             del buf
         tpa.sync_status()
+
+    # ------------------------------------------------ LM head fused into the log-prob pass
+    # The step upstream of the log-prob rows: logits = hidden @ W^T formed on
+    # tcgen05 tiles and consumed in place.  Hidden size 4096 (a reading: the
+    # pages give none; a 151936-token vocabulary goes with 3584-5120 wide
+    # models), weights and hidden states random.  Shown beside it: the
+    # unfused route, a cuBLAS bf16 GEMM writing the logits then the HBM-bound
+    # log-prob pass (context only: library GEMM, not part of this path).
+    lmh = None
+    if run_lp and args.lm_head_hidden > 0:
+        Hh = args.lm_head_hidden
+        hid = make_hidden(4, rows, Hh, str(dev))
+        wlm = make_lm_weight(4, V, Hh, str(dev))
+        lws = torch.empty(tpa.lm_head_workspace_bytes(rows, V, B, T), dtype=torch.uint8, device=dev)
+        lout = tuple(torch.empty_like(x) for x in lp_out)
+        for _ in range(2):
+            tpa.lm_head_logprobs_entropy(dtree, hid, wlm, out=lout, workspace=lws)
+        reps = 3
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            tpa.lm_head_logprobs_entropy(dtree, hid, wlm, out=lout, workspace=lws)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tpa.sync_status()
+        ms_f = e0.elapsed_time(e1) / reps
+        fl = 2.0 * rows * V * Hh
+        torch.matmul(hid, wlm.T, out=logits)
+        e0.record(stream)
+        for _ in range(reps):
+            torch.matmul(hid, wlm.T, out=logits)
+            tpa.tree_logprobs_entropy(dtree, logits, out=lp_out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_u = e0.elapsed_time(e1) / reps
+        lmh = {"rows": rows, "vocab": V, "hidden": Hh, "ms": ms_f, "tflops": fl / (ms_f / 1e3) / 1e12,
+               "frac_of_bf16_peak": fl / (ms_f / 1e3) / 1e12 / _peaks()[0]["bf16_tflops"],
+               "peak": "measured bf16 burst (the kernel is timed alone)",
+               "logits_bytes_not_written": rows * V * 2,
+               "unfused_cublas_gemm_plus_logprob_ms": ms_u}
+        del hid, wlm, lws, lout
 
     # ------------------------------------------------ end to end from host buffers
     e2e = None
@@ -476,7 +518,7 @@ def run_gpu(args, rank, world, local):
         "attn_fwd_bwd_tflops": attn_tflops, "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
         "logprobs_gbs": lp_gbs, "logprobs_frac_hbm": lp_gbs / peaks["hbm_gbs"],
         "roofline": roof, "clocks": clocks, "gpu_launches": n_launch_per_step * args.steps,
-        "e2e": e2e, "cpu_baseline": cpu, "balance": bal,
+        "e2e": e2e, "cpu_baseline": cpu, "balance": bal, "lm_head": lmh,
         "dense_mask": None if dmask is None else {
             **dmask, "frac_hbm_u8": dmask["u8"]["gbs"] / peaks["hbm_gbs"],
             "note": "write-only export of the [B, T, T] ancestor mask (u8) and its bit-packed form; "
@@ -494,6 +536,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--lm-head-hidden", type=int, default=4096,
+                    help="hidden size of the fused LM-head measurement (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-pairs", type=int, default=15000000,
                     help="ancestor pairs in the oracle's bounded sample")

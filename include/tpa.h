@@ -412,6 +412,31 @@ int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* logits, int
                               int32_t layout, int32_t vocab, float* pos_logp, float* pos_entropy,
                               float* seq_logp, float* seq_entropy, void* stream);
 
+/*
+ * tpa_lm_head_logprobs_entropy — the log-prob pass above with the LM head
+ * fused in front of it (the step upstream of §对数概率计算): the logits of
+ * compact tree row r are logits[r, v] = sum_k hidden[r, k] * weight[v, k],
+ * computed tile by tile on tcgen05 tensor cores (bf16 inputs, fp32
+ * accumulation) and consumed in place, so no logits tensor is written.
+ * Outputs and their definitions are those of tpa_tree_logprobs_entropy.
+ *   hidden   [total_tree_tokens, hidden_size] bf16, device, 16-byte aligned;
+ *            row tok_base[b] + p is tree b, position p (compact rows)
+ *   weight   [vocab, hidden_size] bf16, device, 16-byte aligned
+ *   hidden_size a multiple of 64, <= 65536;  vocab >= 1;  every token id of the
+ *            tree must be < vocab (a larger one yields NaN at its position)
+ *   workspace device buffer of tpa_lm_head_workspace_bytes() bytes, 256-byte
+ *            aligned, contents overwritten (per-row softmax partials, label
+ *            logits, a work counter)
+ * Kernels on `stream`: the fused GEMM + statistics kernel, a combine kernel
+ * and the per-sequence gather.  Errors: TPA_ERR_INVALID_ARG,
+ * TPA_ERR_BUFFER_TOO_SMALL, TPA_ERR_CUDA.
+ */
+uint64_t tpa_lm_head_workspace_bytes(int64_t rows, int32_t vocab, int32_t n_trees, int32_t t_pad);
+int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const void* hidden, const void* weight,
+                                 int32_t hidden_size, int32_t vocab, void* workspace,
+                                 uint64_t workspace_bytes, float* pos_logp, float* pos_entropy,
+                                 float* seq_logp, float* seq_entropy, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */

@@ -93,6 +93,10 @@ PROTOTYPES = {
                                             C.c_int32, C.c_float, C.c_int32, C.c_void_p]),
     "tpa_tree_logprobs_entropy": (C.c_int, [C.POINTER(TreeView), C.c_void_p, C.c_int64, C.c_int32, C.c_int32,
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "tpa_lm_head_workspace_bytes": (C.c_uint64, [C.c_int64, C.c_int32, C.c_int32, C.c_int32]),
+    "tpa_lm_head_logprobs_entropy": (C.c_int, [C.POINTER(TreeView), C.c_void_p, C.c_void_p, C.c_int32, C.c_int32,
+                                               C.c_void_p, C.c_uint64, C.c_void_p, C.c_void_p, C.c_void_p,
+                                               C.c_void_p, C.c_void_p]),
     "tpa_sync_status": (C.c_int, [C.c_void_p]),
     "tpa_device_check": (C.c_int, []),
     "tpa_status_string": (C.c_char_p, [C.c_int]),

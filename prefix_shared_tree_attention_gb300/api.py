@@ -327,6 +327,39 @@ def tree_logprobs_entropy(dtree: DeviceTree, logits: torch.Tensor, layout: str =
     return pl, pe, sl, se
 
 
+def lm_head_workspace_bytes(rows: int, vocab: int, n_trees: int, t_pad: int) -> int:
+    return int(lib().tpa_lm_head_workspace_bytes(int(rows), int(vocab), int(n_trees), int(t_pad)))
+
+
+def lm_head_logprobs_entropy(dtree: DeviceTree, hidden: torch.Tensor, weight: torch.Tensor,
+                             out: tuple | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """The log-prob pass with the LM head fused in: ``hidden`` [tree tokens, H]
+    (compact rows) and ``weight`` [V, H], both CUDA bf16; returns the four
+    outputs of ``tree_logprobs_entropy`` without forming the logits."""
+    for name, t in (("hidden", hidden), ("weight", weight)):
+        if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 matrix")
+    if hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden and weight must have the same hidden size")
+    B, T, N = dtree.info.n_trees, dtree.info.t_pad, dtree.info.total_seq_tokens
+    rows, V, H = hidden.shape[0], weight.shape[0], hidden.shape[1]
+    if rows != dtree.info.total_tree_tokens:
+        raise ValueError("hidden must have one row per tree token (compact rows)")
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty((B, T), dtype=torch.float32, device=dev), torch.empty((B, T), dtype=torch.float32, device=dev),
+               torch.empty(N, dtype=torch.float32, device=dev), torch.empty(N, dtype=torch.float32, device=dev))
+    nbytes = lm_head_workspace_bytes(rows, V, B, T)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    pl, pe, sl, se = out
+    check("tpa_lm_head_logprobs_entropy", lib().tpa_lm_head_logprobs_entropy(
+        C.byref(dtree.view), hidden.data_ptr(), weight.data_ptr(), H, V, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), pl.data_ptr(), pe.data_ptr(), sl.data_ptr(), se.data_ptr(),
+        _stream_ptr(stream)))
+    return pl, pe, sl, se
+
+
 def sync_status(stream=None) -> None:
     """Synchronise the stream and raise if any kernel reported a device-side failure."""
     check("tpa_sync_status", lib().tpa_sync_status(_stream_ptr(stream)))

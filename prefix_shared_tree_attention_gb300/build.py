@@ -17,7 +17,7 @@ OBJ_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libtpa.so")
 
-CUDA_SOURCES = ["runtime.cu", "classify.cu", "logprobs.cu", "attn_fwd.cu", "attn_bwd.cu", "dense_mask.cu"]
+CUDA_SOURCES = ["runtime.cu", "classify.cu", "logprobs.cu", "attn_fwd.cu", "attn_bwd.cu", "dense_mask.cu", "lm_head.cu"]
 HOST_SOURCES = ["pack.cpp", "balance.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

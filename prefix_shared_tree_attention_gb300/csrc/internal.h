@@ -12,3 +12,10 @@ int tpa_internal_status_classify(bool clear);
 int tpa_internal_status_logprobs(bool clear);
 int tpa_internal_status_fwd(bool clear);
 int tpa_internal_status_bwd(bool clear);
+int tpa_internal_status_lmh(bool clear);
+
+// The per-sequence gather of the log-prob pass (logprobs.cu), shared with
+// the fused LM-head path: seq_entropy[t] = pos_entropy[position of token t],
+// seq_logp[t] = pos_logp[position of token t+1] (0 at a sequence's end).
+int tpa_internal_seq_gather(const tpa_tree_view* tree, const float* pos_logp, const float* pos_entropy,
+                            float* seq_logp, float* seq_entropy, void* stream);

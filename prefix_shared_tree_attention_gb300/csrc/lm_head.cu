@@ -1,0 +1,462 @@
+// LM head fused into the log-probability pass (tree training page,
+// §对数概率计算, with the step upstream of it folded in): the logits of tree
+// row r are logits[r, v] = sum_k hidden[r, k] * weight[v, k]; they are formed
+// tile by tile on tcgen05 tensor cores and consumed in place — online
+// softmax statistics and the labels of the row — so they never reach HBM.
+//
+// Kernel 1 (lmh_kernel), persistent, one CTA per SM.  A work item is a
+// (128-row tile, chunk of kVt 256-wide vocab tiles) pair; items run in row
+// groups so the hidden rows of a group stay in L2 while its vocab chunks
+// stream past.  Roles:
+//   warp 16        TMA producer: per vocab tile and 64-wide slice of H, the
+//                  128x64 hidden tile and the 256x64 weight tile into a
+//                  4-stage ring (48 KB a stage).
+//   warp 17        MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16, into
+//                  one of two 256-column TMEM accumulators, so a tile's
+//                  epilogue overlaps the next tile's MMAs.
+//   warps 0-15     epilogue: thread r of warpgroup w reads columns
+//                  [64w, 64w+64) of row r, keeps the row's running max m,
+//                  s = sum exp(x - m) and t = sum exp(x - m) x over its
+//                  columns, and stores the raw logit of every label of the row
+//                  (the token of each child position) that falls in them.
+//                  At the item's end the four warpgroups' (m, s, t) of a row
+//                  are merged in shared memory into one partial per (row,
+//                  chunk).
+// Kernel 2 (lmh_combine_kernel): per tree position, merge the partials of its
+// row into lse = M + log S and entropy = lse - T / S, and write
+// pos_logp[c] = logit[c] - lse for each child c; then the per-sequence gather
+// of the log-prob pass.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+#include "tmap.h"
+
+namespace {
+
+__device__ unsigned int g_status_lmh = 0;
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kVt = 8;                               // vocab tiles per work item
+constexpr int kStages = 4;
+constexpr uint32_t kATile = kBM * kBK * 2;           // 16 KB
+constexpr uint32_t kBTile = kBN * kBK * 2;           // 32 KB
+constexpr uint32_t kStage = kATile + kBTile;
+constexpr int kThreads = 576;                        // 16 epilogue warps + TMA + MMA
+constexpr int kWTma = 16, kWMma = 17;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint32_t kOffMerge = kStages * kStage;     // [2 item parities][3 warpgroups][128 rows] (m, s, t, -)
+constexpr uint32_t kOffBar = kOffMerge + 2 * 3 * kBM * 16;
+// full[kStages], empty[kStages], acc_full[2], acc_free[2], item_full[2], item_empty[2], drain,
+// merge_full[2], merge_free[2]
+constexpr int kNBar = 2 * kStages + 13;
+constexpr uint32_t kOffMisc = kOffBar + kNBar * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 32;       // base checked 1024-byte aligned
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct LmhParams {
+  const int32_t* n_tokens;
+  const int64_t* tok_base;
+  const int32_t* tokens;
+  const int32_t* child_off;
+  const int32_t* child_pos;
+  float4* part;        // [rows][n_vc] (m, s, t, -)
+  float* pair_logit;   // [B*T_pad] raw logit of each position's token under its parent row
+  uint32_t* ctr;       // work counter, zeroed before every launch
+  int64_t rows;
+  int32_t n_trees, t_pad, vocab, hidden, n_rt, n_vt, n_vc, group, n_items;
+};
+
+struct LmhItem {
+  int rt, vc;
+};
+
+__device__ __forceinline__ LmhItem decode(const LmhParams& p, int it) {
+  const int per_group = p.group * p.n_vc;
+  const int g = it / per_group;
+  const int base = g * p.group;
+  const int rg = min(p.group, p.n_rt - base);
+  const int rem = it - g * per_group;
+  return LmhItem{base + rem % rg, rem / rg};
+}
+
+// Tree and position of compact row r (tok_base is the exclusive prefix sum).
+__device__ __forceinline__ void row_to_pos(const LmhParams& p, int64_t r, int& b, int& pos) {
+  int lo = 0, hi = p.n_trees - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.tok_base[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  b = lo;
+  pos = int(r - p.tok_base[lo]);
+}
+
+struct Stats {
+  float m, s, t;
+};
+
+__device__ __forceinline__ void stats_merge(Stats& a, const Stats& b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return;
+  const float ca = tc::ex2((a.m - m) * kLog2e), cb = tc::ex2((b.m - m) * kLog2e);
+  a.s = a.s * ca + b.s * cb;
+  a.t = a.t * ca + b.t * cb;
+  a.m = m;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lmh_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+               const LmhParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (tc::smem_u32(smem) & 1023u) {  // uniform over the CTA: every thread leaves
+    if (threadIdx.x == 0) atomicOr(&g_status_lmh, 2u);
+    return;
+  }
+  float4* sMerge = reinterpret_cast<float4*>(smem + kOffMerge);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = bar;
+  uint64_t* empty = bar + kStages;
+  uint64_t* acc_full = bar + 2 * kStages;     // [2]
+  uint64_t* acc_free = acc_full + 2;          // [2]
+  uint64_t* item_full = acc_full + 4;         // [2]
+  uint64_t* item_empty = acc_full + 6;        // [2]
+  uint64_t* drain = acc_full + 8;
+  uint64_t* merge_full = acc_full + 9;        // [2]: warpgroups 1-3 have written an item's statistics
+  uint64_t* merge_free = acc_full + 11;       // [2]: warpgroup 0 has read them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);  // [2]
+  const int warp = threadIdx.x >> 5;
+  const int n_k = p.hidden / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(acc_full + s, 1);
+      tc::mbar_init(acc_free + s, 512);
+      tc::mbar_init(item_full + s, 1);
+      tc::mbar_init(item_empty + s, 1 + 512);
+      tc::mbar_init(merge_full + s, 384);
+      tc::mbar_init(merge_free + s, 128);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == kWMma) tc::tmem_alloc(tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wait_u = [&](uint64_t* b_, uint32_t par) {
+    return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_lmh));
+  };
+
+  if (warp == kWTma) {
+    // ------------------------------------------------------------ producer
+    if (tc::elect_one()) {
+      tc::tma_prefetch_desc(&tm_h);
+      tc::tma_prefetch_desc(&tm_w);
+    }
+    __syncwarp();
+    int q = 0;  // stage loads issued
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+      uint32_t u = 0;
+      if ((threadIdx.x & 31) == 0) u = atomicAdd(p.ctr, 1u);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      const int it = u < uint32_t(p.n_items) ? int(u) : -1;
+      if (tc::elect_one()) {
+        item_ring[k & 1] = it;
+        tc::mbar_arrive(item_full + (k & 1));
+      }
+      __syncwarp();
+      if (it < 0) break;
+      const LmhItem I = decode(p, it);
+      const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
+      for (int vt = I.vc * kVt; ok && vt < vt1; ++vt) {
+        for (int kc = 0; kc < n_k; ++kc, ++q) {
+          const int s = q % kStages;
+          if (!(ok = wait_u(empty + s, ((q / kStages) & 1) ^ 1))) break;
+          if (tc::elect_one()) {
+            uint8_t* dst = smem + s * kStage;
+            tc::mbar_arrive_expect_tx(full + s, kStage);
+            tc::tma_load_3d(dst, &tm_h, full + s, kc * kBK, 0, I.rt * kBM);
+            tc::tma_load_3d(dst + kATile, &tm_w, full + s, kc * kBK, 0, vt * kBN);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
+      volatile int never = 0;
+      for (int j = (q > kStages ? q - kStages : 0); j < q; ++j)
+        tc::mbar_wait(full + (j % kStages), (j / kStages) & 1, &never, &g_status_lmh, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp == kWMma) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = tc::idesc_bf16(kBM, kBN, false, false);
+    const uint64_t dA = tc::smem_desc(tc::smem_u32(smem), 16, 1024);
+    const uint64_t dB = tc::smem_desc(tc::smem_u32(smem + kATile), 16, 1024);
+    int q = 0, nt = 0;  // stages consumed, tiles accumulated
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
+      const int it = item_ring[k & 1];
+      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
+      __syncwarp();
+      if (it < 0) break;
+      const LmhItem I = decode(p, it);
+      const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
+      for (int vt = I.vc * kVt; ok && vt < vt1; ++vt, ++nt) {
+        const int ab = nt & 1;
+        if (nt >= 2 && !(ok = wait_u(acc_free + ab, ((nt >> 1) - 1) & 1))) break;
+        for (int kc = 0; kc < n_k; ++kc, ++q) {
+          const int s = q % kStages;
+          if (!(ok = wait_u(full + s, (q / kStages) & 1))) break;
+          tc::tc_fence_after();
+          if (tc::elect_one()) {
+            const uint32_t so = (s * kStage) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              tc::mma_ss(tmem + 256 * ab, dA + so + ((kk * 32) >> 4), dB + so + ((kk * 32) >> 4), idesc,
+                         (kc > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_commit(empty + s);
+            if (kc + 1 == n_k) tc::mma_commit(acc_full + ab);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (*abort_flag && tc::elect_one()) {  // let issued MMAs finish before TMEM is released
+      volatile int never = 0;
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0, &never, &g_status_lmh, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warpgroups
+    const int w = warp >> 2;          // vocab columns [64w, 64w+64) of each tile
+    const int r = threadIdx.x & 127;  // row of the tile = TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    int nt = 0, ni = 0;  // tiles and items with work processed
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!wait_u(item_full + (k & 1), (k >> 1) & 1)) break;
+      const int it = item_ring[k & 1];
+      tc::mbar_arrive(item_empty + (k & 1));
+      if (it < 0) break;
+      const LmhItem I = decode(p, it);
+      const int64_t row = int64_t(I.rt) * kBM + r;
+      const bool real = row < p.rows;
+      // children of this row: their tokens are its labels
+      int b = 0, pos = 0, c0 = 0, c1 = 0, lmin = 0x7fffffff, lmax = -1;
+      if (real) {
+        row_to_pos(p, row, b, pos);
+        c0 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos];
+        c1 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos + 1];
+        for (int c = c0; c < c1; ++c) {
+          const int tok = p.tokens[int64_t(b) * p.t_pad + p.child_pos[int64_t(b) * p.t_pad + c]];
+          lmin = min(lmin, tok);
+          lmax = max(lmax, tok);
+        }
+      }
+      Stats st{-INFINITY, 0.f, 0.f};
+      const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
+      for (int vt = I.vc * kVt; vt < vt1; ++vt, ++nt) {
+        const int ab = nt & 1;
+        if (!wait_u(acc_full + ab, (nt >> 1) & 1)) { ok = false; break; }
+        tc::tc_fence_after();
+        const int v0 = vt * kBN + 64 * w;  // vocab index of this thread's first column
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t x[32];
+          tc::tmem_ld32(tmem + lane_base + 256 * ab + 64 * w + 32 * h, x);
+          tc::tmem_ld_wait();
+          if (h == 1) {
+            tc::tc_fence_before();
+            tc::mbar_arrive(acc_free + ab);  // both halves are in registers
+          }
+          const int vb = v0 + 32 * h;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (vb + c >= p.vocab) x[c] = __float_as_uint(-INFINITY);
+            mx = fmaxf(mx, __uint_as_float(x[c]));
+          }
+          if (mx > st.m) {
+            const float cf = tc::ex2((st.m - mx) * kLog2e);
+            st.s *= cf;
+            st.t *= cf;
+            st.m = mx;
+          }
+          if (st.m > -INFINITY) {
+            const float mb = st.m * kLog2e;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float xv = __uint_as_float(x[c]);
+              const float e = tc::ex2(fmaf(xv, kLog2e, -mb));
+              st.s += e;
+              st.t = (vb + c < p.vocab) ? fmaf(e, xv, st.t) : st.t;
+            }
+          }
+          if (real && lmax >= vb && lmin < vb + 32) {  // a label may fall in these 32 columns
+            for (int c = c0; c < c1; ++c) {
+              const int cp = p.child_pos[int64_t(b) * p.t_pad + c];
+              const int col = p.tokens[int64_t(b) * p.t_pad + cp] - vb;
+              if (col >= 0 && col < 32) {
+                uint32_t v = x[0];
+#pragma unroll
+                for (int j = 1; j < 32; ++j) v = (col == j) ? x[j] : v;
+                p.pair_logit[int64_t(b) * p.t_pad + cp] = __uint_as_float(v);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      // Merge the four warpgroups' statistics of each row into one partial,
+      // through a buffer that alternates by item.
+      float4* mb = sMerge + (ni & 1) * 3 * kBM;
+      if (w > 0) {
+        if (ni >= 2 && !wait_u(merge_free + (ni & 1), ((ni >> 1) - 1) & 1)) { ok = false; break; }
+        mb[(w - 1) * kBM + r] = make_float4(st.m, st.s, st.t, 0.f);
+        tc::mbar_arrive(merge_full + (ni & 1));
+      } else {
+        if (!wait_u(merge_full + (ni & 1), (ni >> 1) & 1)) { ok = false; break; }
+        if (real) {
+          Stats a = st;
+          for (int u = 0; u < 3; ++u) {
+            const float4 o = mb[u * kBM + r];
+            stats_merge(a, Stats{o.x, o.y, o.z});
+          }
+          p.part[row * p.n_vc + I.vc] = make_float4(a.m, a.s, a.t, 0.f);
+        }
+        tc::mbar_arrive(merge_free + (ni & 1));
+      }
+      ++ni;
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == kWMma) tc::tmem_dealloc(tmem, 512);
+}
+
+// One thread per tree position (b, pos): merges its row's partials; writes its
+// entropy, the log-probs of its children, and 0 where nothing is defined.
+__global__ void __launch_bounds__(256) lmh_combine_kernel(const LmhParams p, const int32_t* __restrict__ parent,
+                                                         float* __restrict__ pos_logp,
+                                                         float* __restrict__ pos_entropy) {
+  const int64_t at = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (at >= int64_t(p.n_trees) * p.t_pad) return;
+  const int b = int(at / p.t_pad), pos = int(at % p.t_pad);
+  if (pos >= p.n_tokens[b]) {
+    pos_logp[at] = 0.f;
+    pos_entropy[at] = 0.f;
+    return;
+  }
+  const int64_t row = p.tok_base[b] + pos;
+  Stats a{-INFINITY, 0.f, 0.f};
+  for (int vc = 0; vc < p.n_vc; ++vc) {
+    const float4 o = p.part[row * p.n_vc + vc];
+    stats_merge(a, Stats{o.x, o.y, o.z});
+  }
+  const float lse = a.m + __log2f(a.s) * kLn2;
+  pos_entropy[at] = lse - a.t / a.s;
+  if (parent[at] < 0) pos_logp[at] = 0.f;  // no parent row: no label
+  const int c0 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos];
+  const int c1 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos + 1];
+  for (int c = c0; c < c1; ++c) {
+    const int cp = p.child_pos[int64_t(b) * p.t_pad + c];
+    const int tok = p.tokens[int64_t(b) * p.t_pad + cp];
+    pos_logp[int64_t(b) * p.t_pad + cp] =
+        (tok >= 0 && tok < p.vocab) ? p.pair_logit[int64_t(b) * p.t_pad + cp] - lse : __int_as_float(0x7fc00000);
+  }
+}
+
+int num_sms_lmh() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  return sms;
+}
+
+inline uint64_t al256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+}  // namespace
+
+TPA_DEFINE_STATUS_READER(tpa_internal_status_lmh, g_status_lmh)
+
+extern "C" uint64_t tpa_lm_head_workspace_bytes(int64_t rows, int32_t vocab, int32_t n_trees, int32_t t_pad) {
+  if (rows < 1 || vocab < 1 || n_trees < 1 || t_pad < 1) return 0;
+  const uint64_t n_vt = (uint64_t(vocab) + kBN - 1) / kBN;
+  const uint64_t n_vc = (n_vt + kVt - 1) / kVt;
+  return 256 + al256(uint64_t(rows) * n_vc * 16) + al256(uint64_t(n_trees) * uint64_t(t_pad) * 4);
+}
+
+extern "C" int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const void* hidden, const void* weight,
+                                            int32_t hidden_size, int32_t vocab, void* workspace,
+                                            uint64_t workspace_bytes, float* pos_logp, float* pos_entropy,
+                                            float* seq_logp, float* seq_entropy, void* stream) {
+  if (!tree || !hidden || !weight || !workspace || !pos_logp || !pos_entropy || !seq_logp || !seq_entropy)
+    return TPA_ERR_INVALID_ARG;
+  if (tree->n_trees < 1 || tree->t_pad < 1 || tree->n_seqs < 1 || tree->total_tree_tokens < 1)
+    return TPA_ERR_INVALID_ARG;
+  if (hidden_size < kBK || hidden_size % kBK != 0 || hidden_size > 65536 || vocab < 1) return TPA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(weight)) & 15) return TPA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return TPA_ERR_INVALID_ARG;
+  const int64_t rows = tree->total_tree_tokens;
+  if (workspace_bytes < tpa_lm_head_workspace_bytes(rows, vocab, tree->n_trees, tree->t_pad))
+    return TPA_ERR_BUFFER_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  LmhParams p;
+  p.n_tokens = tree->n_tokens;
+  p.tok_base = tree->tok_base;
+  p.tokens = tree->tokens;
+  p.child_off = tree->child_off;
+  p.child_pos = tree->child_pos;
+  p.rows = rows;
+  p.n_trees = tree->n_trees;
+  p.t_pad = tree->t_pad;
+  p.vocab = vocab;
+  p.hidden = hidden_size;
+  p.n_rt = int((rows + kBM - 1) / kBM);
+  p.n_vt = (vocab + kBN - 1) / kBN;
+  p.n_vc = (p.n_vt + kVt - 1) / kVt;
+  // rows of a group: their hidden tiles (128 x H bf16 each) take about 48 MB of L2
+  const int64_t per_tile = int64_t(kBM) * hidden_size * 2;
+  p.group = int(std::max<int64_t>(1, std::min<int64_t>(p.n_rt, (int64_t(48) << 20) / per_tile)));
+  p.n_items = p.n_rt * p.n_vc;
+  p.ctr = reinterpret_cast<uint32_t*>(ws);
+  p.part = reinterpret_cast<float4*>(ws + 256);
+  p.pair_logit = reinterpret_cast<float*>(ws + 256 + al256(uint64_t(rows) * p.n_vc * 16));
+  CUtensorMap tm_h, tm_w;
+  if (!tmap::make_rows_heads_d(&tm_h, hidden, uint64_t(rows), 1, uint64_t(hidden_size), kBM) ||
+      !tmap::make_rows_heads_d(&tm_w, weight, uint64_t(vocab), 1, uint64_t(hidden_size), kBN))
+    return TPA_ERR_CUDA;
+  TPA_CUDA_TRY(cudaMemsetAsync(ws, 0, 16, st));
+  TPA_CUDA_TRY(cudaFuncSetAttribute(lmh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+  const int sms = num_sms_lmh();
+  lmh_kernel<<<p.n_items < sms ? p.n_items : sms, kThreads, kSmemBytes, st>>>(tm_h, tm_w, p);
+  TPA_CUDA_TRY(cudaGetLastError());
+  const int64_t n_pos = int64_t(tree->n_trees) * tree->t_pad;
+  lmh_combine_kernel<<<int((n_pos + 255) / 256), 256, 0, st>>>(p, tree->parent, pos_logp, pos_entropy);
+  TPA_CUDA_TRY(cudaGetLastError());
+  return tpa_internal_seq_gather(tree, pos_logp, pos_entropy, seq_logp, seq_entropy, stream);
+}

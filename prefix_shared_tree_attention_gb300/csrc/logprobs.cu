@@ -189,6 +189,12 @@ extern "C" int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* 
       tree->tok_base, tree->tokens, tree->parent, tree->child_off, tree->child_pos, pos_logp,
       pos_entropy);
   TPA_CUDA_TRY(cudaGetLastError());
+  return tpa_internal_seq_gather(tree, pos_logp, pos_entropy, seq_logp, seq_entropy, stream);
+}
+
+int tpa_internal_seq_gather(const tpa_tree_view* tree, const float* pos_logp, const float* pos_entropy,
+                            float* seq_logp, float* seq_entropy, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   seq_gather_kernel<<<tree->n_seqs, 256, 0, st>>>(tree->t_pad, tree->seq_tree, tree->seq_off,
                                                   tree->seq_pos, pos_logp, pos_entropy, seq_logp,
                                                   seq_entropy);

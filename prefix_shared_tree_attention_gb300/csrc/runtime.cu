@@ -100,8 +100,9 @@ int tpa_sync_status(void* stream) {
     return TPA_ERR_CUDA;
   }
   int worst = TPA_OK;
-  const int s[4] = {tpa_internal_status_classify(true), tpa_internal_status_logprobs(true),
-                    tpa_internal_status_fwd(true), tpa_internal_status_bwd(true)};
+  const int s[5] = {tpa_internal_status_classify(true), tpa_internal_status_logprobs(true),
+                    tpa_internal_status_fwd(true), tpa_internal_status_bwd(true),
+                    tpa_internal_status_lmh(true)};
   for (int x : s) {
     if (x == TPA_ERR_CUDA) return TPA_ERR_CUDA;
     if (x != TPA_OK) worst = x;

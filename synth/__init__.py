@@ -211,3 +211,22 @@ def make_logits(cid: int, rows: int, vocab: int, device: str = "cpu", chunk_rows
         r1 = min(rows, r0 + chunk_rows)
         out[r0:r1] = (2.0 * torch.randn((r1 - r0, vocab), generator=g, device=device)).to(torch.bfloat16)
     return out
+
+
+def make_hidden(cid: int, rows: int, hidden: int, device: str = "cpu"):
+    """Hidden states ``[rows, hidden]`` bf16 ~ N(0, 1) (the LM head's input),
+    from a ``torch.Generator`` on ``device`` seeded ``1000 * cid + 6``."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 * cid + 6)
+    return torch.randn((rows, hidden), generator=g, device=device).to(torch.bfloat16)
+
+
+def make_lm_weight(cid: int, vocab: int, hidden: int, device: str = "cpu"):
+    """LM-head weight ``[vocab, hidden]`` bf16 ~ N(0, (2 / sqrt(hidden))^2), so
+    that logits of N(0, 1) hidden states have standard deviation 2 like the
+    logits workload; ``torch.Generator`` on ``device`` seeded ``1000 * cid + 7``."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 * cid + 7)
+    return (torch.randn((vocab, hidden), generator=g, device=device) * (2.0 / hidden ** 0.5)).to(torch.bfloat16)
