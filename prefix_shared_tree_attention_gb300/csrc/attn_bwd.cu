@@ -73,6 +73,7 @@ struct BwdParams {
   uint32_t* sched;      // work counters: [2..3] KV kernel, [4..5] dQ kernel
   int32_t t_pad, n_blk, cap, hq, hkv;
   int32_t n_trees, kv_chunk, kv_nchunk, kv_items, dq_items;
+  int32_t wide;  // gradient outputs 32-byte aligned: fp32 rows stored 32 bytes at a time
   float scale, scale_log2;
 };
 
@@ -92,12 +93,31 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
+__device__ __forceinline__ void st_v8(void* addr, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // Writes 16 fp32 values of one row as fp32 or bf16 (with a scale), or adds
-// them into an fp32 row.
+// them into an fp32 row.  `wide`: the row is 32-byte aligned and fp32 rows
+// go out as two 32-byte stores (one full sector each) instead of four
+// 16-byte stores.
 template <bool F32OUT>
-__device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16], float scale, bool add) {
+__device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16], float scale, bool add,
+                                            bool wide = false) {
   if (F32OUT) {
     float* f = reinterpret_cast<float*>(dst);
+    if (!add && wide) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(__uint_as_float(v[8 * h + e]) * scale);
+        st_v8(f + 8 * h, w);
+      }
+      return;
+    }
     if (add) {
 #pragma unroll
       for (int t = 0; t < 4; ++t)
@@ -611,8 +631,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld16(tmem + lane_base + T_DV + w * DW + c * 16, vv);
         tc::tmem_ld16(tmem + lane_base + T_DK + w * DW + c * 16, kk);
         tc::tmem_ld_wait();
-        store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, add);
-        store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, p.scale, add);
+        store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, add, p.wide);
+        store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, p.scale, add, p.wide);
       }
       tc::tc_fence_before();
       tc::mbar_arrive(acc_free);
@@ -974,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[16];
         tc::tmem_ld16(tmem + lane_base + T_DQ + w * DW + c * 16, v);
         tc::tmem_ld_wait();
-        store_row16<F32OUT>(dq_row + c * 16 * ESZ, v, p.scale, false);
+        store_row16<F32OUT>(dq_row + c * 16 * ESZ, v, p.scale, false, p.wide);
       }
       tc::tc_fence_before();
       tc::mbar_arrive(dq_free);
@@ -1122,6 +1142,7 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.kv_chunk = kv_chunk;
   prm.kv_nchunk = (G * mask->n_blk + prm.kv_chunk - 1) / prm.kv_chunk;
   prm.n_trees = tree->n_trees;
+  prm.wide = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 31) == 0;
   prm.kv_items = tree->n_trees * hkv * mask->n_blk * prm.kv_nchunk;
   prm.dq_items = tree->n_trees * hq * mask->n_blk;
   prm.scale = scale;
