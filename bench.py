@@ -87,6 +87,44 @@ def _profile_traffic(entry: str, tree_tokens: int):
     return total if total > 0 else None
 
 
+def rank_sequences(rank: int, world: int, tpa):
+    """The sequences rank ``rank`` of ``world`` processes.
+
+    One rank: the GRPO-shaped batch (seed 2).  N ranks: N such batches
+    (seeds 2 + 1000 r) are packed together on every rank (the packer is
+    deterministic), and the trees are split over the ranks by KK balancing of
+    each tree's ancestor pairs, the attention work; a rank keeps the
+    sequences of its trees.  Per-rank work stays that of one batch (weak
+    scaling) and the data path needs no collective."""
+    from synth import CONFIGS, flatten_sequences, make_sequences
+    if world == 1:
+        return make_sequences(2, seed=2)
+    seqs = [s for r in range(world) for s in make_sequences(2, seed=2 + 1000 * r)]
+    toks, offs = flatten_sequences(seqs)
+    tree = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=CONFIGS[2].max_tokens_per_mb)
+    arr = tree.arrays()
+    depth, ntok = arr["depth"].reshape(tree.n_trees, -1), arr["n_tokens"]
+    pairs = [int((depth[b, :ntok[b]] + 1).sum()) for b in range(tree.n_trees)]
+    group_of, n_groups, _ = tpa.balance(pairs, 10**15, world, 1, "kk")
+    mine = {b for b in range(tree.n_trees) if group_of[b] == rank % n_groups}
+    return [s for s, b in zip(seqs, arr["seq_tree"]) if int(b) in mine]
+
+
+def reduce_job(flops: float, rows: int, ms: float):
+    """Whole-job totals over the ranks: work summed, time the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return flops, rows, ms
+    t = torch.tensor([flops, float(rows)], dtype=torch.float64)
+    m = torch.tensor([ms], dtype=torch.float64)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t, m = t.to(dev), m.to(dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(t[0]), int(t[1]), float(m[0])
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -242,8 +280,7 @@ def run_gpu(args, rank, world, local):
     dev = torch.device("cuda", local)
     tpa.device_check()
     cfg, lcfg = CONFIGS[2], CONFIGS[4]
-    seed = 2 + 1000 * rank  # weak scaling: every rank packs and processes its own batch of trees
-    seqs = make_sequences(2, seed=seed)
+    seqs = rank_sequences(rank, world, tpa)  # weak scaling: one batch's worth of trees per rank
     toks, offs = flatten_sequences(seqs)
     T, Hq, Hkv, d, V = cfg.max_tokens_per_mb, cfg.n_heads_q, cfg.n_heads_kv, cfg.head_dim, lcfg.logits_vocab
 
@@ -315,10 +352,8 @@ def run_gpu(args, rank, world, local):
     total_ms = t_start.elapsed_time(t_end)
     seg = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)])
     t_cls, t_fwd, t_bwd, t_lp = seg.mean(axis=0)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    # whole job: work summed over the ranks, time of the slowest rank
+    job_flops, job_rows, total_ms = reduce_job(flops_step, rows, total_ms)
     ms_step = total_ms / args.steps
     clocks = clk.summary()
 
@@ -431,7 +466,7 @@ def run_gpu(args, rank, world, local):
         tpa.sync_status()
         h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, dop, lg_host)) + int(info.blob_bytes)
         d2h = sum(x.numel() * x.element_size() for x in out_host) + 2 * 4 * N
-        e2e = {"value": world * flops_step / e2e_sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_flops / e2e_sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_sec * 1e3,
                "includes": "host pack + metadata upload + pinned H2D of q,k,v,dO,logits + device step + "
                            "D2H of O,dQ,dK,dV,seq log-probs/entropies"}
@@ -503,7 +538,7 @@ def run_gpu(args, rank, world, local):
         r = cpu_oracle_run(1, 0, args.oracle_pairs)
         cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
 
-    value = world * flops_step / (ms_step / 1e3) / 1e12
+    value = job_flops / (ms_step / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -511,8 +546,9 @@ def run_gpu(args, rank, world, local):
         "config": {"workload": WORKLOAD, "n_trees": B, "tree_tokens": rows, "original_tokens": int(N),
                    "tree_token_ratio": info.tree_token_ratio, "ancestor_pairs": pairs,
                    "flops_per_step": flops_step, "l2": "inputs larger than L2 (129 MB); no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "tree_tokens_per_s": world * rows / (ms_step / 1e3),
+                   "parallelism": (f"trees split over {world} ranks by KK balancing of ancestor pairs"
+                                   if world > 1 else "single GPU")},
+        "tree_tokens_per_s": job_rows / (ms_step / 1e3),
         "frac_of_bf16_peak": value / peak_sus,
         "breakdown_ms": {"block_classify": t_cls, "attn_fwd": t_fwd, "attn_bwd": t_bwd, "logprobs_entropy": t_lp},
         "attn_fwd_bwd_tflops": attn_tflops, "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
