@@ -56,6 +56,7 @@ struct FwdParams {
   const uint4* qmask;
   uint32_t* sched;   // [0] next work item, [1] finished CTAs (both back to 0 at kernel end)
   int32_t t_pad, n_blk, cap, hq, hkv, n_items;
+  int32_t wide;      // o is 32-byte aligned: its rows go out 32 bytes at a time
   float scale_log2;  // softmax scale * log2(e)
 };
 
@@ -478,11 +479,20 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           w[u] = tc::pack_bf16(__uint_as_float(ov[2 * u]) * inv, __uint_as_float(ov[2 * u + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-        dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        if (p.wide) {  // two 32-byte stores: one full sector each
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + c * 32), "r"(w[0]),
+                       "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                       : "memory");
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + c * 32 + 16),
+                       "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+                       : "memory");
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(o_free + h);  // O_h may be overwritten by the next item
@@ -538,6 +548,7 @@ int launch_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
     return TPA_ERR_CUDA;
   FwdParams prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.wide = (reinterpret_cast<uintptr_t>(o) & 31) == 0;
   prm.lse = lse;
   prm.q_ptr = mask->q_ptr;
   prm.q_idx = mask->q_idx;
