@@ -658,6 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // R[(j+2)%3], whose dS(j-1) dQ(j-1) read before them) are issued then, ahead
 // of dQ(j); the next tile's exponentials overlap dQ(j) and dP(j+1).
 
+constexpr int kNIR = 4;  // dQ item ring slots: the producer publishes an item one ahead
+
 template <int D>
 struct DqCfg {
   static constexpr int NCH = D / 64;
@@ -670,10 +672,12 @@ struct DqCfg {
   static constexpr uint32_t OFF_V = OFF_K + NSK * TILE;
   static constexpr uint32_t OFF_BAR = OFF_V + NSV * TILE;
   // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, dp_full,
-  // dp_free, ds_ready[2], dq_final, dq_free, drain, item_full[2], item_empty[2]
-  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 8 + 4;
+  // dp_free, ds_ready[2], dq_final, dq_free, drain, item_full[NIR], item_empty[NIR]
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 8 + 2 * kNIR;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 32;  // base checked 1024-byte aligned
+  // tmem slot, abort flag, then the item ring: kNIR x {index, n, e0, first CSR entry}
+  static constexpr uint32_t OFF_RING = OFF_MISC + 16;
+  static constexpr uint32_t BYTES = OFF_RING + kNIR * 16;  // base checked 1024-byte aligned
   static_assert(BYTES <= kSmemMax, "shared memory budget");
 };
 
@@ -694,6 +698,16 @@ __device__ __forceinline__ DqItem decode_dq(const BwdParams& p, int it) {
   r.n = rp[r.qb + 1] - r.e0;
   r.list = p.q_idx + int64_t(r.b) * p.cap + r.e0;
   return r;
+}
+
+// (tree, query head, query block) of dQ item `it`, the index arithmetic of
+// decode_dq without its CSR reads.
+__device__ __forceinline__ void dq_coords(const BwdParams& p, int it, int& b, int& h, int& qb) {
+  const int per_b = p.hq * p.n_blk;
+  b = it / per_b;
+  const int rem = it - b * per_b;
+  h = rem / p.n_blk;
+  qb = p.n_blk - 1 - rem % p.n_blk;
 }
 
 __device__ __forceinline__ uint32_t rot3(int j) { return uint32_t(j % 3) * 128u; }
@@ -730,11 +744,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_final = s_full + 5;
   uint64_t* dq_free = s_full + 6;
   uint64_t* drain = s_full + 7;
-  uint64_t* item_full = s_full + 8;    // [2]
-  uint64_t* item_empty = s_full + 10;  // [2]
+  uint64_t* item_full = s_full + 8;            // [kNIR]
+  uint64_t* item_empty = s_full + 8 + kNIR;    // [kNIR]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // [2]
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_RING);  // [kNIR][4]
 
   const int warp = threadIdx.x >> 5;
   const int G = p.hq / p.hkv;
@@ -760,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(dq_final, 1);
     tc::mbar_init(dq_free, 128 * kNWG);
     tc::mbar_init(drain, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kNIR; ++s) {
       tc::mbar_init(item_full + s, 1);
       tc::mbar_init(item_empty + s, NCONS);
     }
@@ -787,23 +801,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     int gk = 0, gv = 0, nq = 0;  // K tiles, V tiles and Q tiles loaded so far
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
-      const int it = fetch_item(p.sched + 4, p.dq_items, item_ring + (k & 1), item_full + (k & 1));
-      if (it < 0) break;
-      const DqItem I = decode_dq(p, it);
-      if (I.n == 0) continue;
-      const int g = I.h / G;
-      const int row0 = I.b * p.t_pad + I.qb * kB;
-      if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
+    // Slot k of the ring gets the k-th item this CTA takes, decoded (index or
+    // -1 once the items are used up, its tile count, CSR start and first
+    // entry), so that no consumer reads the CSR at an item boundary.  Item
+    // k + 1 is published while item k's tiles are still being loaded.
+    auto take = [&](int k, DqItem& I) -> int {  // -2: aborted
+      if (!wait_u(item_empty + (k % kNIR), ((k / kNIR) & 1) ^ 1)) return -2;
+      uint32_t u = 0;
+      if ((threadIdx.x & 31) == 0) u = atomicAdd(p.sched + 4, 1u);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      const int it = u < uint32_t(p.dq_items) ? int(u) : -1;  // unsigned: no index below 0
+      I.n = 0;
+      if (it >= 0) I = decode_dq(p, it);
+      const int first = I.n > 0 ? I.list[0] : 0;
       if (tc::elect_one()) {
-        tc::mbar_arrive_expect_tx(q_full, 2 * TILE);
-        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sQ + c * kChunk, &tm_q, q_full, c * 64, I.h, row0);
-        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sDO + c * kChunk, &tm_do, q_full, c * 64, I.h, row0);
+        volatile int* slot = item_ring + 4 * (k % kNIR);
+        slot[0] = it;
+        slot[1] = I.n;
+        slot[2] = it >= 0 ? I.e0 : 0;
+        slot[3] = first;
+        tc::mbar_arrive(item_full + (k % kNIR));
       }
       __syncwarp();
-      ++nq;
-      int entry = I.list[0];
+      return it;
+    };
+    DqItem I, J;
+    int it = take(0, I);
+    ok = it != -2;
+    for (int k = 0; ok && it >= 0; ++k) {
+      const int g = I.h / G;
+      if (I.n > 0) {
+        const int row0 = I.b * p.t_pad + I.qb * kB;
+        if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          tc::mbar_arrive_expect_tx(q_full, 2 * TILE);
+          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sQ + c * kChunk, &tm_q, q_full, c * 64, I.h, row0);
+          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sDO + c * kChunk, &tm_do, q_full, c * 64, I.h, row0);
+        }
+        __syncwarp();
+        ++nq;
+      }
+      const int jt = take(k + 1, J);
+      if (!(ok = jt != -2)) break;
+      if (jt >= 0 && J.n > 0 && tc::elect_one()) {  // the next item's Q and dO into L2 meanwhile
+        const int nrow0 = J.b * p.t_pad + J.qb * kB;
+        for (int c = 0; c < NCH; ++c) {
+          tc::tma_prefetch_3d(&tm_q, c * 64, J.h, nrow0);
+          tc::tma_prefetch_3d(&tm_do, c * 64, J.h, nrow0);
+        }
+      }
+      __syncwarp();
+      int entry = I.n > 0 ? I.list[0] : 0;
       for (int j = 0; ok && j < I.n; ++j) {
         const int krow = I.b * p.t_pad + (entry >> 1) * kB;
         if (j + 1 < I.n) entry = I.list[j + 1];
@@ -824,6 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         ++gv;
       }
+      I = J;
+      it = jt;
     }
     if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
       volatile int never = 0;
@@ -873,13 +923,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int gt = 0, nq = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
-      const int it = item_ring[k & 1];
-      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
+      if (!(ok = wait_u(item_full + (k % kNIR), (k / kNIR) & 1))) break;
+      const int it = item_ring[4 * (k % kNIR)];
+      const int n = item_ring[4 * (k % kNIR) + 1];
+      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k % kNIR));
       __syncwarp();
       if (it < 0) break;
-      const DqItem I = decode_dq(p, it);
-      const int n = I.n;
       if (n == 0) continue;
       if (!(ok = wait_u(q_full, nq & 1))) break;
       if (!(ok = issue_sdp(gt))) break;
@@ -923,33 +972,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int DW = D / kNWG;
     int gt = 0, nq = 0;
     bool ok = true;
+    // The next item from the ring, with this thread's LSE, D and first mask
+    // word requested before the current item's dQ stores go out (a load
+    // issued behind 64 KB of stores waits for them to drain).
+    struct Next {
+      int it, n, e0, first;
+      float lse, drow;
+      uint32_t mk;
+    };
+    auto prefetch = [&](int k, Next& x) -> bool {
+      if (!wait_u(item_full + (k % kNIR), (k / kNIR) & 1)) return false;
+      const volatile int* slot = item_ring + 4 * (k % kNIR);
+      x.it = slot[0];
+      x.n = slot[1];
+      x.e0 = slot[2];
+      x.first = slot[3];
+      tc::mbar_arrive(item_empty + (k % kNIR));
+      x.lse = 0.f;
+      x.drow = 0.f;
+      x.mk = 0u;
+      if (x.it >= 0 && x.n > 0) {
+        int b, h, qb;
+        dq_coords(p, x.it, b, h, qb);
+        const int64_t vec = (int64_t(b) * p.hq + h) * p.t_pad + qb * kB + r;
+        x.lse = p.lse[vec];
+        x.drow = p.dvec[vec];
+        if (!(x.first & 1))
+          x.mk = reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(b) * p.cap + x.e0) * kB + r)[w];
+      }
+      return true;
+    };
+    Next nx;
+    ok = prefetch(0, nx);
     for (int k = 0; ok; ++k) {
-      if (!wait_u(item_full + (k & 1), (k >> 1) & 1)) break;
-      const int it = item_ring[k & 1];
-      tc::mbar_arrive(item_empty + (k & 1));
-      if (it < 0) break;
-      const DqItem I = decode_dq(p, it);
-      const int row0 = I.b * p.t_pad + I.qb * kB;
-      uint8_t* dq_row = static_cast<uint8_t*>(p.dq) + ((int64_t(row0 + r) * p.hq + I.h) * D + w * DW) * ESZ;
+      const Next I = nx;
+      if (I.it < 0) break;
+      int b, h, qb;
+      dq_coords(p, I.it, b, h, qb);
+      const int row0 = b * p.t_pad + qb * kB;
+      uint8_t* dq_row = static_cast<uint8_t*>(p.dq) + ((int64_t(row0 + r) * p.hq + h) * D + w * DW) * ESZ;
       if (I.n == 0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c = 0; c < DW * ESZ / 16; ++c) reinterpret_cast<uint4*>(dq_row)[c] = z;
+        ok = prefetch(k + 1, nx);
         continue;
       }
-      const int64_t vec = (int64_t(I.b) * p.hq + I.h) * p.t_pad + I.qb * kB + r;
-      const float nlse2 = -p.lse[vec] * kLog2e;
-      const float drow = p.dvec[vec];
+      const float nlse2 = -I.lse * kLog2e;
+      const float drow = I.drow;
       const uint32_t* qmask_row =
-          reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(I.b) * p.cap + I.e0) * kB + r) + w;
-      int entry = I.list[0];
-      uint32_t mk = (entry & 1) ? 0u : qmask_row[0];
+          reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(b) * p.cap + I.e0) * kB + r) + w;
+      const int32_t* list = p.q_idx + int64_t(b) * p.cap + I.e0;
+      int entry = I.first;
+      uint32_t mk = I.mk;
       for (int j = 0; j < I.n; ++j) {
         const int g = gt + j;
         const bool full = entry & 1;
         const uint32_t mcur = mk;  // this group's 32 key columns
         if (j + 1 < I.n) {
-          entry = I.list[j + 1];
+          entry = list[j + 1];
           if (!(entry & 1)) mk = qmask_row[int64_t(j + 1) * kB * 4];
         }
         const uint32_t tS = tmem + lane_base + rot3(g) + kCW * w;
@@ -987,17 +1068,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_before();
         tc::mbar_arrive(ds_ready + (g & 1));
       }
-      if (!ok || !wait_u(dq_final, nq & 1)) { ok = false; break; }
+      if (!ok || !prefetch(k + 1, nx) || !wait_u(dq_final, nq & 1)) { ok = false; break; }
       tc::tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < DW / 16; ++c) {
-        uint32_t v[16];
-        tc::tmem_ld16(tmem + lane_base + T_DQ + w * DW + c * 16, v);
+      if constexpr (DW == 32) {  // one TMEM load for the thread's 32 columns
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + lane_base + T_DQ + w * DW, v);
         tc::tmem_ld_wait();
-        store_row16<F32OUT>(dq_row + c * 16 * ESZ, v, p.scale, false, p.wide);
+        tc::tc_fence_before();
+        tc::mbar_arrive(dq_free);  // the stores below read registers only
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          store_row16<F32OUT>(dq_row + c * 16 * ESZ, reinterpret_cast<const uint32_t(&)[16]>(v[16 * c]), p.scale,
+                              false, p.wide);
+      } else {
+#pragma unroll
+        for (int c = 0; c < DW / 16; ++c) {
+          uint32_t v[16];
+          tc::tmem_ld16(tmem + lane_base + T_DQ + w * DW + c * 16, v);
+          tc::tmem_ld_wait();
+          store_row16<F32OUT>(dq_row + c * 16 * ESZ, v, p.scale, false, p.wide);
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(dq_free);
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(dq_free);
       gt += I.n;
       ++nq;
     }
