@@ -13,21 +13,23 @@
 //      into them).
 //  (2) KV kernel: work items are (key tile, kv head, tree, chunk of up to 64
 //      steps of that key tile's column), a step being one (query head, query
-//      tile) pair of the per-key-block CSR, run as two units of 64 queries.
-//      Per unit the MMA issuer runs S^T = K Q^T and dP^T = V dO^T; four compute
-//      warpgroups (thread r = key row r = TMEM lane r; warpgroup w = query
-//      columns of the unit) write P^T and dS^T back into TMEM as packed bf16,
-//      and the issuer runs dV += P^T dO and dK += dS^T Q with A read from
-//      TMEM.  Two units are in flight, one per pair of warpgroups (units of
-//      even parity to warpgroups 0-1, odd to 2-3), so one pair's TMEM round
-//      trips overlap the other pair's work and the MMAs of both.  A key only sees the query interval
-//      [j, E[j]], applied on PARTIAL tiles.
+//      tile) pair of the per-key-block CSR.  Per step the MMA issuer runs
+//      S^T = K Q^T and dP^T = V dO^T into two TMEM regions that swap roles
+//      every step; four compute warpgroups (thread r = key row r = TMEM lane
+//      r; warpgroup w = query columns [32w, 32w+32)) write P^T and dS^T back
+//      into the S^T region as packed bf16, and the issuer runs dV += P^T dO
+//      and dK += dS^T Q with A read from TMEM, issuing the next step's S^T as
+//      soon as this step's dP^T has been read.  A key only sees the query
+//      interval [j, E[j]], applied on PARTIAL tiles.
 //  (3) dQ kernel: work items are (query tile, query head, tree); it walks the
 //      query block's key tiles like the forward, rotating S, dP and packed dS
 //      through three TMEM regions so the next tile's S and dP run while this
 //      tile's dS is formed: dS = P (dP - D) with the forward's LSE and the
 //      partial-tile bit masks, dQ += dS K accumulated in TMEM; dQ is stored
-//      once.
+//      once.  With d = 128 and an even number of query heads per key/value
+//      head, the pair form of this kernel runs two heads of a group on the
+//      two SMs of a TPC with M = 256 MMAs (cta_group::2), each SM holding
+//      half of every B operand.
 // Both main kernels are persistent: one CTA per SM takes items from a counter
 // in the block-mask buffer, barrier phases run on across items, and the issuer
 // warps run converged with an elected lane issuing each copy, MMA and commit.
@@ -141,22 +143,6 @@ __device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16
     d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
     d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
-}
-
-// Item fetch shared by the producers of both kernels: one lane takes the next
-// index from the counter, the elected lane publishes it.
-// Returns -1 once the items are used up.
-__device__ __forceinline__ int fetch_item(uint32_t* counter, int n_items, volatile int* ring, uint64_t* full) {
-  uint32_t u = 0;
-  if ((threadIdx.x & 31) == 0) u = atomicAdd(counter, 1u);
-  u = __shfl_sync(0xffffffffu, u, 0);
-  const int it = u < uint32_t(n_items) ? int(u) : -1;  // unsigned: no index below 0
-  if (tc::elect_one()) {
-    *ring = it;
-    tc::mbar_arrive(full);
-  }
-  __syncwarp();
-  return it;
 }
 
 // The last CTA to finish rearms a kernel's work counter for the next call.
@@ -842,7 +828,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
       }
       const int jt = take(k + 1, J);
-      if (!(ok = jt != -2)) break;
+      ok = jt != -2;
+      if (!ok) break;
       if (jt >= 0 && J.n > 0 && tc::elect_one()) {  // the next item's Q and dO into L2 meanwhile
         const int nrow0 = J.b * p.t_pad + J.qb * kB;
         for (int c = 0; c < NCH; ++c) {
@@ -1103,6 +1090,523 @@ __global__ void __launch_bounds__(kThreads, 1)
   rearm_counter(p.sched + 4);
 }
 
+// =========================================================================== dQ kernel, head pairs
+//
+// For d = 128 and GQA groups of an even number of query heads, a cluster of
+// two CTAs (the two SMs of a TPC) takes one (query tile, head pair, tree)
+// item, CTA c computing query head 2p + c.  Both heads read the same key and
+// value head, so every MMA of the step runs once over the pair with M = 256
+// (cta_group::2): each CTA keeps its own Q and dO tiles and its own rows of
+// S, dP, dS and dQ in TMEM exactly as above, but only half of each B
+// operand -- keys [64c, 64c+64) of the K and V tiles for S and dP, and
+// head-dim columns [64c, 64c+64) of the K tile for dQ.  Per 128x128x16 MMA a
+// CTA reads 6 KB of shared memory instead of 8 KB, and per step it loads
+// 48 KB of K and V instead of 64 KB: the MMAs are no longer held back by
+// shared-memory bandwidth.  The even CTA fetches the items and issues every
+// MMA; the copies of both CTAs complete on its barriers, its MMA completions
+// are multicast to both CTAs, and each compute warp signals it once.
+//
+// TMEM (per CTA): S in [0, 128), dP in [128, 256), packed dS in two 64-column
+// buffers [256, 384), the dQ accumulator in [384, 512).  S(j+1) is issued as
+// soon as the compute warps have read S(j), at the start of step j's
+// exponentials, dP(j+1) once they have read dP(j), and dQ(j) once dS(j) is
+// packed; an MMA's completion is only seen a few hundred cycles after its
+// issue, and this order keeps the next step's S and dP ahead of the compute
+// warps, so that the tensor pipe, not that latency, sets the pace.
+
+constexpr int kNWarpsC = 4 * kNWG;  // compute warps per CTA
+
+template <int D>
+struct Dq2Cfg {
+  static_assert(D == 128, "head pairs: d = 128");
+  static constexpr uint32_t TILE = 2 * kChunk;   // Q or dO tile, 128 rows x 128 columns
+  static constexpr uint32_t PIECE = kChunk / 2;  // 64 rows x 64 columns
+  // K stage: [my 64 keys x columns 0-63 | my keys x 64-127 | keys 0-63 x my column half |
+  // keys 64-127 x my column half]; V stage: my keys x both column halves.
+  static constexpr uint32_t KST = 4 * PIECE;
+  static constexpr uint32_t VST = 2 * PIECE;
+  // K(j) is read by S(j) and dQ(j), V(j) by dP(j), which is issued later
+  // in the step than S(j): one V stage more than K stages.
+  static constexpr int NSK = 3, NSV = 4;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_DO = TILE;
+  static constexpr uint32_t OFF_K = 2 * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + NSK * KST;
+  static constexpr uint32_t OFF_BAR = OFF_V + NSV * VST;
+  // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, dp_full,
+  // s_free, dp_free, ds_ready[2], ds_free[2], dq_final, dq_free, drain, item_full[NIR], item_empty[NIR]
+  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 11 + 2 * kNIR;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t OFF_RING = OFF_MISC + 16;  // kNIR x {index, n, e0, first CSR entry}
+  static constexpr uint32_t BYTES = OFF_RING + kNIR * 16;
+  static_assert(BYTES <= kSmemMax, "shared memory budget");
+};
+
+// (tree, head pair, query block) of pair item `it`, in decode_dq's order.
+__device__ __forceinline__ void dq2_coords(const BwdParams& p, int it, int& b, int& hp, int& qb) {
+  const int per_b = (p.hq >> 1) * p.n_blk;
+  b = it / per_b;
+  const int rem = it - b * per_b;
+  hp = rem / p.n_blk;
+  qb = p.n_blk - 1 - rem % p.n_blk;
+}
+
+template <int D, bool F32OUT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_bwd_dq2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k64,
+                        const __grid_constant__ CUtensorMap tm_v64, const __grid_constant__ CUtensorMap tm_do,
+                        const BwdParams p) {
+  using C = Dq2Cfg<D>;
+  constexpr int NSK = C::NSK, NSV = C::NSV;
+  constexpr uint32_t TILE = C::TILE, PIECE = C::PIECE, KST = C::KST, VST = C::VST;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  if (tc::smem_u32(smem) & 1023u) {  // the same for every CTA of the launch: all leave
+    if (threadIdx.x == 0) atomicOr(&g_status_bwd, 2u);
+    return;
+  }
+  const uint32_t crank = tc::cta_rank();
+  const bool lead = crank == 0;
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sDO = smem + C::OFF_DO;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bar;
+  uint64_t* q_empty = bar + 1;
+  uint64_t* k_full = bar + 2;
+  uint64_t* k_empty = k_full + NSK;
+  uint64_t* v_full = k_empty + NSK;
+  uint64_t* v_empty = v_full + NSV;
+  uint64_t* s_full = v_empty + NSV;
+  uint64_t* dp_full = s_full + 1;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* dp_free = s_full + 3;
+  uint64_t* ds_ready = s_full + 4;  // [2]
+  uint64_t* ds_free = s_full + 6;   // [2]
+  uint64_t* dq_final = s_full + 8;
+  uint64_t* dq_free = s_full + 9;
+  uint64_t* drain = s_full + 10;
+  uint64_t* item_full = s_full + 11;          // [kNIR]
+  uint64_t* item_empty = s_full + 11 + kNIR;  // [kNIR]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_RING);  // [kNIR][4]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.hq / p.hkv;
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DS = 256, T_DQ = 384;
+  // item-slot consumers, all arriving on the even CTA: its MMA warp and
+  // compute warps, the odd CTA's producer and compute warps
+  constexpr int NCONS2 = 2 * (1 + kNWarpsC);
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
+    for (int s = 0; s < NSK; ++s) {
+      tc::mbar_init(k_full + s, 1);
+      tc::mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
+      tc::mbar_init(v_full + s, 1);
+      tc::mbar_init(v_empty + s, 1);
+    }
+    tc::mbar_init(s_full, 1);
+    tc::mbar_init(dp_full, 1);
+    tc::mbar_init(s_free, 2 * kNWarpsC);
+    tc::mbar_init(dp_free, 2 * kNWarpsC);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(ds_ready + s, 2 * kNWarpsC);
+      tc::mbar_init(ds_free + s, 1);
+    }
+    tc::mbar_init(dq_final, 1);
+    tc::mbar_init(dq_free, 2 * kNWarpsC);
+    tc::mbar_init(drain, 1);
+    for (int s = 0; s < kNIR; ++s) {
+      tc::mbar_init(item_full + s, 1);
+      tc::mbar_init(item_empty + s, NCONS2);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == kWMma) tc::tmem_alloc2(tmem_slot, 512);
+  tc::tc_fence_before();
+  tc::cluster_sync();  // both CTAs' barriers exist before either signals the other
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto wait_u = [&](uint64_t* b_, uint32_t par) {
+    return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_bwd));
+  };
+  auto wait_ring = [&](uint64_t* b_, uint32_t par) {  // item slots: written across the pair
+    return __all_sync(0xffffffffu, tc::mbar_wait_cluster(b_, par, abort_flag, &g_status_bwd));
+  };
+  // one arrival per warp on the even CTA's copy of `b_` (after the warp's own tcgen05 fences)
+  auto warp_arrive_lead = [&](uint64_t* b_) {
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive_remote(tc::peer_addr(b_, 0));
+    __syncwarp();
+  };
+
+  if (warp == kWTma) {
+    // ------------------------------------------------------------ producers (both CTAs)
+    if (tc::elect_one()) {
+      tc::tma_prefetch_desc(&tm_q);
+      tc::tma_prefetch_desc(&tm_k64);
+      tc::tma_prefetch_desc(&tm_v64);
+      tc::tma_prefetch_desc(&tm_do);
+    }
+    __syncwarp();
+    int gk = 0, gv = 0, nq = 0;
+    bool ok = true;
+    struct Item {
+      int it, n, e0;
+    };
+    // Even CTA: slot k gets the k-th item the pair takes, written into both
+    // CTAs' rings, one item ahead of the loads.  Odd CTA: reads slot k.
+    auto take = [&](int k, Item& I) -> bool {
+      const int slot = k % kNIR;
+      if (!wait_u(item_empty + slot, ((k / kNIR) & 1) ^ 1)) return false;
+      uint32_t u = 0;
+      if (lane == 0) u = atomicAdd(p.sched + 4, 1u);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      I.it = u < uint32_t(p.dq_items) ? int(u) : -1;  // unsigned: no index below 0
+      I.n = 0;
+      I.e0 = 0;
+      int first = 0;
+      if (I.it >= 0) {
+        int b, hp, qb;
+        dq2_coords(p, I.it, b, hp, qb);
+        const int32_t* rp = p.q_ptr + b * (p.n_blk + 1);
+        I.e0 = rp[qb];
+        I.n = rp[qb + 1] - I.e0;
+        if (I.n > 0) first = p.q_idx[int64_t(b) * p.cap + I.e0];
+      }
+      if (tc::elect_one()) {
+        volatile int* mine = item_ring + 4 * slot;
+        mine[0] = I.it;
+        mine[1] = I.n;
+        mine[2] = I.e0;
+        mine[3] = first;
+        const uint32_t peer = tc::peer_addr(const_cast<int*>(mine), 1);
+        tc::st_cluster_u32(peer, uint32_t(I.it));
+        tc::st_cluster_u32(peer + 4, uint32_t(I.n));
+        tc::st_cluster_u32(peer + 8, uint32_t(I.e0));
+        tc::st_cluster_u32(peer + 12, uint32_t(first));
+        tc::mbar_arrive(item_full + slot);
+        tc::mbar_arrive_release_cluster(tc::peer_addr(item_full + slot, 1));  // after the ring stores
+      }
+      __syncwarp();
+      return true;
+    };
+    auto read = [&](int k, Item& I) -> bool {
+      const int slot = k % kNIR;
+      if (!wait_ring(item_full + slot, (k / kNIR) & 1)) return false;
+      I.it = item_ring[4 * slot];
+      I.n = item_ring[4 * slot + 1];
+      I.e0 = item_ring[4 * slot + 2];
+      warp_arrive_lead(item_empty + slot);
+      return true;
+    };
+    const uint32_t l_qfull = tc::peer_addr(q_full, 0);
+    Item I, J;
+    ok = lead ? take(0, I) : read(0, I);
+    for (int k = 0; ok && I.it >= 0; ++k) {
+      int b, hp, qb;
+      dq2_coords(p, I.it, b, hp, qb);
+      const int h = 2 * hp + int(crank);
+      const int g = (2 * hp) / G;
+      if (I.n > 0) {
+        const int row0 = b * p.t_pad + qb * kB;
+        if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          if (lead) tc::mbar_arrive_expect_tx(q_full, 2 * 2 * TILE);  // Q and dO of both CTAs
+          for (int c = 0; c < 2; ++c) tc::tma_load_3d_pair(sQ + c * kChunk, &tm_q, l_qfull, c * 64, h, row0);
+          for (int c = 0; c < 2; ++c) tc::tma_load_3d_pair(sDO + c * kChunk, &tm_do, l_qfull, c * 64, h, row0);
+        }
+        __syncwarp();
+        ++nq;
+      }
+      if (lead) {
+        if (!(ok = take(k + 1, J))) break;
+        if (J.it >= 0 && J.n > 0 && tc::elect_one()) {  // the next item's Q and dO (both heads) into L2
+          int nb, nhp, nqb;
+          dq2_coords(p, J.it, nb, nhp, nqb);
+          const int nrow0 = nb * p.t_pad + nqb * kB;
+          for (int e = 0; e < 2; ++e)
+            for (int c = 0; c < 2; ++c) {
+              tc::tma_prefetch_3d(&tm_q, c * 64, 2 * nhp + e, nrow0);
+              tc::tma_prefetch_3d(&tm_do, c * 64, 2 * nhp + e, nrow0);
+            }
+        }
+        __syncwarp();
+      }
+      const int32_t* list = p.q_idx + int64_t(b) * p.cap + I.e0;
+      int entry = I.n > 0 ? list[0] : 0;
+      for (int j = 0; ok && j < I.n; ++j) {
+        const int krow = b * p.t_pad + (entry >> 1) * kB;
+        if (j + 1 < I.n) entry = list[j + 1];
+        const int sk = gk % NSK;
+        if (!(ok = wait_u(k_empty + sk, ((gk / NSK) & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          if (lead) tc::mbar_arrive_expect_tx(k_full + sk, 2 * KST);
+          const uint32_t lb = tc::peer_addr(k_full + sk, 0);
+          uint8_t* st = sK + sk * KST;
+          const int mine = krow + 64 * int(crank);
+          tc::tma_load_3d_pair(st, &tm_k64, lb, 0, g, mine);                       // my keys, columns 0-63
+          tc::tma_load_3d_pair(st + PIECE, &tm_k64, lb, 64, g, mine);              // my keys, columns 64-127
+          tc::tma_load_3d_pair(st + 2 * PIECE, &tm_k64, lb, 64 * int(crank), g, krow);       // keys 0-63
+          tc::tma_load_3d_pair(st + 3 * PIECE, &tm_k64, lb, 64 * int(crank), g, krow + 64);  // keys 64-127
+        }
+        __syncwarp();
+        ++gk;
+        const int sv = gv % NSV;
+        if (!(ok = wait_u(v_empty + sv, ((gv / NSV) & 1) ^ 1))) break;
+        if (tc::elect_one()) {
+          if (lead) tc::mbar_arrive_expect_tx(v_full + sv, 2 * VST);
+          const uint32_t lb = tc::peer_addr(v_full + sv, 0);
+          uint8_t* st = sV + sv * VST;
+          const int mine = krow + 64 * int(crank);
+          tc::tma_load_3d_pair(st, &tm_v64, lb, 0, g, mine);
+          tc::tma_load_3d_pair(st + PIECE, &tm_v64, lb, 64, g, mine);
+        }
+        __syncwarp();
+        ++gv;
+      }
+      if (!ok) break;
+      if (lead) {
+        I = J;
+      } else if (!(ok = read(k + 1, I))) {
+        break;
+      }
+    }
+    if (*abort_flag) {  // copies into this CTA's shared memory complete on the even CTA's barriers:
+      const long long t0 = clock64();  // give any still in flight time to land before the CTA leaves
+      while (clock64() - t0 < 400000) {
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWMma) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lead) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16(256, 128, false, false);
+      constexpr uint32_t idesc_q = tc::idesc_bf16(256, D, false, true);
+      const uint64_t dQ_ = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
+      const uint64_t dDO_ = tc::smem_desc(tc::smem_u32(sDO), 16, 1024);
+      const uint64_t dKx = tc::smem_desc(tc::smem_u32(sK), 16, 1024);               // my keys, K-major B
+      const uint64_t dKy = tc::smem_desc(tc::smem_u32(sK + 2 * PIECE), kChunk, 1024);  // my columns, MN-major B
+      const uint64_t dVx = tc::smem_desc(tc::smem_u32(sV), 16, 1024);
+      auto issue_s = [&](int gt) -> bool {  // S(gt) = Q K^T over the pair
+        const int sk = gt % NSK;
+        if (!wait_u(k_full + sk, (gt / NSK) & 1)) return false;
+        tc::tc_fence_after();
+        if (tc::elect_one()) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            tc::mma2_ss(tmem + T_S, dQ_ + kslice(k), dKx + ((sk * KST) >> 4) + kslice(k, PIECE), idesc_s, k > 0);
+          tc::mma2_commit_both(s_full);
+        }
+        __syncwarp();
+        return true;
+      };
+      auto issue_dp = [&](int gt) -> bool {  // dP(gt) = dO V^T over the pair
+        const int sv = gt % NSV;
+        if (!wait_u(v_full + sv, (gt / NSV) & 1)) return false;
+        tc::tc_fence_after();
+        if (tc::elect_one()) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            tc::mma2_ss(tmem + T_DP, dDO_ + kslice(k), dVx + ((sv * VST) >> 4) + kslice(k, PIECE), idesc_s, k > 0);
+          tc::mma2_commit_both(dp_full);
+          tc::mma2_commit_both(v_empty + sv);
+        }
+        __syncwarp();
+        return true;
+      };
+      int gt = 0, nq = 0;
+      auto commit = [&](uint64_t* b_) {
+        if (tc::elect_one()) tc::mma2_commit_both(b_);
+        __syncwarp();
+      };
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (!(ok = wait_ring(item_full + (k % kNIR), (k / kNIR) & 1))) break;
+        const int it = item_ring[4 * (k % kNIR)];
+        const int n = item_ring[4 * (k % kNIR) + 1];
+        if (tc::elect_one()) tc::mbar_arrive(item_empty + (k % kNIR));
+        __syncwarp();
+        if (it < 0) break;
+        if (n == 0) continue;
+        // the previous item's last S and dP have been read (waited below)
+        if (!(ok = wait_u(q_full, nq & 1))) break;
+        if (!(ok = issue_s(gt) && issue_dp(gt))) break;
+        if (n == 1) commit(q_empty);  // Q and dO are read by S and dP only
+        for (int j = 0; ok && j < n; ++j) {
+          const int g = gt + j, sk = g % NSK;
+          if (!(ok = wait_u(s_free, g & 1))) break;
+          if (j + 1 < n && !(ok = issue_s(g + 1))) break;
+          if (!(ok = wait_u(dp_free, g & 1))) break;
+          if (j + 1 < n) {
+            if (!(ok = issue_dp(g + 1))) break;
+            if (j + 2 == n) commit(q_empty);
+          }
+          if (!(ok = wait_u(ds_ready + (g & 1), (g >> 1) & 1))) break;
+          if (j == 0 && nq > 0 && !(ok = wait_u(dq_free, (nq - 1) & 1))) break;
+          tc::tc_fence_after();
+          if (tc::elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K over the pair, dS packed in T_DS[g&1]
+              tc::mma2_ts(tmem + T_DQ, tmem + T_DS + 64 * (g & 1) + 8 * kk,
+                          dKy + ((sk * KST) >> 4) + ((kk * 2048) >> 4), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+            tc::mma2_commit_both(ds_free + (g & 1));
+            tc::mma2_commit_both(k_empty + sk);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        commit(dq_final);
+        gt += n;
+        ++nq;
+      }
+      if (*abort_flag && tc::elect_one()) {
+        volatile int never = 0;
+        tc::mma2_commit_both(drain);
+        tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
+      }
+      __syncwarp();
+    }
+  } else if (warp < kNWarpsC) {
+    // ------------------------------------------------------------ compute warpgroups (both CTAs)
+    const int w = warp >> 2;          // key columns [32w, 32w+32) of each tile
+    const int r = threadIdx.x & 127;  // query row = TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    constexpr int ESZ = F32OUT ? 4 : 2;
+    constexpr int DW = D / kNWG;
+    int gt = 0, nq = 0;
+    bool ok = true;
+    struct Next {
+      int it, n, e0, first;
+      float lse, drow;
+      uint32_t mk;
+    };
+    auto prefetch = [&](int k, Next& x) -> bool {
+      const int slot = k % kNIR;
+      if (!wait_ring(item_full + slot, (k / kNIR) & 1)) return false;
+      x.it = item_ring[4 * slot];
+      x.n = item_ring[4 * slot + 1];
+      x.e0 = item_ring[4 * slot + 2];
+      x.first = item_ring[4 * slot + 3];
+      warp_arrive_lead(item_empty + slot);
+      x.lse = 0.f;
+      x.drow = 0.f;
+      x.mk = 0u;
+      if (x.it >= 0 && x.n > 0) {
+        int b, hp, qb;
+        dq2_coords(p, x.it, b, hp, qb);
+        const int64_t vec = (int64_t(b) * p.hq + 2 * hp + int(crank)) * p.t_pad + qb * kB + r;
+        x.lse = p.lse[vec];
+        x.drow = p.dvec[vec];
+        if (!(x.first & 1))
+          x.mk = reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(b) * p.cap + x.e0) * kB + r)[w];
+      }
+      return true;
+    };
+    Next nx;
+    ok = prefetch(0, nx);
+    for (int k = 0; ok; ++k) {
+      const Next I = nx;
+      if (I.it < 0) break;
+      int b, hp, qb;
+      dq2_coords(p, I.it, b, hp, qb);
+      const int h = 2 * hp + int(crank);
+      const int row0 = b * p.t_pad + qb * kB;
+      uint8_t* dq_row = static_cast<uint8_t*>(p.dq) + ((int64_t(row0 + r) * p.hq + h) * D + w * DW) * ESZ;
+      if (I.n == 0) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < DW * ESZ / 16; ++c) reinterpret_cast<uint4*>(dq_row)[c] = z;
+        ok = prefetch(k + 1, nx);
+        continue;
+      }
+      const float nlse2 = -I.lse * kLog2e;
+      const float drow = I.drow;
+      const uint32_t* qmask_row =
+          reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(b) * p.cap + I.e0) * kB + r) + w;
+      const int32_t* list = p.q_idx + int64_t(b) * p.cap + I.e0;
+      int entry = I.first;
+      uint32_t mk = I.mk;
+      for (int j = 0; j < I.n; ++j) {
+        const int g = gt + j;
+        const bool full = entry & 1;
+        const uint32_t mcur = mk;
+        if (j + 1 < I.n) {
+          entry = list[j + 1];
+          if (!(entry & 1)) mk = qmask_row[int64_t(j + 1) * kB * 4];
+        }
+        if (!wait_u(s_full, g & 1)) { ok = false; break; }
+        tc::tc_fence_after();
+        float pf[kCW];
+        {
+          uint32_t sv[kCW];
+          tc::tmem_ld32(tmem + lane_base + T_S + kCW * w, sv);
+          tc::tmem_ld_wait();
+          tc::tc_fence_before();
+          warp_arrive_lead(s_free);  // S of the next tile may be issued now
+#pragma unroll
+          for (int c = 0; c < kCW; ++c) pf[c] = tc::ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, nlse2));
+          if (!full) {
+#pragma unroll
+            for (int c = 0; c < kCW; ++c)
+              if (!((mcur >> c) & 1u)) pf[c] = 0.f;
+          }
+        }
+        if (!wait_u(dp_full, g & 1)) { ok = false; break; }
+        tc::tc_fence_after();
+        {
+          uint32_t dpv[kCW];
+          tc::tmem_ld32(tmem + lane_base + T_DP + kCW * w, dpv);
+          tc::tmem_ld_wait();
+          tc::tc_fence_before();
+          warp_arrive_lead(dp_free);
+          uint32_t dw[kCW / 2];
+#pragma unroll
+          for (int e = 0; e < kCW / 2; ++e)
+            dw[e] = tc::pack_bf16(pf[2 * e] * (__uint_as_float(dpv[2 * e]) - drow),
+                                  pf[2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - drow));
+          // dS(g) goes where dS(g-2) was: wait until dQ(g-2) has read it
+          if (g >= 2 && !wait_u(ds_free + (g & 1), ((g >> 1) - 1) & 1)) { ok = false; break; }
+          tc::tc_fence_after();
+          tc::tmem_st16(tmem + lane_base + T_DS + 64 * (g & 1) + 16 * w, dw);
+          tc::tmem_st_wait();
+        }
+        tc::tc_fence_before();
+        warp_arrive_lead(ds_ready + (g & 1));
+      }
+      if (!ok || !prefetch(k + 1, nx) || !wait_u(dq_final, nq & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + lane_base + T_DQ + w * DW, v);
+        tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        warp_arrive_lead(dq_free);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          store_row16<F32OUT>(dq_row + c * 16 * ESZ, reinterpret_cast<const uint32_t(&)[16]>(v[16 * c]), p.scale,
+                              false, p.wide);
+      }
+      gt += I.n;
+      ++nq;
+    }
+  }
+
+  tc::tc_fence_before();
+  tc::cluster_sync();  // the pair's MMAs into either CTA's TMEM are done before it is freed
+  tc::tc_fence_after();
+  if (warp == kWMma) tc::tmem_dealloc2(tmem, 512);
+  rearm_counter(p.sched + 4);
+}
+
 // D[b, h, i] = sum_d dO * O (fp32) for real rows, 0 for pad rows.  The
 // [B*T*Hq, D] bf16 rows of O and dO are read with 16-byte loads, four per
 // lane in flight: a warp covers 128 * 32 / D rows per pass, D / 8 lanes per
@@ -1186,12 +1690,6 @@ int num_sms() {
   return sms;
 }
 
-int grid_for(int64_t work, int per_block) {
-  const int64_t want = (work + per_block - 1) / per_block;
-  const int64_t cap = int64_t(num_sms()) * 8;
-  return int(want < 1 ? 1 : (want > cap ? cap : want));
-}
-
 template <int D, bool F32OUT>
 int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const void* q, const void* k,
                const void* v, const void* o, const float* lse, const void* dout, void* dq, void* dk,
@@ -1246,6 +1744,20 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   attn_bwd_kv_kernel<D, F32OUT><<<prm.kv_items < sms ? prm.kv_items : sms, kThreads, KvCfg<D>::BYTES, st>>>(
       tq, tk, tv, tdo, prm);
   TPA_CUDA_TRY(cudaGetLastError());
+  if constexpr (D == 128) {
+    if (G % 2 == 0 && sms >= 2) {  // head pairs of one key/value head on the two SMs of a TPC
+      CUtensorMap tk64, tv64;
+      if (!tmap::make_rows_heads_d(&tk64, k, rows, hkv, D, 64) || !tmap::make_rows_heads_d(&tv64, v, rows, hkv, D, 64))
+        return TPA_ERR_CUDA;
+      prm.dq_items = tree->n_trees * (hq / 2) * mask->n_blk;
+      const int pairs = prm.dq_items < sms / 2 ? prm.dq_items : sms / 2;
+      TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq2_kernel<D, F32OUT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Dq2Cfg<D>::BYTES));
+      attn_bwd_dq2_kernel<D, F32OUT><<<2 * pairs, kThreads, Dq2Cfg<D>::BYTES, st>>>(tq, tk64, tv64, tdo, prm);
+      TPA_CUDA_TRY(cudaGetLastError());
+      return TPA_OK;
+    }
+  }
   TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     DqCfg<D>::BYTES));
   attn_bwd_dq_kernel<D, F32OUT><<<prm.dq_items < sms ? prm.dq_items : sms, kThreads, DqCfg<D>::BYTES, st>>>(
