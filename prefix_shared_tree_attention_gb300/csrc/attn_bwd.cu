@@ -1112,9 +1112,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // exponentials, dP(j+1) once they have read dP(j), and dQ(j) once dS(j) is
 // packed; an MMA's completion is only seen a few hundred cycles after its
 // issue, and this order keeps the next step's S and dP ahead of the compute
-// warps, so that the tensor pipe, not that latency, sets the pace.
+// warps, so that the tensor pipe, not that latency, sets the pace.  S and dP
+// are issued by one warp, dQ by another.
 
 constexpr int kNWarpsC = 4 * kNWG;  // compute warps per CTA
+// One MMA takes 64 cycles of the pair's tensor pipes but about as long to
+// issue from one thread, so two warps issue: one S and dP, one dQ (they
+// touch disjoint TMEM and are ordered through the compute warps' signals).
+constexpr int kWMmaQ = kWMma + 1;
+constexpr int kThreads2 = kThreads + 32;
 
 template <int D>
 struct Dq2Cfg {
@@ -1125,17 +1131,18 @@ struct Dq2Cfg {
   // keys 64-127 x my column half]; V stage: my keys x both column halves.
   static constexpr uint32_t KST = 4 * PIECE;
   static constexpr uint32_t VST = 2 * PIECE;
-  // K(j) is read by S(j) and dQ(j), V(j) by dP(j), which is issued later
-  // in the step than S(j): one V stage more than K stages.
-  static constexpr int NSK = 3, NSV = 4;
+  // Two Q buffers: the next item's Q lands while this item runs, so its
+  // first S is issued as soon as this item's last S has been read.
+  static constexpr int NSQ = 2, NSK = 3, NSV = 2;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_DO = TILE;
-  static constexpr uint32_t OFF_K = 2 * TILE;
+  static constexpr uint32_t OFF_DO = NSQ * TILE;
+  static constexpr uint32_t OFF_K = OFF_DO + TILE;
   static constexpr uint32_t OFF_V = OFF_K + NSK * KST;
   static constexpr uint32_t OFF_BAR = OFF_V + NSV * VST;
-  // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full, dp_full,
-  // s_free, dp_free, ds_ready[2], ds_free[2], dq_final, dq_free, drain, item_full[NIR], item_empty[NIR]
-  static constexpr int NBAR = 2 + 2 * NSK + 2 * NSV + 11 + 2 * kNIR;
+  // q_full[NSQ], q_empty[NSQ], do_full, do_empty, k_full[NSK], k_empty[NSK], v_full[NSV],
+  // v_empty[NSV], s_full, dp_full, s_free, dp_free, ds_ready[2], ds_free[2], dq_final, dq_free,
+  // drain[2], item_full[NIR], item_empty[NIR]
+  static constexpr int NBAR = 2 * NSQ + 2 + 2 * NSK + 2 * NSV + 12 + 2 * kNIR;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t OFF_RING = OFF_MISC + 16;  // kNIR x {index, n, e0, first CSR entry}
   static constexpr uint32_t BYTES = OFF_RING + kNIR * 16;
@@ -1152,12 +1159,12 @@ __device__ __forceinline__ void dq2_coords(const BwdParams& p, int it, int& b, i
 }
 
 template <int D, bool F32OUT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
     attn_bwd_dq2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k64,
                         const __grid_constant__ CUtensorMap tm_v64, const __grid_constant__ CUtensorMap tm_do,
                         const BwdParams p) {
   using C = Dq2Cfg<D>;
-  constexpr int NSK = C::NSK, NSV = C::NSV;
+  constexpr int NSQ = C::NSQ, NSK = C::NSK, NSV = C::NSV;
   constexpr uint32_t TILE = C::TILE, PIECE = C::PIECE, KST = C::KST, VST = C::VST;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -1172,9 +1179,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bar;
-  uint64_t* q_empty = bar + 1;
-  uint64_t* k_full = bar + 2;
+  uint64_t* q_full = bar;              // [NSQ]
+  uint64_t* q_empty = bar + NSQ;       // [NSQ]
+  uint64_t* do_full = bar + 2 * NSQ;
+  uint64_t* do_empty = do_full + 1;
+  uint64_t* k_full = do_full + 2;
   uint64_t* k_empty = k_full + NSK;
   uint64_t* v_full = k_empty + NSK;
   uint64_t* v_empty = v_full + NSV;
@@ -1186,9 +1195,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* ds_free = s_full + 6;   // [2]
   uint64_t* dq_final = s_full + 8;
   uint64_t* dq_free = s_full + 9;
-  uint64_t* drain = s_full + 10;
-  uint64_t* item_full = s_full + 11;          // [kNIR]
-  uint64_t* item_empty = s_full + 11 + kNIR;  // [kNIR]
+  uint64_t* drain = s_full + 10;              // [2]: one per issuing warp
+  uint64_t* item_full = s_full + 12;          // [kNIR]
+  uint64_t* item_empty = s_full + 12 + kNIR;  // [kNIR]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_RING);  // [kNIR][4]
@@ -1197,13 +1206,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = p.hq / p.hkv;
   constexpr uint32_t T_S = 0, T_DP = 128, T_DS = 256, T_DQ = 384;
-  // item-slot consumers, all arriving on the even CTA: its MMA warp and
+  // item-slot consumers, all arriving on the even CTA: its two MMA warps and
   // compute warps, the odd CTA's producer and compute warps
-  constexpr int NCONS2 = 2 * (1 + kNWarpsC);
+  constexpr int NCONS2 = 2 * (1 + kNWarpsC) + 1;
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(q_full, 1);
-    tc::mbar_init(q_empty, 1);
+    for (int s = 0; s < NSQ; ++s) {
+      tc::mbar_init(q_full + s, 1);
+      tc::mbar_init(q_empty + s, 1);
+    }
+    tc::mbar_init(do_full, 1);
+    tc::mbar_init(do_empty, 1);
     for (int s = 0; s < NSK; ++s) {
       tc::mbar_init(k_full + s, 1);
       tc::mbar_init(k_empty + s, 1);
@@ -1223,6 +1236,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc::mbar_init(dq_final, 1);
     tc::mbar_init(dq_free, 2 * kNWarpsC);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(drain + 1, 1);
     for (int s = 0; s < kNIR; ++s) {
       tc::mbar_init(item_full + s, 1);
       tc::mbar_init(item_empty + s, NCONS2);
@@ -1308,39 +1322,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       warp_arrive_lead(item_empty + slot);
       return true;
     };
-    const uint32_t l_qfull = tc::peer_addr(q_full, 0);
+    // Q of an item goes into buffer (count of loaded Q tiles) % NSQ; it is
+    // requested as soon as the item is known, one item ahead of its K/V.
+    int nd = 0;  // dO tiles loaded
+    auto load_q = [&](const Item& X) -> bool {
+      int xb, xhp, xqb;
+      dq2_coords(p, X.it, xb, xhp, xqb);
+      const int qs = nq % NSQ;
+      if (!wait_u(q_empty + qs, ((nq / NSQ) & 1) ^ 1)) return false;
+      if (tc::elect_one()) {
+        if (lead) tc::mbar_arrive_expect_tx(q_full + qs, 2 * TILE);  // Q of both CTAs
+        const uint32_t lb = tc::peer_addr(q_full + qs, 0);
+        for (int c = 0; c < 2; ++c)
+          tc::tma_load_3d_pair(sQ + qs * TILE + c * kChunk, &tm_q, lb, c * 64, 2 * xhp + int(crank),
+                               xb * p.t_pad + xqb * kB);
+      }
+      __syncwarp();
+      ++nq;
+      return true;
+    };
     Item I, J;
     ok = lead ? take(0, I) : read(0, I);
+    if (ok && I.it >= 0 && I.n > 0) ok = load_q(I);
     for (int k = 0; ok && I.it >= 0; ++k) {
       int b, hp, qb;
       dq2_coords(p, I.it, b, hp, qb);
       const int h = 2 * hp + int(crank);
       const int g = (2 * hp) / G;
-      if (I.n > 0) {
-        const int row0 = b * p.t_pad + qb * kB;
-        if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
-        if (tc::elect_one()) {
-          if (lead) tc::mbar_arrive_expect_tx(q_full, 2 * 2 * TILE);  // Q and dO of both CTAs
-          for (int c = 0; c < 2; ++c) tc::tma_load_3d_pair(sQ + c * kChunk, &tm_q, l_qfull, c * 64, h, row0);
-          for (int c = 0; c < 2; ++c) tc::tma_load_3d_pair(sDO + c * kChunk, &tm_do, l_qfull, c * 64, h, row0);
+      // dO(k) and the next item's Q after this item's first K and V tiles:
+      // dO waits for the previous item's last dP, and the first S and dP of
+      // this item should not wait behind that.
+      auto load_do_and_next = [&]() -> bool {
+        if (I.n > 0) {
+          if (!wait_u(do_empty, (nd & 1) ^ 1)) return false;
+          if (tc::elect_one()) {
+            if (lead) tc::mbar_arrive_expect_tx(do_full, 2 * TILE);  // dO of both CTAs
+            const uint32_t lb = tc::peer_addr(do_full, 0);
+            for (int c = 0; c < 2; ++c)
+              tc::tma_load_3d_pair(sDO + c * kChunk, &tm_do, lb, c * 64, h, b * p.t_pad + qb * kB);
+          }
+          __syncwarp();
+          ++nd;
         }
-        __syncwarp();
-        ++nq;
-      }
-      if (lead) {
-        if (!(ok = take(k + 1, J))) break;
-        if (J.it >= 0 && J.n > 0 && tc::elect_one()) {  // the next item's Q and dO (both heads) into L2
-          int nb, nhp, nqb;
-          dq2_coords(p, J.it, nb, nhp, nqb);
-          const int nrow0 = nb * p.t_pad + nqb * kB;
-          for (int e = 0; e < 2; ++e)
-            for (int c = 0; c < 2; ++c) {
-              tc::tma_prefetch_3d(&tm_q, c * 64, 2 * nhp + e, nrow0);
-              tc::tma_prefetch_3d(&tm_do, c * 64, 2 * nhp + e, nrow0);
-            }
+        if (!(lead ? take(k + 1, J) : read(k + 1, J))) return false;
+        if (J.it >= 0 && J.n > 0) {
+          if (!load_q(J)) return false;
+          if (tc::elect_one()) {  // and its dO into L2 for when the buffer frees
+            int nb, nhp, nqb;
+            dq2_coords(p, J.it, nb, nhp, nqb);
+            for (int c = 0; c < 2; ++c)
+              tc::tma_prefetch_3d(&tm_do, c * 64, 2 * nhp + int(crank), nb * p.t_pad + nqb * kB);
+          }
+          __syncwarp();
         }
-        __syncwarp();
-      }
+        return true;
+      };
+      if (I.n == 0 && !(ok = load_do_and_next())) break;
       const int32_t* list = p.q_idx + int64_t(b) * p.cap + I.e0;
       int entry = I.n > 0 ? list[0] : 0;
       for (int j = 0; ok && j < I.n; ++j) {
@@ -1372,13 +1409,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         ++gv;
+        if (j == 0 && !(ok = load_do_and_next())) break;
       }
       if (!ok) break;
-      if (lead) {
-        I = J;
-      } else if (!(ok = read(k + 1, I))) {
-        break;
-      }
+      I = J;
     }
     if (*abort_flag) {  // copies into this CTA's shared memory complete on the even CTA's barriers:
       const long long t0 = clock64();  // give any still in flight time to land before the CTA leaves
@@ -1387,23 +1421,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kWMma) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
+    // ------------------------------------------------------------ S and dP issuer (even CTA)
     if (lead) {
       constexpr uint32_t idesc_s = tc::idesc_bf16(256, 128, false, false);
-      constexpr uint32_t idesc_q = tc::idesc_bf16(256, D, false, true);
       const uint64_t dQ_ = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
       const uint64_t dDO_ = tc::smem_desc(tc::smem_u32(sDO), 16, 1024);
       const uint64_t dKx = tc::smem_desc(tc::smem_u32(sK), 16, 1024);               // my keys, K-major B
-      const uint64_t dKy = tc::smem_desc(tc::smem_u32(sK + 2 * PIECE), kChunk, 1024);  // my columns, MN-major B
       const uint64_t dVx = tc::smem_desc(tc::smem_u32(sV), 16, 1024);
-      auto issue_s = [&](int gt) -> bool {  // S(gt) = Q K^T over the pair
+      auto issue_s = [&](int gt, int qs) -> bool {  // S(gt) = Q K^T over the pair, Q in buffer qs
         const int sk = gt % NSK;
         if (!wait_u(k_full + sk, (gt / NSK) & 1)) return false;
         tc::tc_fence_after();
         if (tc::elect_one()) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            tc::mma2_ss(tmem + T_S, dQ_ + kslice(k), dKx + ((sk * KST) >> 4) + kslice(k, PIECE), idesc_s, k > 0);
+            tc::mma2_ss(tmem + T_S, dQ_ + ((qs * TILE) >> 4) + kslice(k), dKx + ((sk * KST) >> 4) + kslice(k, PIECE),
+                        idesc_s, k > 0);
           tc::mma2_commit_both(s_full);
         }
         __syncwarp();
@@ -1438,18 +1471,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (it < 0) break;
         if (n == 0) continue;
         // the previous item's last S and dP have been read (waited below)
-        if (!(ok = wait_u(q_full, nq & 1))) break;
-        if (!(ok = issue_s(gt) && issue_dp(gt))) break;
-        if (n == 1) commit(q_empty);  // Q and dO are read by S and dP only
+        const int qs = nq % NSQ;
+        if (!(ok = wait_u(q_full + qs, (nq / NSQ) & 1))) break;
+        if (!(ok = issue_s(gt, qs))) break;
+        if (n == 1) commit(q_empty + qs);  // Q is read by S only, dO by dP only
+        if (!(ok = wait_u(do_full, nq & 1) && issue_dp(gt))) break;
+        if (n == 1) commit(do_empty);
         for (int j = 0; ok && j < n; ++j) {
-          const int g = gt + j, sk = g % NSK;
+          const int g = gt + j;
           if (!(ok = wait_u(s_free, g & 1))) break;
-          if (j + 1 < n && !(ok = issue_s(g + 1))) break;
+          if (j + 1 < n) {
+            if (!(ok = issue_s(g + 1, qs))) break;
+            if (j + 2 == n) commit(q_empty + qs);
+          }
           if (!(ok = wait_u(dp_free, g & 1))) break;
           if (j + 1 < n) {
             if (!(ok = issue_dp(g + 1))) break;
-            if (j + 2 == n) commit(q_empty);
+            if (j + 2 == n) commit(do_empty);
           }
+        }
+        if (!ok) break;
+        gt += n;
+        ++nq;
+      }
+      if (*abort_flag && tc::elect_one()) {
+        volatile int never = 0;
+        tc::mma2_commit_both(drain);
+        tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
+      }
+      __syncwarp();
+    }
+  } else if (warp == kWMmaQ) {
+    // ------------------------------------------------------------ dQ issuer (even CTA)
+    if (lead) {
+      constexpr uint32_t idesc_q = tc::idesc_bf16(256, D, false, true);
+      const uint64_t dKy = tc::smem_desc(tc::smem_u32(sK + 2 * PIECE), kChunk, 1024);  // my columns, MN-major B
+      int gt = 0, nq = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (!(ok = wait_ring(item_full + (k % kNIR), (k / kNIR) & 1))) break;
+        const int it = item_ring[4 * (k % kNIR)];
+        const int n = item_ring[4 * (k % kNIR) + 1];
+        if (tc::elect_one()) tc::mbar_arrive(item_empty + (k % kNIR));
+        __syncwarp();
+        if (it < 0) break;
+        if (n == 0) continue;
+        for (int j = 0; ok && j < n; ++j) {
+          const int g = gt + j, sk = g % NSK;
           if (!(ok = wait_u(ds_ready + (g & 1), (g >> 1) & 1))) break;
           if (j == 0 && nq > 0 && !(ok = wait_u(dq_free, (nq - 1) & 1))) break;
           tc::tc_fence_after();
@@ -1459,19 +1527,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tc::mma2_ts(tmem + T_DQ, tmem + T_DS + 64 * (g & 1) + 8 * kk,
                           dKy + ((sk * KST) >> 4) + ((kk * 2048) >> 4), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
             tc::mma2_commit_both(ds_free + (g & 1));
-            tc::mma2_commit_both(k_empty + sk);
+            tc::mma2_commit_both(k_empty + sk);  // S(g) was read before dS(g) existed
           }
           __syncwarp();
         }
         if (!ok) break;
-        commit(dq_final);
+        if (tc::elect_one()) tc::mma2_commit_both(dq_final);
+        __syncwarp();
         gt += n;
         ++nq;
       }
       if (*abort_flag && tc::elect_one()) {
         volatile int never = 0;
-        tc::mma2_commit_both(drain);
-        tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
+        tc::mma2_commit_both(drain + 1);
+        tc::mbar_wait(drain + 1, 0, &never, &g_status_bwd, 100000000ull);
       }
       __syncwarp();
     }
@@ -1753,7 +1822,7 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
       const int pairs = prm.dq_items < sms / 2 ? prm.dq_items : sms / 2;
       TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq2_kernel<D, F32OUT>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Dq2Cfg<D>::BYTES));
-      attn_bwd_dq2_kernel<D, F32OUT><<<2 * pairs, kThreads, Dq2Cfg<D>::BYTES, st>>>(tq, tk64, tv64, tdo, prm);
+      attn_bwd_dq2_kernel<D, F32OUT><<<2 * pairs, kThreads2, Dq2Cfg<D>::BYTES, st>>>(tq, tk64, tv64, tdo, prm);
       TPA_CUDA_TRY(cudaGetLastError());
       return TPA_OK;
     }
