@@ -62,7 +62,7 @@ def _peaks():
 PROFILES = {
     "tpa_tree_attn_fwd": ["attn_fwd_grpo_3trees_ncu_full.md"],
     "tpa_tree_attn_bwd": ["bwd_pre_grpo_3trees_ncu_full.md", "attn_bwd_kv_grpo_3trees_ncu_full.md",
-                          "attn_bwd_dq_grpo_3trees_ncu_full.md"],
+                          "attn_bwd_dq2_grpo_3trees_ncu_full.md"],
 }
 
 
