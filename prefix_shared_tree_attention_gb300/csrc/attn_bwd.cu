@@ -1580,6 +1580,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
       }
       return true;
     };
+    // An item's dQ is read out during the next item's first tile, after its
+    // exponentials: the 64 KB of stores then drain while that tile's dP is
+    // still loading instead of holding up its S (loads and barrier waits
+    // issued behind a burst of stores wait for it).
+    uint8_t* pend_row = nullptr;
+    int pend_nq = 0;
+    auto readout = [&]() -> bool {
+      if (!wait_u(dq_final, pend_nq & 1)) return false;
+      tc::tc_fence_after();
+      uint32_t v[32];
+      tc::tmem_ld32(tmem + lane_base + T_DQ + w * DW, v);
+      tc::tmem_ld_wait();
+      tc::tc_fence_before();
+      warp_arrive_lead(dq_free);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        store_row16<F32OUT>(pend_row + c * 16 * ESZ, reinterpret_cast<const uint32_t(&)[16]>(v[16 * c]), p.scale,
+                            false, p.wide);
+      pend_row = nullptr;
+      return true;
+    };
     Next nx;
     ok = prefetch(0, nx);
     for (int k = 0; ok; ++k) {
@@ -1629,6 +1650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
               if (!((mcur >> c) & 1u)) pf[c] = 0.f;
           }
         }
+        if (j == 0 && pend_row != nullptr && !readout()) { ok = false; break; }
         if (!wait_u(dp_full, g & 1)) { ok = false; break; }
         tc::tc_fence_after();
         {
@@ -1651,22 +1673,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         tc::tc_fence_before();
         warp_arrive_lead(ds_ready + (g & 1));
       }
-      if (!ok || !prefetch(k + 1, nx) || !wait_u(dq_final, nq & 1)) { ok = false; break; }
-      tc::tc_fence_after();
-      {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + lane_base + T_DQ + w * DW, v);
-        tc::tmem_ld_wait();
-        tc::tc_fence_before();
-        warp_arrive_lead(dq_free);
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          store_row16<F32OUT>(dq_row + c * 16 * ESZ, reinterpret_cast<const uint32_t(&)[16]>(v[16 * c]), p.scale,
-                              false, p.wide);
-      }
+      if (!ok || !prefetch(k + 1, nx)) { ok = false; break; }
+      pend_row = dq_row;
+      pend_nq = nq;
       gt += I.n;
       ++nq;
     }
+    if (ok && pend_row != nullptr) readout();  // the CTA's last item
   }
 
   tc::tc_fence_before();
