@@ -117,6 +117,7 @@ CASES = [
     (3, 10, 180, 2, 256, 2, 2, 128),
     (4, 3, 128, 50, 256, 2, 1, 64),     # exact block multiple, little sharing
     (5, 14, 120, 3, 512, 8, 2, 128),    # several trees
+    (6, 6, 120, 3, 384, 8, 1, 128),     # group of 8 query heads per kv head, odd block count
 ]
 
 
@@ -169,6 +170,27 @@ def test_attention_bf16_gradients(tpa):
         assert_attn_close_bf16_out(dv[b], dV, f"bf16 dV tree {b}")
     # the bf16 outputs are the fp32 ones rounded (same accumulation)
     assert torch.equal(dk, f32[1].to(torch.bfloat16)) and torch.equal(dv, f32[2].to(torch.bfloat16))
+
+
+def test_attention_bf16_gradients_d128(tpa):
+    # d 128 with an even group size: the CTA-pair dQ kernel's bf16 outputs
+    rng = np.random.default_rng(502)
+    seqs = random_small_sequences(rng, 9, 280, 4, min_len=1)
+    T = 512
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    (q, k, v, do), (qc, kc, vc, doc) = random_inputs(tree.n_trees, T, 8, 2, 128, 2)
+    o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, grad_dtype=torch.bfloat16)
+    f32 = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do)
+    tpa.sync_status()
+    for b, t in enumerate(pk.trees):
+        dQ, dK, dV = oracle.attn_backward(t, qc[b], kc[b], vc[b], doc[b], t_pad=T)
+        assert_attn_close_bf16_out(dq[b], dQ, f"bf16 dQ tree {b}")
+        assert_attn_close_bf16_out(dk[b], dK, f"bf16 dK tree {b}")
+        assert_attn_close_bf16_out(dv[b], dV, f"bf16 dV tree {b}")
+    # the bf16 outputs are the fp32 ones rounded (same accumulation)
+    assert all(torch.equal(x, y.to(torch.bfloat16)) for x, y in zip((dq, dk, dv), f32))
 
 
 def test_attention_single_chain_minimal(tpa):
