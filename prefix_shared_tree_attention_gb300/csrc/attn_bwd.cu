@@ -315,6 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The dQ kernel after this one neither reads nor writes what this one
+  // writes: it may take the SMs this kernel's CTAs leave.  It reads D, so
+  // it is let go only once the preprocess before this kernel has completed.
+  if (threadIdx.x == 0) {
+    tc::grid_wait_prior();
+    tc::grid_launch_dependents();
+  }
   auto wait_u = [&](uint64_t* b_, uint32_t par) {
     return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_bwd));
   };
@@ -328,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tm_do);
     }
     __syncwarp();
+    tc::grid_wait_prior();  // D, loaded with each dO stage, comes from the preprocess
     int qs = 0, nk = 0, nq_half = 0;  // steps loaded, K/V loads, and a lone Q load in flight
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -529,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (I.n <= 0) {
         // a key tile no query sees: zero rows (the preprocess zeroed fp32 outputs)
         if (!F32OUT && I.s0 == 0) {
+          tc::grid_wait_prior();
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int c = 0; c < DW * ESZ / 16; ++c) {
@@ -608,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(ds_ready);
       }
       if (!ok || !wait_u(acc_full, nk & 1)) { ok = false; break; }
+      if (nk == 0) tc::grid_wait_prior();  // rows the preprocess zeroed are added into
       // ---- dK, dV rows of this key tile (warpgroup w: head-dim columns [w d/4, (w+1) d/4))
       tc::tc_fence_after();
       const bool add = F32OUT && (G * I.n_col > p.kv_chunk);  // several chunks add into one row
@@ -1687,6 +1697,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
   tc::tc_fence_after();
   if (warp == kWMma) tc::tmem_dealloc2(tmem, 512);
   rearm_counter(p.sched + 4);
+  // launched behind the KV kernel with programmatic serialization: do not
+  // complete before it, so that work after this launch sees both finished
+  tc::grid_wait_prior();
 }
 
 // D[b, h, i] = sum_d dO * O (fp32) for real rows, 0 for pad rows.  The
@@ -1706,6 +1719,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                      const int32_t* __restrict__ k_ptr, int32_t n_trees,
                                                      int32_t n_blk, int32_t hkv, int32_t group,
                                                      int32_t kv_chunk) {
+  tc::grid_launch_dependents();     // the KV kernel waits for this one where it reads D or the zeroed rows
   constexpr int LPR = D / 8;        // lanes per row (16 bytes each)
   constexpr int RPL = 32 / LPR;     // rows per warp load
   constexpr int RPW = 4 * RPL;      // rows per warp pass
@@ -1823,9 +1837,19 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   const int sms = num_sms();
   TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_kv_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     KvCfg<D>::BYTES));
-  attn_bwd_kv_kernel<D, F32OUT><<<prm.kv_items < sms ? prm.kv_items : sms, kThreads, KvCfg<D>::BYTES, st>>>(
-      tq, tk, tv, tdo, prm);
-  TPA_CUDA_TRY(cudaGetLastError());
+  {  // may start while the preprocess finishes (it waits where it needs its results)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(prm.kv_items < sms ? prm.kv_items : sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = KvCfg<D>::BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    TPA_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_bwd_kv_kernel<D, F32OUT>, tq, tk, tv, tdo, prm));
+  }
   if constexpr (D == 128) {
     if (G % 2 == 0 && sms >= 2) {  // head pairs of one key/value head on the two SMs of a TPC
       CUtensorMap tk64, tv64;
@@ -1835,8 +1859,18 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
       const int pairs = prm.dq_items < sms / 2 ? prm.dq_items : sms / 2;
       TPA_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq2_kernel<D, F32OUT>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Dq2Cfg<D>::BYTES));
-      attn_bwd_dq2_kernel<D, F32OUT><<<2 * pairs, kThreads2, Dq2Cfg<D>::BYTES, st>>>(tq, tk64, tv64, tdo, prm);
-      TPA_CUDA_TRY(cudaGetLastError());
+      // starts on the SMs the KV kernel's last CTAs free (the two are independent)
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * pairs);
+      cfg.blockDim = dim3(kThreads2);
+      cfg.dynamicSmemBytes = Dq2Cfg<D>::BYTES;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      TPA_CUDA_TRY(cudaLaunchKernelEx(&cfg, attn_bwd_dq2_kernel<D, F32OUT>, tq, tk64, tv64, tdo, prm));
       return TPA_OK;
     }
   }

@@ -269,6 +269,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// ---------------------------------------------------------------- dependent launches
+//
+// A kernel launched with programmatic stream serialization may start once
+// every CTA of the kernel before it has run launch_dependents (or exited);
+// grid_wait_prior blocks until that earlier kernel has completed and its
+// memory writes are visible.
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- CTA pairs
 //
 // A cluster of two CTAs on the two SMs of a TPC runs one M=256 MMA over
