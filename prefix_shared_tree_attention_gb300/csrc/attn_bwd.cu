@@ -415,7 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // Per step t: dV(t) once P^T(t) is packed, S^T(t+1) into B_t once dP^T(t)
     // has been read, dK(t) once dS^T(t) is packed, then dP^T(t+1) into A_t
-    // (in order behind dV(t) and dK(t), which read it).
+    // (in order behind dV(t) and dK(t), which read it).  One thread runs
+    // the whole loop: a warp-level sync after tcgen05.mma holds the warp until
+    // the thread's queued MMAs have gone into the pipe, so waits of a warp in
+    // step would leave the tensor pipe idle between groups.
     constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_kv = tc::idesc_bf16(128, D, false, true);
     const uint64_t dK_ = tc::smem_desc(tc::smem_u32(sK), 16, 1024);
@@ -424,48 +427,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dDOk = tc::smem_desc(tc::smem_u32(sDO), 16, 1024);      // dO as K-major B
     const uint64_t dQm = tc::smem_desc(tc::smem_u32(sQ), kChunk, 1024);    // Q as MN-major B
     const uint64_t dDOm = tc::smem_desc(tc::smem_u32(sDO), kChunk, 1024);  // dO as MN-major B
+    auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
     auto issue_s = [&](int gs) -> bool {  // S^T(gs) = K Q^T into A_gs
-      if (!wait_u(q_full + gs % NSQ, (gs / NSQ) & 1)) return false;
+      if (!wait1(q_full + gs % NSQ, (gs / NSQ) & 1)) return false;
       tc::tc_fence_after();
       const uint32_t so = ((gs % NSQ) * TILE) >> 4;
-      if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          tc::mma_ss(tmem + reg_s(gs), dK_ + kslice(k), dQk + so + kslice(k), idesc_s, k > 0);
-        tc::mma_commit(s_full);
-      }
-      __syncwarp();
+      for (int k = 0; k < D / 16; ++k)
+        tc::mma_ss(tmem + reg_s(gs), dK_ + kslice(k), dQk + so + kslice(k), idesc_s, k > 0);
+      tc::mma_commit(s_full);
       return true;
     };
     auto issue_dp = [&](int gs) -> bool {  // dP^T(gs) = V dO^T into B_gs
-      if (!wait_u(do_full + gs % NSD, (gs / NSD) & 1)) return false;
+      if (!wait1(do_full + gs % NSD, (gs / NSD) & 1)) return false;
       tc::tc_fence_after();
       const uint32_t so = ((gs % NSD) * TILE) >> 4;
-      if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          tc::mma_ss(tmem + reg_s(gs + 1), dV_ + kslice(k), dDOk + so + kslice(k), idesc_s, k > 0);
-        tc::mma_commit(dp_full);
-      }
-      __syncwarp();
+      for (int k = 0; k < D / 16; ++k)
+        tc::mma_ss(tmem + reg_s(gs + 1), dV_ + kslice(k), dDOk + so + kslice(k), idesc_s, k > 0);
+      tc::mma_commit(dp_full);
       return true;
     };
-    auto commit = [&](uint64_t* b_) {
-      if (tc::elect_one()) tc::mma_commit(b_);
-      __syncwarp();
-    };
+    auto commit = [&](uint64_t* b_) { tc::mma_commit(b_); };
+    if (tc::elect_one()) {
     int qs = 0, nk = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
+      if (!(ok = wait1(item_full + (k & 1), (k >> 1) & 1))) break;
       const int it = item_ring[k & 1];
-      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
-      __syncwarp();
+      tc::mbar_arrive(item_empty + (k & 1));
       if (it < 0) break;
       const KvItem I = decode_kv(p, it);
       const int n = I.n;
       if (n <= 0) continue;
-      if (!(ok = wait_u(kv_full, nk & 1))) break;
+      if (!(ok = wait1(kv_full, nk & 1))) break;
       tc::tc_fence_after();
       if (!(ok = issue_s(qs) && issue_dp(qs))) break;
       if (n == 1) commit(kv_empty);  // K and V are read by S^T and dP^T only
@@ -473,32 +468,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gs = qs + t, sq = gs % NSQ, sd = gs % NSD;
         const uint32_t soq = (sq * TILE) >> 4, sod = (sd * TILE) >> 4;
         const uint32_t A = tmem + reg_s(gs);
-        if (!(ok = wait_u(p_ready, gs & 1))) break;
-        if (t == 0 && nk > 0 && !(ok = wait_u(acc_free, (nk - 1) & 1))) break;
+        if (!(ok = wait1(p_ready, gs & 1))) break;
+        if (t == 0 && nk > 0 && !(ok = wait1(acc_free, (nk - 1) & 1))) break;
         tc::tc_fence_after();
-        if (tc::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kB / 16; ++kk)  // dV += P^T dO, P^T packed bf16 in A_t
-            mma_ts(tmem + T_DV, packed_a(A, 0, kk), dDOm + sod + ((kk * 2048) >> 4), idesc_kv,
-                   (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < kB / 16; ++kk)  // dV += P^T dO, P^T packed bf16 in A_t
+          mma_ts(tmem + T_DV, packed_a(A, 0, kk), dDOm + sod + ((kk * 2048) >> 4), idesc_kv,
+                 (t > 0 || kk > 0) ? 1u : 0u);
         // dV(t) keeps the tensor pipe busy while dP^T(t) is read out of B_t
         if (t + 1 < n) {
-          if (!(ok = wait_u(dp_free, gs & 1))) break;
+          if (!(ok = wait1(dp_free, gs & 1))) break;
           if (!(ok = issue_s(gs + 1))) break;
         }
-        if (!(ok = wait_u(ds_ready, gs & 1))) break;
+        if (!(ok = wait1(ds_ready, gs & 1))) break;
         tc::tc_fence_after();
-        if (tc::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in A_t
-            mma_ts(tmem + T_DK, packed_a(A, 16, kk), dQm + soq + ((kk * 2048) >> 4), idesc_kv,
-                   (t > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(q_empty + sq);
-          tc::mma_commit(do_empty + sd);  // after dS^T(t): the compute threads are done with LSE, D
-        }
-        __syncwarp();
+        for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in A_t
+          mma_ts(tmem + T_DK, packed_a(A, 16, kk), dQm + soq + ((kk * 2048) >> 4), idesc_kv,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(q_empty + sq);
+        tc::mma_commit(do_empty + sd);  // after dS^T(t): the compute threads are done with LSE, D
         if (t + 1 < n) {
           if (!(ok = issue_dp(gs + 1))) break;
           if (t + 2 == n) commit(kv_empty);
@@ -509,10 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       qs += n;
       ++nk;
     }
-    if (*abort_flag && tc::elect_one()) {  // let issued MMAs finish before TMEM is released
+    if (*abort_flag) {  // let issued MMAs finish before TMEM is released
       volatile int never = 0;
       tc::mma_commit(drain);
       tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
+    }
     }
     __syncwarp();
   } else if (warp < 4 * kNWG) {
@@ -883,6 +873,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread runs the whole loop (a warp-level sync after tcgen05.mma
+    // would hold the warp until the queued MMAs have gone into the pipe).
     constexpr uint32_t idesc_s = tc::idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_q = tc::idesc_bf16(128, D, false, true);
     const uint64_t dQ_ = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
@@ -890,74 +882,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKk = tc::smem_desc(tc::smem_u32(sK), 16, 1024);      // K as K-major B
     const uint64_t dKm = tc::smem_desc(tc::smem_u32(sK), kChunk, 1024);  // K as MN-major B
     const uint64_t dV_ = tc::smem_desc(tc::smem_u32(sV), 16, 1024);
+    auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
     auto issue_sdp = [&](int gt) -> bool {  // S(gt) = Q K^T into R[gt%3]; dP(gt) = dO V^T into R[(gt+1)%3]
       const int sk = gt % NSK, sv = gt % NSV;
-      if (!wait_u(k_full + sk, (gt / NSK) & 1)) return false;
+      if (!wait1(k_full + sk, (gt / NSK) & 1)) return false;
       tc::tc_fence_after();
-      if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          tc::mma_ss(tmem + rot3(gt), dQ_ + kslice(k), dKk + ((sk * TILE) >> 4) + kslice(k), idesc_s, k > 0);
-        tc::mma_commit(s_full);
-      }
-      __syncwarp();
-      if (!wait_u(v_full + sv, (gt / NSV) & 1)) return false;
+      for (int k = 0; k < D / 16; ++k)
+        tc::mma_ss(tmem + rot3(gt), dQ_ + kslice(k), dKk + ((sk * TILE) >> 4) + kslice(k), idesc_s, k > 0);
+      tc::mma_commit(s_full);
+      if (!wait1(v_full + sv, (gt / NSV) & 1)) return false;
       tc::tc_fence_after();
-      if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          tc::mma_ss(tmem + rot3(gt + 1), dDO_ + kslice(k), dV_ + ((sv * TILE) >> 4) + kslice(k), idesc_s, k > 0);
-        tc::mma_commit(dp_full);
-        tc::mma_commit(v_empty + sv);
-      }
-      __syncwarp();
+      for (int k = 0; k < D / 16; ++k)
+        tc::mma_ss(tmem + rot3(gt + 1), dDO_ + kslice(k), dV_ + ((sv * TILE) >> 4) + kslice(k), idesc_s, k > 0);
+      tc::mma_commit(dp_full);
+      tc::mma_commit(v_empty + sv);
       return true;
     };
-    auto commit = [&](uint64_t* b_) {
-      if (tc::elect_one()) tc::mma_commit(b_);
-      __syncwarp();
-    };
+    auto commit = [&](uint64_t* b_) { tc::mma_commit(b_); };
+    if (tc::elect_one()) {
     int gt = 0, nq = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_full + (k % kNIR), (k / kNIR) & 1))) break;
+      if (!(ok = wait1(item_full + (k % kNIR), (k / kNIR) & 1))) break;
       const int it = item_ring[4 * (k % kNIR)];
       const int n = item_ring[4 * (k % kNIR) + 1];
-      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k % kNIR));
-      __syncwarp();
+      tc::mbar_arrive(item_empty + (k % kNIR));
       if (it < 0) break;
       if (n == 0) continue;
-      if (!(ok = wait_u(q_full, nq & 1))) break;
+      if (!(ok = wait1(q_full, nq & 1))) break;
       if (!(ok = issue_sdp(gt))) break;
       if (n == 1) commit(q_empty);  // Q and dO are read by S and dP only
       for (int j = 0; ok && j < n; ++j) {
         const int g = gt + j, sk = g % NSK;
         if (j + 1 < n) {  // the next tile's S and dP once dP(j) has been read
-          if (!(ok = wait_u(dp_free, g & 1))) break;
+          if (!(ok = wait1(dp_free, g & 1))) break;
           if (!(ok = issue_sdp(g + 1))) break;
           if (j + 2 == n) commit(q_empty);
         }
-        if (!(ok = wait_u(ds_ready + (g & 1), (g >> 1) & 1))) break;
-        if (j == 0 && nq > 0 && !(ok = wait_u(dq_free, (nq - 1) & 1))) break;
+        if (!(ok = wait1(ds_ready + (g & 1), (g >> 1) & 1))) break;
+        if (j == 0 && nq > 0 && !(ok = wait1(dq_free, (nq - 1) & 1))) break;
         tc::tc_fence_after();
-        if (tc::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K, dS packed bf16 in R[g%3]
-            mma_ts(tmem + T_DQ, packed_a(tmem + rot3(g), 0, kk), dKm + ((sk * TILE) >> 4) + ((kk * 2048) >> 4),
-                   idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(k_empty + sk);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K, dS packed bf16 in R[g%3]
+          mma_ts(tmem + T_DQ, packed_a(tmem + rot3(g), 0, kk), dKm + ((sk * TILE) >> 4) + ((kk * 2048) >> 4),
+                 idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(k_empty + sk);
       }
       if (!ok) break;
       commit(dq_final);
       gt += n;
       ++nq;
     }
-    if (*abort_flag && tc::elect_one()) {
+    if (*abort_flag) {
       volatile int never = 0;
       tc::mma_commit(drain);
       tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
+    }
     }
     __syncwarp();
   } else if (warp < 4 * kNWG) {
@@ -1432,69 +1414,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ S and dP issuer (even CTA)
-    if (lead) {
+    // Each issuer is one thread running the whole loop: a warp-level sync
+    // after tcgen05.mma holds the warp until the thread's queued MMAs have
+    // gone into the pipe, which would leave the pipe idle during its waits.
+    if (lead && tc::elect_one()) {
       constexpr uint32_t idesc_s = tc::idesc_bf16(256, 128, false, false);
       const uint64_t dQ_ = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
       const uint64_t dDO_ = tc::smem_desc(tc::smem_u32(sDO), 16, 1024);
       const uint64_t dKx = tc::smem_desc(tc::smem_u32(sK), 16, 1024);               // my keys, K-major B
       const uint64_t dVx = tc::smem_desc(tc::smem_u32(sV), 16, 1024);
+      auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
       auto issue_s = [&](int gt, int qs) -> bool {  // S(gt) = Q K^T over the pair, Q in buffer qs
         const int sk = gt % NSK;
-        if (!wait_u(k_full + sk, (gt / NSK) & 1)) return false;
+        if (!wait1(k_full + sk, (gt / NSK) & 1)) return false;
         tc::tc_fence_after();
-        if (tc::elect_one()) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            tc::mma2_ss(tmem + T_S, dQ_ + ((qs * TILE) >> 4) + kslice(k), dKx + ((sk * KST) >> 4) + kslice(k, PIECE),
-                        idesc_s, k > 0);
-          tc::mma2_commit_both(s_full);
-        }
-        __syncwarp();
+        for (int k = 0; k < D / 16; ++k)
+          tc::mma2_ss(tmem + T_S, dQ_ + ((qs * TILE) >> 4) + kslice(k), dKx + ((sk * KST) >> 4) + kslice(k, PIECE),
+                      idesc_s, k > 0);
+        tc::mma2_commit_both(s_full);
         return true;
       };
       auto issue_dp = [&](int gt) -> bool {  // dP(gt) = dO V^T over the pair
         const int sv = gt % NSV;
-        if (!wait_u(v_full + sv, (gt / NSV) & 1)) return false;
+        if (!wait1(v_full + sv, (gt / NSV) & 1)) return false;
         tc::tc_fence_after();
-        if (tc::elect_one()) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            tc::mma2_ss(tmem + T_DP, dDO_ + kslice(k), dVx + ((sv * VST) >> 4) + kslice(k, PIECE), idesc_s, k > 0);
-          tc::mma2_commit_both(dp_full);
-          tc::mma2_commit_both(v_empty + sv);
-        }
-        __syncwarp();
+        for (int k = 0; k < D / 16; ++k)
+          tc::mma2_ss(tmem + T_DP, dDO_ + kslice(k), dVx + ((sv * VST) >> 4) + kslice(k, PIECE), idesc_s, k > 0);
+        tc::mma2_commit_both(dp_full);
+        tc::mma2_commit_both(v_empty + sv);
         return true;
       };
       int gt = 0, nq = 0;
-      auto commit = [&](uint64_t* b_) {
-        if (tc::elect_one()) tc::mma2_commit_both(b_);
-        __syncwarp();
-      };
+      auto commit = [&](uint64_t* b_) { tc::mma2_commit_both(b_); };
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        if (!(ok = wait_ring(item_full + (k % kNIR), (k / kNIR) & 1))) break;
+        if (!(ok = tc::mbar_wait_cluster(item_full + (k % kNIR), (k / kNIR) & 1, abort_flag, &g_status_bwd))) break;
         const int it = item_ring[4 * (k % kNIR)];
         const int n = item_ring[4 * (k % kNIR) + 1];
-        if (tc::elect_one()) tc::mbar_arrive(item_empty + (k % kNIR));
-        __syncwarp();
+        tc::mbar_arrive(item_empty + (k % kNIR));
         if (it < 0) break;
         if (n == 0) continue;
         // the previous item's last S and dP have been read (waited below)
         const int qs = nq % NSQ;
-        if (!(ok = wait_u(q_full + qs, (nq / NSQ) & 1))) break;
+        if (!(ok = wait1(q_full + qs, (nq / NSQ) & 1))) break;
         if (!(ok = issue_s(gt, qs))) break;
         if (n == 1) commit(q_empty + qs);  // Q is read by S only, dO by dP only
-        if (!(ok = wait_u(do_full, nq & 1) && issue_dp(gt))) break;
+        if (!(ok = wait1(do_full, nq & 1) && issue_dp(gt))) break;
         if (n == 1) commit(do_empty);
         for (int j = 0; ok && j < n; ++j) {
           const int g = gt + j;
-          if (!(ok = wait_u(s_free, g & 1))) break;
+          if (!(ok = wait1(s_free, g & 1))) break;
           if (j + 1 < n) {
             if (!(ok = issue_s(g + 1, qs))) break;
             if (j + 2 == n) commit(q_empty + qs);
           }
-          if (!(ok = wait_u(dp_free, g & 1))) break;
+          if (!(ok = wait1(dp_free, g & 1))) break;
           if (j + 1 < n) {
             if (!(ok = issue_dp(g + 1))) break;
             if (j + 2 == n) commit(do_empty);
@@ -1504,56 +1480,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         gt += n;
         ++nq;
       }
-      if (*abort_flag && tc::elect_one()) {
+      if (*abort_flag) {
         volatile int never = 0;
         tc::mma2_commit_both(drain);
         tc::mbar_wait(drain, 0, &never, &g_status_bwd, 100000000ull);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else if (warp == kWMmaQ) {
     // ------------------------------------------------------------ dQ issuer (even CTA)
-    if (lead) {
+    if (lead && tc::elect_one()) {
+      auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
       constexpr uint32_t idesc_q = tc::idesc_bf16(256, D, false, true);
       const uint64_t dKy = tc::smem_desc(tc::smem_u32(sK + 2 * PIECE), kChunk, 1024);  // my columns, MN-major B
       int gt = 0, nq = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        if (!(ok = wait_ring(item_full + (k % kNIR), (k / kNIR) & 1))) break;
+        if (!(ok = tc::mbar_wait_cluster(item_full + (k % kNIR), (k / kNIR) & 1, abort_flag, &g_status_bwd))) break;
         const int it = item_ring[4 * (k % kNIR)];
         const int n = item_ring[4 * (k % kNIR) + 1];
-        if (tc::elect_one()) tc::mbar_arrive(item_empty + (k % kNIR));
-        __syncwarp();
+        tc::mbar_arrive(item_empty + (k % kNIR));
         if (it < 0) break;
         if (n == 0) continue;
         for (int j = 0; ok && j < n; ++j) {
           const int g = gt + j, sk = g % NSK;
-          if (!(ok = wait_u(ds_ready + (g & 1), (g >> 1) & 1))) break;
-          if (j == 0 && nq > 0 && !(ok = wait_u(dq_free, (nq - 1) & 1))) break;
+          if (!(ok = wait1(ds_ready + (g & 1), (g >> 1) & 1))) break;
+          if (j == 0 && nq > 0 && !(ok = wait1(dq_free, (nq - 1) & 1))) break;
           tc::tc_fence_after();
-          if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K over the pair, dS packed in T_DS[g&1]
-              tc::mma2_ts(tmem + T_DQ, tmem + T_DS + 64 * (g & 1) + 8 * kk,
-                          dKy + ((sk * KST) >> 4) + ((kk * 2048) >> 4), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
-            tc::mma2_commit_both(ds_free + (g & 1));
-            tc::mma2_commit_both(k_empty + sk);  // S(g) was read before dS(g) existed
-          }
-          __syncwarp();
+          for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K over the pair, dS packed in T_DS[g&1]
+            tc::mma2_ts(tmem + T_DQ, tmem + T_DS + 64 * (g & 1) + 8 * kk,
+                        dKy + ((sk * KST) >> 4) + ((kk * 2048) >> 4), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma2_commit_both(ds_free + (g & 1));
+          tc::mma2_commit_both(k_empty + sk);  // S(g) was read before dS(g) existed
         }
         if (!ok) break;
-        if (tc::elect_one()) tc::mma2_commit_both(dq_final);
-        __syncwarp();
+        tc::mma2_commit_both(dq_final);
         gt += n;
         ++nq;
       }
-      if (*abort_flag && tc::elect_one()) {
+      if (*abort_flag) {
         volatile int never = 0;
         tc::mma2_commit_both(drain + 1);
         tc::mbar_wait(drain + 1, 0, &never, &g_status_bwd, 100000000ull);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else if (warp < kNWarpsC) {
     // ------------------------------------------------------------ compute warpgroups (both CTAs)
     const int w = warp >> 2;          // key columns [32w, 32w+32) of each tile

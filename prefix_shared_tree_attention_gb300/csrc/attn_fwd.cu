@@ -64,16 +64,20 @@ template <int D, int NH>
 struct FwdCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = NCH * kChunk;   // one 128 x D bf16 tile
-  static constexpr uint32_t BASE = NH * TILE + 4096;
+  // O leaves through the TMA engine, 64 columns (one 16 KB swizzled box) of
+  // a head at a time, staged here per head
+  static constexpr uint32_t STAGE = NH * kChunk;
+  static constexpr uint32_t BASE = NH * TILE + STAGE + 512;  // + barriers and flags
   static constexpr int NS_FIT = int((kSmemMax - 1024 - BASE) / (2 * TILE));
   static constexpr int NS = NS_FIT > 3 ? 3 : NS_FIT;  // K and V ring depth
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + NH * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
-  static constexpr uint32_t OFF_BAR = OFF_V + NS * TILE;
+  static constexpr uint32_t OFF_STAGE = OFF_V + NS * TILE;
+  static constexpr uint32_t OFF_BAR = OFF_STAGE + STAGE;
   // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[NH], p_full[NH],
-  // o_free[NH], o_final, drain, item_full[2], item_empty[2]
-  static constexpr int NBAR = 2 + 4 * NS + 3 * NH + 2 + 4;
+  // o_free[NH], stage_full[NH], stage_free[NH], o_final, drain, item_full[2], item_empty[2]
+  static constexpr int NBAR = 2 + 4 * NS + 5 * NH + 2 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;  // + alignment slack
   static constexpr int THREADS = 128 * NH + 64;
@@ -143,7 +147,8 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int it) {
 template <int D, int NH>
 __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
   using C = FwdCfg<D, NH>;
   constexpr int NCH = C::NCH, NS = C::NS;
   constexpr uint32_t TILE = C::TILE;
@@ -162,7 +167,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   uint64_t* s_full = v_empty + NS;
   uint64_t* p_full = s_full + NH;
   uint64_t* o_free = p_full + NH;
-  uint64_t* o_final = o_free + NH;
+  uint64_t* stage_full = o_free + NH;     // [NH]: the warpgroup wrote its O stage
+  uint64_t* stage_free = stage_full + NH;  // [NH]: the TMA engine has read it
+  uint64_t* o_final = stage_free + NH;
   uint64_t* drain = o_final + 1;
   uint64_t* item_full = drain + 1;   // [2]
   uint64_t* item_empty = drain + 3;  // [2]
@@ -187,6 +194,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       tc::mbar_init(s_full + h, 1);
       tc::mbar_init(p_full + h, 128);
       tc::mbar_init(o_free + h, 128);
+      tc::mbar_init(stage_full + h, 128);
+      tc::mbar_init(stage_free + h, 1);
     }
     tc::mbar_init(o_final, 1);
     tc::mbar_init(drain, 1);
@@ -275,6 +284,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     __syncwarp();
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread runs the whole loop.  A warp-level sync after tcgen05.mma
+    // holds the warp until the thread's queued MMAs have gone into the pipe,
+    // so with the warp in step every wait between MMA groups would leave the
+    // tensor pipe idle; a lone thread's waits overlap the queued MMAs.
     constexpr uint32_t idesc_qk = tc::idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, false, true);
     // Descriptors are built once; a k-step or stage only adds (byte offset >> 4)
@@ -284,44 +297,36 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     const uint64_t dV = tc::smem_desc(tc::smem_u32(sV), kChunk, 1024);
     auto issue_s = [&](int h, int s) {  // S_h = Q_h K(s)^T
       const uint64_t qa = dQ + ((h * TILE) >> 4), kb_ = dK + ((s * TILE) >> 4);
-      if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
-          tc::mma_ss(tmem + h * 128, qa + off, kb_ + off, idesc_qk, k > 0);
-        }
-        tc::mma_commit(s_full + h);
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = ((k >> 2) * kChunk + (k & 3) * 32) >> 4;
+        tc::mma_ss(tmem + h * 128, qa + off, kb_ + off, idesc_qk, k > 0);
       }
-      __syncwarp();
+      tc::mma_commit(s_full + h);
     };
     auto issue_pv = [&](int h, int s, bool first) {  // O_h (+)= P_h V(s), P_h read from TMEM
       const uint64_t vb = dV + ((s * TILE) >> 4);
-      if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < kB / 16; ++k)
-          mma_ts(tmem + 128 * NH + h * 128, tmem + h * 128 + k * 8, vb + ((k * 2048) >> 4), idesc_pv,
-                 (!first || k > 0) ? 1u : 0u);
-      }
-      __syncwarp();
+      for (int k = 0; k < kB / 16; ++k)
+        mma_ts(tmem + 128 * NH + h * 128, tmem + h * 128 + k * 8, vb + ((k * 2048) >> 4), idesc_pv,
+               (!first || k > 0) ? 1u : 0u);
     };
-    auto commit = [&](uint64_t* b_) {
-      if (tc::elect_one()) tc::mma_commit(b_);
-      __syncwarp();
-    };
+    auto commit = [&](uint64_t* b_) { tc::mma_commit(b_); };
+    auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_fwd); };
+    if (tc::elect_one()) {
     int kt = 0, vt = 0, tb = 0, nq = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
+      if (!(ok = wait1(item_full + (k & 1), (k >> 1) & 1))) break;
       const int it = item_ring[k & 1];
-      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
-      __syncwarp();
+      tc::mbar_arrive(item_empty + (k & 1));
       if (it < 0) break;
       const Item I = decode_item<NH>(p, it);
       const int n_it = I.n_it;
       if (n_it == 0) continue;
       // S_h(0): the S regions were last read by the previous item's PV (issued
       // earlier, executed in order) and its softmax (done before its p_full).
-      if (!(ok = wait_u(q_full, nq & 1) && wait_u(k_full + kt % NS, (kt / NS) & 1))) break;
+      if (!(ok = wait1(q_full, nq & 1) && wait1(k_full + kt % NS, (kt / NS) & 1))) break;
       tc::tc_fence_after();
       for (int h = 0; h < NH; ++h) issue_s(h, kt % NS);
       commit(k_empty + kt % NS);
@@ -330,14 +335,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
         const int gv = vt + j, sv = gv % NS;
         const int gk1 = kt + j + 1, s1 = gk1 % NS;
         const bool more = j + 1 < n_it;
-        if (!(ok = wait_u(v_full + sv, (gv / NS) & 1))) break;
+        if (!(ok = wait1(v_full + sv, (gv / NS) & 1))) break;
         for (int h = 0; h < NH && ok; ++h) {
-          if (!(ok = wait_u(p_full + h, (tb + j) & 1))) break;
-          if (j == 0 && nq > 0 && !(ok = wait_u(o_free + h, (nq - 1) & 1))) break;
+          if (!(ok = wait1(p_full + h, (tb + j) & 1))) break;
+          if (j == 0 && nq > 0 && !(ok = wait1(o_free + h, (nq - 1) & 1))) break;
           tc::tc_fence_after();
           issue_pv(h, sv, j == 0);
           if (more) {
-            if (h == 0 && !(ok = wait_u(k_full + s1, (gk1 / NS) & 1))) break;
+            if (h == 0 && !(ok = wait1(k_full + s1, (gk1 / NS) & 1))) break;
             tc::tc_fence_after();
             issue_s(h, s1);
           }
@@ -355,10 +360,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       tb += n_it;
       ++nq;
     }
-    if (*abort_flag && tc::elect_one()) {  // let issued MMAs finish before TMEM is released
+    if (*abort_flag) {  // let issued MMAs finish before TMEM is released
       volatile int never = 0;
       tc::mma_commit(drain);
       tc::mbar_wait(drain, 0, &never, &g_status_fwd, 100000000ull);
+    }
     }
     __syncwarp();
   } else {
@@ -373,6 +379,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_fwd));
     };
     int tb = 0, nq = 0;
+    int su = 0;  // uses of this warpgroup's O stage so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
       if (!wait_all(item_full + (k & 1), (k >> 1) & 1)) break;
@@ -470,32 +477,52 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
       if (!ok || !wait_all(o_final, nq & 1)) { ok = false; break; }
       tc::tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      // O_h / l as bf16 through a 16 KB swizzled stage, 64 columns at a time,
+      // written out by the TMA engine: the item's 32 KB of O rows do not hold
+      // up this warpgroup's next loads and barrier waits behind a burst of
+      // stores.  Thread r == 0 issues the copies; before a refill it waits
+      // until the engine has read the stage and frees it for the others.
+      uint8_t* stg = smem + C::OFF_STAGE + h * kChunk;
+      const int orow0 = I.b * p.t_pad + I.qb * kB;
+      for (int half = 0; half < NCH && ok; ++half, ++su) {
+        uint32_t w[32];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tc::tmem_ld32(tO + c * 32, ov);
-        tc::tmem_ld_wait();
-        uint32_t w[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[32];
+          tc::tmem_ld32(tO + half * 64 + c * 32, ov);
+          tc::tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          w[u] = tc::pack_bf16(__uint_as_float(ov[2 * u]) * inv, __uint_as_float(ov[2 * u + 1]) * inv);
-        if (p.wide) {  // two 32-byte stores: one full sector each
-          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + c * 32), "r"(w[0]),
-                       "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                       : "memory");
-          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(orow + c * 32 + 16),
-                       "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
-                       : "memory");
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          for (int u = 0; u < 16; ++u)
+            w[16 * c + u] = tc::pack_bf16(__uint_as_float(ov[2 * u]) * inv, __uint_as_float(ov[2 * u + 1]) * inv);
         }
+        if (half == NCH - 1) {
+          tc::tc_fence_before();
+          tc::mbar_arrive(o_free + h);  // O_h may be overwritten by the next item
+        }
+        if (su > 0) {
+          if (r == 0) {
+            tc::bulk_wait_read();
+            tc::mbar_arrive(stage_free + h);
+          }
+          if (!wait_all(stage_free + h, (su - 1) & 1)) { ok = false; break; }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(stg + tc::sw128_offset(uint32_t(r), uint32_t(c))) =
+              make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(stage_full + h);
+        bool staged = true;
+        if (r == 0) {
+          staged = tc::mbar_wait(stage_full + h, su & 1, abort_flag, &g_status_fwd);
+          if (staged) {
+            tc::tma_store_3d(&tm_o, stg, half * 64, I.h0 + h, orow0);
+            tc::bulk_commit();
+          }
+        }
+        if (!__all_sync(0xffffffffu, staged)) { ok = false; break; }
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(o_free + h);  // O_h may be overwritten by the next item
+      if (!ok) break;
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       *lse_out = l_run > 0.f ? (m_use + __log2f(l_run)) * kLn2 : 0.f;
       tb += n_it;
@@ -503,6 +530,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     }
   }
 
+  if (warp < W_TMA && (threadIdx.x & 127) == 0) tc::bulk_wait_all();  // this warpgroup's O copies
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -527,13 +555,14 @@ int num_sms() {
 }
 
 template <int D, int NH>
-int launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, FwdParams prm,
+int launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                   FwdParams prm,
                    int n_trees, cudaStream_t st) {
   using C = FwdCfg<D, NH>;
   prm.n_items = prm.n_blk * (prm.hq / NH) * n_trees;
   const int grid = prm.n_items < num_sms() ? prm.n_items : num_sms();
   TPA_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES));
-  attn_fwd_kernel<D, NH><<<grid, C::THREADS, C::BYTES, st>>>(tq, tk, tv, prm);
+  attn_fwd_kernel<D, NH><<<grid, C::THREADS, C::BYTES, st>>>(tq, tk, tv, to, prm);
   TPA_CUDA_TRY(cudaGetLastError());
   return TPA_OK;
 }
@@ -542,9 +571,9 @@ template <int D>
 int launch_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const void* q, const void* k,
                const void* v, void* o, float* lse, int hq, int hkv, float scale, cudaStream_t st) {
   const uint64_t rows = uint64_t(tree->n_trees) * tree->t_pad;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!tmap::make_rows_heads_d(&tq, q, rows, hq, D) || !tmap::make_rows_heads_d(&tk, k, rows, hkv, D) ||
-      !tmap::make_rows_heads_d(&tv, v, rows, hkv, D))
+      !tmap::make_rows_heads_d(&tv, v, rows, hkv, D) || !tmap::make_rows_heads_d(&to, o, rows, hq, D))
     return TPA_ERR_CUDA;
   FwdParams prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
@@ -561,8 +590,8 @@ int launch_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.hkv = hkv;
   prm.n_items = 0;
   prm.scale_log2 = scale * kLog2e;
-  if ((hq / hkv) % 2 == 0) return launch_fwd_cfg<D, 2>(tq, tk, tv, prm, tree->n_trees, st);
-  return launch_fwd_cfg<D, 1>(tq, tk, tv, prm, tree->n_trees, st);
+  if ((hq / hkv) % 2 == 0) return launch_fwd_cfg<D, 2>(tq, tk, tv, to, prm, tree->n_trees, st);
+  return launch_fwd_cfg<D, 1>(tq, tk, tv, to, prm, tree->n_trees, st);
 }
 
 }  // namespace
