@@ -481,13 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = issue_s(gs + 1))) break;
         }
         if (!(ok = wait1(ds_ready, gs & 1))) break;
+        // dO(t) was last read by dV(t), and the compute threads are done with
+        // its LSE and D: the stage is free once the MMAs issued so far are
+        tc::mma_commit(do_empty + sd);
         tc::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in A_t
           mma_ts(tmem + T_DK, packed_a(A, 16, kk), dQm + soq + ((kk * 2048) >> 4), idesc_kv,
                  (t > 0 || kk > 0) ? 1u : 0u);
         tc::mma_commit(q_empty + sq);
-        tc::mma_commit(do_empty + sd);  // after dS^T(t): the compute threads are done with LSE, D
         if (t + 1 < n) {
           if (!(ok = issue_dp(gs + 1))) break;
           if (t + 2 == n) commit(kv_empty);
@@ -559,13 +561,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld_wait();
           const int lo = j - (qb * kB + kCW * w);  // visible query columns: [lo, hi]
           const int hi = Ej - (qb * kB + kCW * w);
+          const uint64_t sl2 = tc::f2(p.scale_log2, p.scale_log2), nl2 = tc::f2(-kLog2e, -kLog2e);
 #pragma unroll
-          for (int c4 = 0; c4 < kCW / 4; ++c4) {
+          for (int c4 = 0; c4 < kCW / 4; ++c4) {  // packed pairs: S*scale*log2e - LSE*log2e
             const float4 l = l4[c4];
-            const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              pf[4 * c4 + e] = tc::ex2(fmaf(__uint_as_float(sv[4 * c4 + e]), p.scale_log2, -lv[e] * kLog2e));
+            const int c = 4 * c4;
+            const uint64_t a01 = tc::fma2(tc::f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2,
+                                          tc::mul2(tc::f2(l.x, l.y), nl2));
+            const uint64_t a23 = tc::fma2(tc::f2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2,
+                                          tc::mul2(tc::f2(l.z, l.w), nl2));
+            float x0, x1, x2, x3;
+            tc::unf2(a01, x0, x1);
+            tc::unf2(a23, x2, x3);
+            pf[c] = tc::ex2(x0);
+            pf[c + 1] = tc::ex2(x1);
+            pf[c + 2] = tc::ex2(x2);
+            pf[c + 3] = tc::ex2(x3);
           }
           if (!full) {
 #pragma unroll
@@ -592,13 +603,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4* d4 = reinterpret_cast<const float4*>(sDv + st * kB + kCW * w);
           uint32_t dw[kCW / 2];
 #pragma unroll
-          for (int c4 = 0; c4 < kCW / 4; ++c4) {
+          for (int c4 = 0; c4 < kCW / 4; ++c4) {  // packed pairs: P (dP - D)
             const float4 dd = d4[c4];
             const int c = 4 * c4;
-            dw[2 * c4] = tc::pack_bf16(pf[c] * (__uint_as_float(dpv[c]) - dd.x),
-                                       pf[c + 1] * (__uint_as_float(dpv[c + 1]) - dd.y));
-            dw[2 * c4 + 1] = tc::pack_bf16(pf[c + 2] * (__uint_as_float(dpv[c + 2]) - dd.z),
-                                           pf[c + 3] * (__uint_as_float(dpv[c + 3]) - dd.w));
+            const uint64_t g01 = tc::mul2(tc::f2(pf[c], pf[c + 1]),
+                                          tc::sub2(tc::f2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                                   tc::f2(dd.x, dd.y)));
+            const uint64_t g23 = tc::mul2(tc::f2(pf[c + 2], pf[c + 3]),
+                                          tc::sub2(tc::f2(__uint_as_float(dpv[c + 2]), __uint_as_float(dpv[c + 3])),
+                                                   tc::f2(dd.z, dd.w)));
+            float y0, y1, y2, y3;
+            tc::unf2(g01, y0, y1);
+            tc::unf2(g23, y2, y3);
+            dw[2 * c4] = tc::pack_bf16(y0, y1);
+            dw[2 * c4 + 1] = tc::pack_bf16(y2, y3);
           }
           tc::tmem_st16(tA + 16, dw);  // second half of this group's S^T columns
           tc::tmem_st_wait();
@@ -997,8 +1015,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = prefetch(k + 1, nx);
         continue;
       }
-      const float nlse2 = -I.lse * kLog2e;
-      const float drow = I.drow;
+      const float nlse = -I.lse * kLog2e;
+      const uint64_t sl2 = tc::f2(p.scale_log2, p.scale_log2), nl2 = tc::f2(nlse, nlse);
+      const uint64_t drow2 = tc::f2(I.drow, I.drow);
       const uint32_t* qmask_row =
           reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(b) * p.cap + I.e0) * kB + r) + w;
       const int32_t* list = p.q_idx + int64_t(b) * p.cap + I.e0;
@@ -1021,7 +1040,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld32(tS, sv);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < kCW; ++c) pf[c] = tc::ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, nlse2));
+          for (int c = 0; c < kCW; c += 2) {  // packed pairs: S*scale*log2e - LSE*log2e
+            float x0, x1;
+            tc::unf2(tc::fma2(tc::f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2, nl2), x0, x1);
+            pf[c] = tc::ex2(x0);
+            pf[c + 1] = tc::ex2(x1);
+          }
           if (!full) {
 #pragma unroll
             for (int c = 0; c < kCW; ++c)
@@ -1038,9 +1062,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_arrive(dp_free);  // R[(g+1)%3] may take S of the next tile now
           uint32_t dw[kCW / 2];
 #pragma unroll
-          for (int e = 0; e < kCW / 2; ++e)
-            dw[e] = tc::pack_bf16(pf[2 * e] * (__uint_as_float(dpv[2 * e]) - drow),
-                                  pf[2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - drow));
+          for (int e = 0; e < kCW / 2; ++e) {  // packed pairs: P (dP - D)
+            float y0, y1;
+            tc::unf2(tc::mul2(tc::f2(pf[2 * e], pf[2 * e + 1]),
+                              tc::sub2(tc::f2(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), drow2)),
+                     y0, y1);
+            dw[e] = tc::pack_bf16(y0, y1);
+          }
           tc::tmem_st16(tS, dw);  // dS over the first half of this group's S columns
           tc::tmem_st_wait();
         }
@@ -1600,8 +1628,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         ok = prefetch(k + 1, nx);
         continue;
       }
-      const float nlse2 = -I.lse * kLog2e;
-      const float drow = I.drow;
+      const float nlse = -I.lse * kLog2e;
+      const uint64_t sl2 = tc::f2(p.scale_log2, p.scale_log2), nl2 = tc::f2(nlse, nlse);
+      const uint64_t drow2 = tc::f2(I.drow, I.drow);
       const uint32_t* qmask_row =
           reinterpret_cast<const uint32_t*>(p.qmask + (int64_t(b) * p.cap + I.e0) * kB + r) + w;
       const int32_t* list = p.q_idx + int64_t(b) * p.cap + I.e0;
@@ -1625,7 +1654,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
           tc::tc_fence_before();
           warp_arrive_lead(s_free);  // S of the next tile may be issued now
 #pragma unroll
-          for (int c = 0; c < kCW; ++c) pf[c] = tc::ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, nlse2));
+          for (int c = 0; c < kCW; c += 2) {  // packed pairs: S*scale*log2e - LSE*log2e
+            float x0, x1;
+            tc::unf2(tc::fma2(tc::f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2, nl2), x0, x1);
+            pf[c] = tc::ex2(x0);
+            pf[c + 1] = tc::ex2(x1);
+          }
           if (!full) {
 #pragma unroll
             for (int c = 0; c < kCW; ++c)
@@ -1643,9 +1677,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
           warp_arrive_lead(dp_free);
           uint32_t dw[kCW / 2];
 #pragma unroll
-          for (int e = 0; e < kCW / 2; ++e)
-            dw[e] = tc::pack_bf16(pf[2 * e] * (__uint_as_float(dpv[2 * e]) - drow),
-                                  pf[2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - drow));
+          for (int e = 0; e < kCW / 2; ++e) {  // packed pairs: P (dP - D)
+            float y0, y1;
+            tc::unf2(tc::mul2(tc::f2(pf[2 * e], pf[2 * e + 1]),
+                              tc::sub2(tc::f2(__uint_as_float(dpv[2 * e]), __uint_as_float(dpv[2 * e + 1])), drow2)),
+                     y0, y1);
+            dw[e] = tc::pack_bf16(y0, y1);
+          }
           // dS(g) goes where dS(g-2) was: wait until dQ(g-2) has read it
           if (g >= 2 && !wait_u(ds_free + (g & 1), ((g >> 1) - 1) & 1)) { ok = false; break; }
           tc::tc_fence_after();
