@@ -174,7 +174,9 @@ struct KvCfg {
   static constexpr int NCH = D / 64;
   static constexpr uint32_t TILE = NCH * kChunk;  // 128-row tile of K, V, Q or dO
   // Q ring one stage deeper than the dO ring: Q(t) feeds S^T(t), which is
-  // issued a step before dP^T(t).  LSE and D travel with dO.
+  // issued a step before dP^T(t), and dK(t), the step's last MMA.  LSE
+  // travels with dO (read before P^T(t) is published, so the dO stage frees
+  // once dV(t) is done), D with Q (read until dS^T(t) is published).
   static constexpr int NSQ = D == 128 ? 3 : 4;
   static constexpr int NSD = D == 128 ? 2 : 3;
   static constexpr uint32_t OFF_K = 0;
@@ -182,8 +184,8 @@ struct KvCfg {
   static constexpr uint32_t OFF_Q = OFF_V + TILE;
   static constexpr uint32_t OFF_DO = OFF_Q + NSQ * TILE;
   static constexpr uint32_t OFF_LSE = OFF_DO + NSD * TILE;    // NSD x 128 fp32
-  static constexpr uint32_t OFF_DV = OFF_LSE + NSD * kB * 4;  // NSD x 128 fp32
-  static constexpr uint32_t OFF_BAR = OFF_DV + NSD * kB * 4;
+  static constexpr uint32_t OFF_DV = OFF_LSE + NSD * kB * 4;  // NSQ x 128 fp32
+  static constexpr uint32_t OFF_BAR = OFF_DV + NSQ * kB * 4;
   // kv_full, kv_empty, q_full[NSQ], q_empty[NSQ], do_full[NSD], do_empty[NSD], s_full, dp_full,
   // p_ready, dp_free, ds_ready, acc_full, acc_free, drain, item_full[2], item_empty[2]
   static constexpr int NBAR = 2 + 2 * NSQ + 2 * NSD + 8 + 4;
@@ -328,87 +330,75 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWTma) {
     // ------------------------------------------------------------ producer
+    // One thread runs the whole loop, like the MMA issuer: a warp-level sync
+    // right after the bulk copies would hold the warp until they are issued.
     if (tc::elect_one()) {
       tc::tma_prefetch_desc(&tm_q);
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
       tc::tma_prefetch_desc(&tm_do);
-    }
-    __syncwarp();
-    tc::grid_wait_prior();  // D, loaded with each dO stage, comes from the preprocess
-    int qs = 0, nk = 0, nq_half = 0;  // steps loaded, K/V loads, and a lone Q load in flight
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
-      // Take indices until one has work (bf16 outputs also need the zero
-      // rows of key tiles no query sees); only that one is handed on.
-      int it = -1;
-      KvItem I;
-      for (;;) {
-        uint32_t u = 0;
-        if ((threadIdx.x & 31) == 0) u = atomicAdd(p.sched + 2, 1u);
-        u = __shfl_sync(0xffffffffu, u, 0);
-        if (u >= uint32_t(p.kv_items)) break;  // unsigned: no index below 0
-        I = decode_kv(p, int(u));
-        if (I.n > 0 || (!F32OUT && I.s0 == 0)) {
-          it = int(u);
-          break;
+      tc::grid_wait_prior();  // D, loaded with each dO stage, comes from the preprocess
+      auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
+      int qs = 0, nk = 0, nq_half = 0;  // steps loaded, K/V loads, and a lone Q load in flight
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (!(ok = wait1(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+        // Take indices until one has work (bf16 outputs also need the zero
+        // rows of key tiles no query sees); only that one is handed on.
+        int it = -1;
+        KvItem I;
+        for (;;) {
+          const uint32_t u = atomicAdd(p.sched + 2, 1u);
+          if (u >= uint32_t(p.kv_items)) break;  // unsigned: no index below 0
+          I = decode_kv(p, int(u));
+          if (I.n > 0 || (!F32OUT && I.s0 == 0)) {
+            it = int(u);
+            break;
+          }
         }
-      }
-      if (tc::elect_one()) {
         item_ring[k & 1] = it;
         tc::mbar_arrive(item_full + (k & 1));
-      }
-      __syncwarp();
-      if (it < 0) break;
-      if (I.n <= 0) continue;
-      const int krow = I.b * p.t_pad + I.kb * kB;
-      if (!(ok = wait_u(kv_empty, (nk & 1) ^ 1))) break;
-      if (tc::elect_one()) {
+        if (it < 0) break;
+        if (I.n <= 0) continue;
+        const int krow = I.b * p.t_pad + I.kb * kB;
+        if (!(ok = wait1(kv_empty, (nk & 1) ^ 1))) break;
         tc::mbar_arrive_expect_tx(kv_full, 2 * TILE);
         for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sK + c * kChunk, &tm_k, kv_full, c * 64, I.g, krow);
         for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sV + c * kChunk, &tm_v, kv_full, c * 64, I.g, krow);
-      }
-      __syncwarp();
-      ++nk;
-      int entry = I.list[I.s0 % I.n_col];
-      for (int t = 0; t < I.n; ++t) {
-        const int sq = qs % NSQ, sd = qs % NSD;
-        const int s = I.s0 + t;
-        const int h = I.g * G + s / I.n_col;
-        const int qb = entry >> 1;
-        if (t + 1 < I.n) entry = I.list[(s + 1) % I.n_col];
-        const int qrow = I.b * p.t_pad + qb * kB;
-        const int64_t vec = (int64_t(I.b) * p.hq + h) * p.t_pad + qb * kB;
-        if (!(ok = wait_u(q_empty + sq, ((qs / NSQ) & 1) ^ 1))) break;
-        if (tc::elect_one()) {
-          tc::mbar_arrive_expect_tx(q_full + sq, TILE);
+        ++nk;
+        int entry = I.list[I.s0 % I.n_col];
+        for (int t = 0; t < I.n; ++t) {
+          const int sq = qs % NSQ, sd = qs % NSD;
+          const int s = I.s0 + t;
+          const int h = I.g * G + s / I.n_col;
+          const int qb = entry >> 1;
+          if (t + 1 < I.n) entry = I.list[(s + 1) % I.n_col];
+          const int qrow = I.b * p.t_pad + qb * kB;
+          const int64_t vec = (int64_t(I.b) * p.hq + h) * p.t_pad + qb * kB;
+          if (!(ok = wait1(q_empty + sq, ((qs / NSQ) & 1) ^ 1))) break;
+          tc::mbar_arrive_expect_tx(q_full + sq, TILE + kB * 4);
           for (int c = 0; c < NCH; ++c)
             tc::tma_load_3d(sQ + sq * TILE + c * kChunk, &tm_q, q_full + sq, c * 64, h, qrow);
-        }
-        __syncwarp();
-        nq_half = 1;  // this step's Q load is in flight, its dO load not yet
-        if (!(ok = wait_u(do_empty + sd, ((qs / NSD) & 1) ^ 1))) break;
-        if (tc::elect_one()) {
-          tc::mbar_arrive_expect_tx(do_full + sd, TILE + 2 * kB * 4);
+          tc::bulk_load(sDv + sq * kB, p.dvec + vec, kB * 4, q_full + sq);
+          nq_half = 1;  // this step's Q load is in flight, its dO load not yet
+          if (!(ok = wait1(do_empty + sd, ((qs / NSD) & 1) ^ 1))) break;
+          tc::mbar_arrive_expect_tx(do_full + sd, TILE + kB * 4);
           for (int c = 0; c < NCH; ++c)
             tc::tma_load_3d(sDO + sd * TILE + c * kChunk, &tm_do, do_full + sd, c * 64, h, qrow);
           tc::bulk_load(sLSE + sd * kB, p.lse + vec, kB * 4, do_full + sd);
-          tc::bulk_load(sDv + sd * kB, p.dvec + vec, kB * 4, do_full + sd);
+          nq_half = 0;
+          ++qs;
         }
-        __syncwarp();
-        nq_half = 0;
-        ++qs;
       }
-    }
-    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
-      volatile int never = 0;
-      if (nk > 0) tc::mbar_wait(kv_full, (nk - 1) & 1, &never, &g_status_bwd, 100000000ull);
-      const int nq = qs + nq_half;  // Q loads issued
-      for (int j = (nq > NSQ ? nq - NSQ : 0); j < nq; ++j)
-        tc::mbar_wait(q_full + (j % NSQ), (j / NSQ) & 1, &never, &g_status_bwd, 100000000ull);
-      for (int j = (qs > NSD ? qs - NSD : 0); j < qs; ++j)
-        tc::mbar_wait(do_full + (j % NSD), (j / NSD) & 1, &never, &g_status_bwd, 100000000ull);
+      if (*abort_flag) {  // let the copies already issued land before the CTA exits
+        volatile int never = 0;
+        if (nk > 0) tc::mbar_wait(kv_full, (nk - 1) & 1, &never, &g_status_bwd, 100000000ull);
+        const int nq = qs + nq_half;  // Q loads issued
+        for (int j = (nq > NSQ ? nq - NSQ : 0); j < nq; ++j)
+          tc::mbar_wait(q_full + (j % NSQ), (j / NSQ) & 1, &never, &g_status_bwd, 100000000ull);
+        for (int j = (qs > NSD ? qs - NSD : 0); j < qs; ++j)
+          tc::mbar_wait(do_full + (j % NSD), (j / NSD) & 1, &never, &g_status_bwd, 100000000ull);
+      }
     }
     __syncwarp();
   } else if (warp == kWMma) {
@@ -475,21 +465,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kB / 16; ++kk)  // dV += P^T dO, P^T packed bf16 in A_t
           mma_ts(tmem + T_DV, packed_a(A, 0, kk), dDOm + sod + ((kk * 2048) >> 4), idesc_kv,
                  (t > 0 || kk > 0) ? 1u : 0u);
+        // dO(t) was last read by dV(t), its LSE before P^T(t) was published:
+        // the stage is free once the MMAs issued so far are
+        tc::mma_commit(do_empty + sd);
         // dV(t) keeps the tensor pipe busy while dP^T(t) is read out of B_t
         if (t + 1 < n) {
           if (!(ok = wait1(dp_free, gs & 1))) break;
           if (!(ok = issue_s(gs + 1))) break;
         }
         if (!(ok = wait1(ds_ready, gs & 1))) break;
-        // dO(t) was last read by dV(t), and the compute threads are done with
-        // its LSE and D: the stage is free once the MMAs issued so far are
-        tc::mma_commit(do_empty + sd);
         tc::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kB / 16; ++kk)  // dK += dS^T Q, dS^T packed bf16 in A_t
           mma_ts(tmem + T_DK, packed_a(A, 16, kk), dQm + soq + ((kk * 2048) >> 4), idesc_kv,
                  (t > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_commit(q_empty + sq);
+        tc::mma_commit(q_empty + sq);  // Q(t) read by S^T(t) and dK(t), its D before dS^T(t)
         if (t + 1 < n) {
           if (!(ok = issue_dp(gs + 1))) break;
           if (t + 2 == n) commit(kv_empty);
@@ -544,13 +534,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Ej = (j < n_tok) ? p.subtree_end[krow + r] : -1;
       int entry = I.list[I.s0 % I.n_col];
       for (int t = 0; t < I.n; ++t) {
-        const int gs = qs + t, st = gs % NSD;  // LSE and D sit in the dO stage
+        const int gs = qs + t, st = gs % NSD, sq = gs % NSQ;  // LSE sits in the dO stage, D in the Q stage
         const int qb = entry >> 1;
         const bool full = entry & 1;
         if (t + 1 < I.n) entry = I.list[(I.s0 + t + 1) % I.n_col];
         const uint32_t tA = tmem + lane_base + reg_s(gs) + kCW * w;      // S^T, then P^T | dS^T
         const uint32_t tB = tmem + lane_base + reg_s(gs + 1) + kCW * w;  // dP^T
-        if (!wait_u(do_full + st, (gs / NSD) & 1) || !wait_u(s_full, gs & 1)) { ok = false; break; }
+        if (!wait_u(do_full + st, (gs / NSD) & 1) || !wait_u(q_full + sq, (gs / NSQ) & 1) ||
+            !wait_u(s_full, gs & 1)) {
+          ok = false;
+          break;
+        }
         tc::tc_fence_after();
         // ---- P^T = exp2(S * scale*log2e - LSE*log2e) on this group's 32 query columns
         float pf[kCW];
@@ -600,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld_wait();
           tc::tc_fence_before();
           tc::mbar_arrive(dp_free);  // B_t may take S^T of the next step now
-          const float4* d4 = reinterpret_cast<const float4*>(sDv + st * kB + kCW * w);
+          const float4* d4 = reinterpret_cast<const float4*>(sDv + sq * kB + kCW * w);
           uint32_t dw[kCW / 2];
 #pragma unroll
           for (int c4 = 0; c4 < kCW / 4; ++c4) {  // packed pairs: P (dP - D)
@@ -796,13 +790,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWTma) {
     // ------------------------------------------------------------ producer
+    // One thread runs the whole loop, like the MMA issuer: a warp-level sync
+    // right after the bulk copies would hold the warp until they are issued.
     if (tc::elect_one()) {
-      tc::tma_prefetch_desc(&tm_q);
-      tc::tma_prefetch_desc(&tm_k);
-      tc::tma_prefetch_desc(&tm_v);
-      tc::tma_prefetch_desc(&tm_do);
-    }
-    __syncwarp();
+    tc::tma_prefetch_desc(&tm_q);
+    tc::tma_prefetch_desc(&tm_k);
+    tc::tma_prefetch_desc(&tm_v);
+    tc::tma_prefetch_desc(&tm_do);
+    auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
     int gk = 0, gv = 0, nq = 0;  // K tiles, V tiles and Q tiles loaded so far
     bool ok = true;
     // Slot k of the ring gets the k-th item this CTA takes, decoded (index or
@@ -810,23 +805,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // entry), so that no consumer reads the CSR at an item boundary.  Item
     // k + 1 is published while item k's tiles are still being loaded.
     auto take = [&](int k, DqItem& I) -> int {  // -2: aborted
-      if (!wait_u(item_empty + (k % kNIR), ((k / kNIR) & 1) ^ 1)) return -2;
-      uint32_t u = 0;
-      if ((threadIdx.x & 31) == 0) u = atomicAdd(p.sched + 4, 1u);
-      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!wait1(item_empty + (k % kNIR), ((k / kNIR) & 1) ^ 1)) return -2;
+      const uint32_t u = atomicAdd(p.sched + 4, 1u);
       const int it = u < uint32_t(p.dq_items) ? int(u) : -1;  // unsigned: no index below 0
       I.n = 0;
       if (it >= 0) I = decode_dq(p, it);
       const int first = I.n > 0 ? I.list[0] : 0;
-      if (tc::elect_one()) {
-        volatile int* slot = item_ring + 4 * (k % kNIR);
-        slot[0] = it;
-        slot[1] = I.n;
-        slot[2] = it >= 0 ? I.e0 : 0;
-        slot[3] = first;
-        tc::mbar_arrive(item_full + (k % kNIR));
-      }
-      __syncwarp();
+      volatile int* slot = item_ring + 4 * (k % kNIR);
+      slot[0] = it;
+      slot[1] = I.n;
+      slot[2] = it >= 0 ? I.e0 : 0;
+      slot[3] = first;
+      tc::mbar_arrive(item_full + (k % kNIR));
       return it;
     };
     DqItem I, J;
@@ -836,57 +826,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = I.h / G;
       if (I.n > 0) {
         const int row0 = I.b * p.t_pad + I.qb * kB;
-        if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
-        if (tc::elect_one()) {
-          tc::mbar_arrive_expect_tx(q_full, 2 * TILE);
-          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sQ + c * kChunk, &tm_q, q_full, c * 64, I.h, row0);
-          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sDO + c * kChunk, &tm_do, q_full, c * 64, I.h, row0);
-        }
-        __syncwarp();
+        if (!(ok = wait1(q_empty, (nq & 1) ^ 1))) break;
+        tc::mbar_arrive_expect_tx(q_full, 2 * TILE);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sQ + c * kChunk, &tm_q, q_full, c * 64, I.h, row0);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sDO + c * kChunk, &tm_do, q_full, c * 64, I.h, row0);
         ++nq;
       }
       const int jt = take(k + 1, J);
       ok = jt != -2;
       if (!ok) break;
-      if (jt >= 0 && J.n > 0 && tc::elect_one()) {  // the next item's Q and dO into L2 meanwhile
+      if (jt >= 0 && J.n > 0) {  // the next item's Q and dO into L2 meanwhile
         const int nrow0 = J.b * p.t_pad + J.qb * kB;
         for (int c = 0; c < NCH; ++c) {
           tc::tma_prefetch_3d(&tm_q, c * 64, J.h, nrow0);
           tc::tma_prefetch_3d(&tm_do, c * 64, J.h, nrow0);
         }
       }
-      __syncwarp();
       int entry = I.n > 0 ? I.list[0] : 0;
       for (int j = 0; ok && j < I.n; ++j) {
         const int krow = I.b * p.t_pad + (entry >> 1) * kB;
         if (j + 1 < I.n) entry = I.list[j + 1];
         const int sk = gk % NSK;
-        if (!(ok = wait_u(k_empty + sk, ((gk / NSK) & 1) ^ 1))) break;
-        if (tc::elect_one()) {
-          tc::mbar_arrive_expect_tx(k_full + sk, TILE);
-          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sK + sk * TILE + c * kChunk, &tm_k, k_full + sk, c * 64, g, krow);
-        }
-        __syncwarp();
+        if (!(ok = wait1(k_empty + sk, ((gk / NSK) & 1) ^ 1))) break;
+        tc::mbar_arrive_expect_tx(k_full + sk, TILE);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sK + sk * TILE + c * kChunk, &tm_k, k_full + sk, c * 64, g, krow);
         ++gk;
         const int sv = gv % NSV;
-        if (!(ok = wait_u(v_empty + sv, ((gv / NSV) & 1) ^ 1))) break;
-        if (tc::elect_one()) {
-          tc::mbar_arrive_expect_tx(v_full + sv, TILE);
-          for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sV + sv * TILE + c * kChunk, &tm_v, v_full + sv, c * 64, g, krow);
-        }
-        __syncwarp();
+        if (!(ok = wait1(v_empty + sv, ((gv / NSV) & 1) ^ 1))) break;
+        tc::mbar_arrive_expect_tx(v_full + sv, TILE);
+        for (int c = 0; c < NCH; ++c) tc::tma_load_3d(sV + sv * TILE + c * kChunk, &tm_v, v_full + sv, c * 64, g, krow);
         ++gv;
       }
       I = J;
       it = jt;
     }
-    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
+    if (*abort_flag) {  // let the copies already issued land before the CTA exits
       volatile int never = 0;
       if (nq > 0) tc::mbar_wait(q_full, (nq - 1) & 1, &never, &g_status_bwd, 100000000ull);
       for (int jj = (gk > NSK ? gk - NSK : 0); jj < gk; ++jj)
         tc::mbar_wait(k_full + (jj % NSK), (jj / NSK) & 1, &never, &g_status_bwd, 100000000ull);
       for (int jj = (gv > NSV ? gv - NSV : 0); jj < gv; ++jj)
         tc::mbar_wait(v_full + (jj % NSV), (jj / NSV) & 1, &never, &g_status_bwd, 100000000ull);
+    }
     }
     __syncwarp();
   } else if (warp == kWMma) {
@@ -1284,13 +1265,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
 
   if (warp == kWTma) {
     // ------------------------------------------------------------ producers (both CTAs)
+    // One thread runs the whole loop, like the MMA issuers: a warp-level sync
+    // right after the bulk copies would hold the warp until they are issued.
     if (tc::elect_one()) {
-      tc::tma_prefetch_desc(&tm_q);
-      tc::tma_prefetch_desc(&tm_k64);
-      tc::tma_prefetch_desc(&tm_v64);
-      tc::tma_prefetch_desc(&tm_do);
-    }
-    __syncwarp();
+    tc::tma_prefetch_desc(&tm_q);
+    tc::tma_prefetch_desc(&tm_k64);
+    tc::tma_prefetch_desc(&tm_v64);
+    tc::tma_prefetch_desc(&tm_do);
+    auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
     int gk = 0, gv = 0, nq = 0;
     bool ok = true;
     struct Item {
@@ -1300,10 +1282,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
     // CTAs' rings, one item ahead of the loads.  Odd CTA: reads slot k.
     auto take = [&](int k, Item& I) -> bool {
       const int slot = k % kNIR;
-      if (!wait_u(item_empty + slot, ((k / kNIR) & 1) ^ 1)) return false;
-      uint32_t u = 0;
-      if (lane == 0) u = atomicAdd(p.sched + 4, 1u);
-      u = __shfl_sync(0xffffffffu, u, 0);
+      if (!wait1(item_empty + slot, ((k / kNIR) & 1) ^ 1)) return false;
+      const uint32_t u = atomicAdd(p.sched + 4, 1u);
       I.it = u < uint32_t(p.dq_items) ? int(u) : -1;  // unsigned: no index below 0
       I.n = 0;
       I.e0 = 0;
@@ -1316,30 +1296,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         I.n = rp[qb + 1] - I.e0;
         if (I.n > 0) first = p.q_idx[int64_t(b) * p.cap + I.e0];
       }
-      if (tc::elect_one()) {
-        volatile int* mine = item_ring + 4 * slot;
-        mine[0] = I.it;
-        mine[1] = I.n;
-        mine[2] = I.e0;
-        mine[3] = first;
-        const uint32_t peer = tc::peer_addr(const_cast<int*>(mine), 1);
-        tc::st_cluster_u32(peer, uint32_t(I.it));
-        tc::st_cluster_u32(peer + 4, uint32_t(I.n));
-        tc::st_cluster_u32(peer + 8, uint32_t(I.e0));
-        tc::st_cluster_u32(peer + 12, uint32_t(first));
-        tc::mbar_arrive(item_full + slot);
-        tc::mbar_arrive_release_cluster(tc::peer_addr(item_full + slot, 1));  // after the ring stores
-      }
-      __syncwarp();
+      volatile int* mine = item_ring + 4 * slot;
+      mine[0] = I.it;
+      mine[1] = I.n;
+      mine[2] = I.e0;
+      mine[3] = first;
+      const uint32_t peer = tc::peer_addr(const_cast<int*>(mine), 1);
+      tc::st_cluster_u32(peer, uint32_t(I.it));
+      tc::st_cluster_u32(peer + 4, uint32_t(I.n));
+      tc::st_cluster_u32(peer + 8, uint32_t(I.e0));
+      tc::st_cluster_u32(peer + 12, uint32_t(first));
+      tc::mbar_arrive(item_full + slot);
+      tc::mbar_arrive_release_cluster(tc::peer_addr(item_full + slot, 1));  // after the ring stores
       return true;
     };
     auto read = [&](int k, Item& I) -> bool {
       const int slot = k % kNIR;
-      if (!wait_ring(item_full + slot, (k / kNIR) & 1)) return false;
+      if (!tc::mbar_wait_cluster(item_full + slot, (k / kNIR) & 1, abort_flag, &g_status_bwd)) return false;
       I.it = item_ring[4 * slot];
       I.n = item_ring[4 * slot + 1];
       I.e0 = item_ring[4 * slot + 2];
-      warp_arrive_lead(item_empty + slot);
+      tc::mbar_arrive_remote(tc::peer_addr(item_empty + slot, 0));  // this warp's one arrival
       return true;
     };
     // Q of an item goes into buffer (count of loaded Q tiles) % NSQ; it is
@@ -1349,15 +1326,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
       int xb, xhp, xqb;
       dq2_coords(p, X.it, xb, xhp, xqb);
       const int qs = nq % NSQ;
-      if (!wait_u(q_empty + qs, ((nq / NSQ) & 1) ^ 1)) return false;
-      if (tc::elect_one()) {
-        if (lead) tc::mbar_arrive_expect_tx(q_full + qs, 2 * TILE);  // Q of both CTAs
-        const uint32_t lb = tc::peer_addr(q_full + qs, 0);
-        for (int c = 0; c < 2; ++c)
-          tc::tma_load_3d_pair(sQ + qs * TILE + c * kChunk, &tm_q, lb, c * 64, 2 * xhp + int(crank),
-                               xb * p.t_pad + xqb * kB);
-      }
-      __syncwarp();
+      if (!wait1(q_empty + qs, ((nq / NSQ) & 1) ^ 1)) return false;
+      if (lead) tc::mbar_arrive_expect_tx(q_full + qs, 2 * TILE);  // Q of both CTAs
+      const uint32_t lb = tc::peer_addr(q_full + qs, 0);
+      for (int c = 0; c < 2; ++c)
+        tc::tma_load_3d_pair(sQ + qs * TILE + c * kChunk, &tm_q, lb, c * 64, 2 * xhp + int(crank),
+                             xb * p.t_pad + xqb * kB);
       ++nq;
       return true;
     };
@@ -1374,26 +1348,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
       // this item should not wait behind that.
       auto load_do_and_next = [&]() -> bool {
         if (I.n > 0) {
-          if (!wait_u(do_empty, (nd & 1) ^ 1)) return false;
-          if (tc::elect_one()) {
-            if (lead) tc::mbar_arrive_expect_tx(do_full, 2 * TILE);  // dO of both CTAs
-            const uint32_t lb = tc::peer_addr(do_full, 0);
-            for (int c = 0; c < 2; ++c)
-              tc::tma_load_3d_pair(sDO + c * kChunk, &tm_do, lb, c * 64, h, b * p.t_pad + qb * kB);
-          }
-          __syncwarp();
+          if (!wait1(do_empty, (nd & 1) ^ 1)) return false;
+          if (lead) tc::mbar_arrive_expect_tx(do_full, 2 * TILE);  // dO of both CTAs
+          const uint32_t lb = tc::peer_addr(do_full, 0);
+          for (int c = 0; c < 2; ++c)
+            tc::tma_load_3d_pair(sDO + c * kChunk, &tm_do, lb, c * 64, h, b * p.t_pad + qb * kB);
           ++nd;
         }
         if (!(lead ? take(k + 1, J) : read(k + 1, J))) return false;
         if (J.it >= 0 && J.n > 0) {
           if (!load_q(J)) return false;
-          if (tc::elect_one()) {  // and its dO into L2 for when the buffer frees
-            int nb, nhp, nqb;
-            dq2_coords(p, J.it, nb, nhp, nqb);
-            for (int c = 0; c < 2; ++c)
-              tc::tma_prefetch_3d(&tm_do, c * 64, 2 * nhp + int(crank), nb * p.t_pad + nqb * kB);
-          }
-          __syncwarp();
+          int nb, nhp, nqb;  // and its dO into L2 for when the buffer frees
+          dq2_coords(p, J.it, nb, nhp, nqb);
+          for (int c = 0; c < 2; ++c)
+            tc::tma_prefetch_3d(&tm_do, c * 64, 2 * nhp + int(crank), nb * p.t_pad + nqb * kB);
         }
         return true;
       };
@@ -1404,8 +1372,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         const int krow = b * p.t_pad + (entry >> 1) * kB;
         if (j + 1 < I.n) entry = list[j + 1];
         const int sk = gk % NSK;
-        if (!(ok = wait_u(k_empty + sk, ((gk / NSK) & 1) ^ 1))) break;
-        if (tc::elect_one()) {
+        if (!(ok = wait1(k_empty + sk, ((gk / NSK) & 1) ^ 1))) break;
+        {
           if (lead) tc::mbar_arrive_expect_tx(k_full + sk, 2 * KST);
           const uint32_t lb = tc::peer_addr(k_full + sk, 0);
           uint8_t* st = sK + sk * KST;
@@ -1415,11 +1383,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
           tc::tma_load_3d_pair(st + 2 * PIECE, &tm_k64, lb, 64 * int(crank), g, krow);       // keys 0-63
           tc::tma_load_3d_pair(st + 3 * PIECE, &tm_k64, lb, 64 * int(crank), g, krow + 64);  // keys 64-127
         }
-        __syncwarp();
         ++gk;
         const int sv = gv % NSV;
-        if (!(ok = wait_u(v_empty + sv, ((gv / NSV) & 1) ^ 1))) break;
-        if (tc::elect_one()) {
+        if (!(ok = wait1(v_empty + sv, ((gv / NSV) & 1) ^ 1))) break;
+        {
           if (lead) tc::mbar_arrive_expect_tx(v_full + sv, 2 * VST);
           const uint32_t lb = tc::peer_addr(v_full + sv, 0);
           uint8_t* st = sV + sv * VST;
@@ -1427,7 +1394,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
           tc::tma_load_3d_pair(st, &tm_v64, lb, 0, g, mine);
           tc::tma_load_3d_pair(st + PIECE, &tm_v64, lb, 64, g, mine);
         }
-        __syncwarp();
         ++gv;
         if (j == 0 && !(ok = load_do_and_next())) break;
       }
@@ -1438,6 +1404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
       const long long t0 = clock64();  // give any still in flight time to land before the CTA leaves
       while (clock64() - t0 < 400000) {
       }
+    }
     }
     __syncwarp();
   } else if (warp == kWMma) {

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);  // [2]
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int hkv_group = p.hq / p.hkv;
   constexpr int W_TMA = 4 * NH, W_MMA = 4 * NH + 1;
 
@@ -198,74 +198,60 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Issuer warps run converged (waits, counters and descriptors stay
-  // warp-uniform); the elected lane alone issues each copy, MMA and commit.
-  auto wait_u = [&](uint64_t* b_, uint32_t par) {
-    return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_fwd));
-  };
   if (warp == W_TMA) {
     // ------------------------------------------------------------ producer
+    // One thread runs the whole loop, like the MMA issuer: a warp-level sync
+    // right after the bulk copies would hold the warp until they are issued.
     if (tc::elect_one()) {
       tc::tma_prefetch_desc(&tm_q);
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
-    }
-    __syncwarp();
-    int kt = 0, vt = 0, nq = 0;  // ring counters and non-empty items so far
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      // fetch the next work item and hand it to the other roles
-      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
-      uint32_t u = 0;
-      if (lane == 0) u = atomicAdd(p.sched, 1u);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      const int it = u < uint32_t(p.n_items) ? int(u) : -1;  // unsigned: no index below 0
-      if (tc::elect_one()) {
+      auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_fwd); };
+      int kt = 0, vt = 0, nq = 0;  // ring counters and non-empty items so far
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        // fetch the next work item and hand it to the other roles
+        if (!(ok = wait1(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+        const uint32_t u = atomicAdd(p.sched, 1u);
+        const int it = u < uint32_t(p.n_items) ? int(u) : -1;  // unsigned: no index below 0
         item_ring[k & 1] = it;
         tc::mbar_arrive(item_full + (k & 1));
-      }
-      __syncwarp();
-      if (it < 0) break;
-      const Item I = decode_item<NH>(p, it);
-      if (I.n_it == 0) continue;
-      const int32_t* list = p.q_idx + int64_t(I.b) * p.cap + I.e0;
-      const int g = I.h0 / hkv_group;
-      if (!(ok = wait_u(q_empty, (nq & 1) ^ 1))) break;
-      if (tc::elect_one()) {
+        if (it < 0) break;
+        const Item I = decode_item<NH>(p, it);
+        if (I.n_it == 0) continue;
+        const int32_t* list = p.q_idx + int64_t(I.b) * p.cap + I.e0;
+        const int g = I.h0 / hkv_group;
+        if (!(ok = wait1(q_empty, (nq & 1) ^ 1))) break;
         tc::mbar_arrive_expect_tx(q_full, NH * TILE);
         for (int h = 0; h < NH; ++h)
           for (int c = 0; c < NCH; ++c)
             tc::tma_load_3d(sQ + h * TILE + c * kChunk, &tm_q, q_full, c * 64, I.h0 + h, I.b * p.t_pad + I.qb * kB);
-      }
-      __syncwarp();
-      // K runs ahead of V by one tile: the MMA needs K(j+1) before V(j).
-      int kj = 0, vj = 0;
-      while (kj < I.n_it || vj < I.n_it) {
-        const bool do_k = kj < I.n_it && kj <= vj + 1;
-        const int j = do_k ? kj : vj;
-        const int krow = I.b * p.t_pad + (list[j] >> 1) * kB;
-        const int gx = (do_k ? kt : vt) + j, s = gx % NS;
-        if (!(ok = wait_u((do_k ? k_empty : v_empty) + s, ((gx / NS) & 1) ^ 1))) break;
-        if (tc::elect_one()) {
+        // K runs ahead of V by one tile: the MMA needs K(j+1) before V(j).
+        int kj = 0, vj = 0;
+        while (kj < I.n_it || vj < I.n_it) {
+          const bool do_k = kj < I.n_it && kj <= vj + 1;
+          const int j = do_k ? kj : vj;
+          const int krow = I.b * p.t_pad + (list[j] >> 1) * kB;
+          const int gx = (do_k ? kt : vt) + j, s = gx % NS;
+          if (!(ok = wait1((do_k ? k_empty : v_empty) + s, ((gx / NS) & 1) ^ 1))) break;
           uint64_t* fb = (do_k ? k_full : v_full) + s;
           uint8_t* dst = (do_k ? sK : sV) + s * TILE;
           tc::mbar_arrive_expect_tx(fb, TILE);
           for (int c = 0; c < NCH; ++c)
             tc::tma_load_3d(dst + c * kChunk, do_k ? &tm_k : &tm_v, fb, c * 64, g, krow);
+          if (do_k) ++kj; else ++vj;
         }
-        __syncwarp();
-        if (do_k) ++kj; else ++vj;
+        kt += kj;
+        vt += vj;
+        ++nq;
       }
-      kt += kj;
-      vt += vj;
-      ++nq;
-    }
-    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
-      volatile int never = 0;
-      for (int j = (kt > NS ? kt - NS : 0); j < kt; ++j)
-        tc::mbar_wait(k_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
-      for (int j = (vt > NS ? vt - NS : 0); j < vt; ++j)
-        tc::mbar_wait(v_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
+      if (*abort_flag) {  // let the copies already issued land before the CTA exits
+        volatile int never = 0;
+        for (int j = (kt > NS ? kt - NS : 0); j < kt; ++j)
+          tc::mbar_wait(k_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
+        for (int j = (vt > NS ? vt - NS : 0); j < vt; ++j)
+          tc::mbar_wait(v_full + (j % NS), (j / NS) & 1, &never, &g_status_fwd, 100000000ull);
+      }
     }
     __syncwarp();
   } else if (warp == W_MMA) {
