@@ -1703,7 +1703,20 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   const int lane = threadIdx.x & 31;
   const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
   const int64_t n_pass = (n_rows + RPW - 1) / RPW;
+  // When a pass's RPW rows are heads of one token (Hq a multiple of RPW) the
+  // token is found with one 32-bit division a pass and a padding token's rows
+  // are not read at all.
+  const bool tok_pass = hq % RPW == 0 && n_rows < (int64_t(1) << 31);
   for (int64_t ps = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; ps < n_pass; ps += warps) {
+    int pb = 0, pi = 0, ph = 0;
+    bool live = true;
+    if (tok_pass) {
+      const uint32_t r0 = uint32_t(ps * RPW), tok = r0 / uint32_t(hq);
+      pb = int(tok / uint32_t(t_pad));
+      pi = int(tok - uint32_t(pb) * uint32_t(t_pad));
+      ph = int(r0 - tok * uint32_t(hq));
+      live = pi < n_tokens[pb];
+    }
     uint4 va[4], vc[4];
     int64_t row[4];
 #pragma unroll
@@ -1711,7 +1724,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       row[k] = ps * RPW + k * RPL + lane / LPR;
       va[k] = make_uint4(0, 0, 0, 0);
       vc[k] = va[k];
-      if (row[k] < n_rows) {
+      if (row[k] < n_rows && live) {
         va[k] = reinterpret_cast<const uint4*>(o + row[k] * D)[lane % LPR];
         vc[k] = reinterpret_cast<const uint4*>(dout + row[k] * D)[lane % LPR];
       }
@@ -1728,10 +1741,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 #pragma unroll
       for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
       if (lane % LPR == 0 && row[k] < n_rows) {
-        const int h = int(row[k] % hq);
-        const int64_t bt = row[k] / hq;
-        const int b = int(bt / t_pad), i = int(bt % t_pad);
-        dvec[(int64_t(b) * hq + h) * t_pad + i] = (i < n_tokens[b]) ? s : 0.f;
+        if (tok_pass) {
+          const int h = ph + k * RPL + lane / LPR;
+          dvec[(int64_t(pb) * hq + h) * t_pad + pi] = live ? s : 0.f;
+        } else {
+          const int h = int(row[k] % hq);
+          const int64_t bt = row[k] / hq;
+          const int b = int(bt / t_pad), i = int(bt % t_pad);
+          dvec[(int64_t(b) * hq + h) * t_pad + i] = (i < n_tokens[b]) ? s : 0.f;
+        }
       }
     }
   }
