@@ -445,6 +445,17 @@ int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const void* hidden, 
  * kernels: TPA_OK, TPA_ERR_DEVICE_TIMEOUT or TPA_ERR_CUDA. */
 int tpa_sync_status(void* stream);
 
+/* Diagnostic for the bounded waits above: launches one thread on `stream`
+ * that waits on a shared-memory mbarrier with the same clock-bounded wait the
+ * attention kernels use (`limit_ns` in nanoseconds, counted in SM cycles at no
+ * more than 2.1 GHz, so the real bound is at least that long).  arrive != 0:
+ * the thread completes the barrier's phase first and the wait succeeds;
+ * arrive == 0: nothing arrives, the wait runs out and sets the device status
+ * word, so the next tpa_sync_status() returns TPA_ERR_DEVICE_TIMEOUT (and
+ * clears it).  No fault or hang is involved: the kernel returns either way.
+ * Errors: TPA_ERR_INVALID_ARG (limit_ns 0 or above 10 s), TPA_ERR_CUDA. */
+int tpa_wait_probe(uint64_t limit_ns, int32_t arrive, void* stream);
+
 /* TPA_OK when the current CUDA device is compute capability 10.3 (sm_103),
  * TPA_ERR_UNSUPPORTED_DEVICE otherwise, TPA_ERR_CUDA without a device. */
 int tpa_device_check(void);

@@ -22,5 +22,5 @@ from .api import (  # noqa: F401
     BlockMask, DeviceTree, Tree, balance, block_classify, dense_mask, device_check, extract_sequences,
     lm_head_logprobs_entropy, lm_head_workspace_bytes, packing_metrics, sync_status, tree_attn_bwd,
     tree_pack_padded,
-    tree_attn_bwd_workspace_bytes, tree_attn_fwd, tree_logprobs_entropy, tree_pack,
+    tree_attn_bwd_workspace_bytes, tree_attn_fwd, tree_logprobs_entropy, tree_pack, wait_probe,
 )

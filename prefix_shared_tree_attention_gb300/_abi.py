@@ -99,6 +99,7 @@ PROTOTYPES = {
                                                C.c_void_p, C.c_void_p]),
     "tpa_sync_status": (C.c_int, [C.c_void_p]),
     "tpa_device_check": (C.c_int, []),
+    "tpa_wait_probe": (C.c_int, [C.c_uint64, C.c_int32, C.c_void_p]),
     "tpa_status_string": (C.c_char_p, [C.c_int]),
     "tpa_version": (C.c_int, []),
 }

@@ -365,5 +365,12 @@ def sync_status(stream=None) -> None:
     check("tpa_sync_status", lib().tpa_sync_status(_stream_ptr(stream)))
 
 
+def wait_probe(limit_ns: int, arrive: bool, stream=None) -> None:
+    """Launch the bounded-wait diagnostic (tpa_wait_probe): with ``arrive``
+    False its one wait runs out after about ``limit_ns`` and the next
+    ``sync_status`` raises TPA_ERR_DEVICE_TIMEOUT."""
+    check("tpa_wait_probe", lib().tpa_wait_probe(int(limit_ns), 1 if arrive else 0, _stream_ptr(stream)))
+
+
 def device_check() -> None:
     check("tpa_device_check", lib().tpa_device_check())

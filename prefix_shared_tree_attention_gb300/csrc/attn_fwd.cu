@@ -566,9 +566,31 @@ int launch_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   return launch_fwd_cfg<D, 1>(tq, tk, tv, to, prm, tree->n_trees, st);
 }
 
+// One thread waits on an mbarrier with the bounded wait every role of the
+// attention kernels uses.  arrive != 0: the thread completes the phase itself
+// first, so the wait succeeds; arrive == 0: nothing arrives, the wait gives up
+// after about limit_ns, raises the abort flag and sets the device status word.
+__global__ void wait_probe_kernel(uint64_t limit_ns, int arrive) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  tc::mbar_init(&bar, 1);
+  tc::fence_mbar_init();
+  if (arrive) tc::mbar_arrive(&bar);
+  (void)tc::mbar_wait(&bar, 0, &abort_flag, &g_status_fwd, limit_ns);
+}
+
 }  // namespace
 
 TPA_DEFINE_STATUS_READER(tpa_internal_status_fwd, g_status_fwd)
+
+extern "C" int tpa_wait_probe(uint64_t limit_ns, int32_t arrive, void* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return TPA_ERR_INVALID_ARG;
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, arrive);
+  TPA_CUDA_TRY(cudaGetLastError());
+  return TPA_OK;
+}
 
 int tpa_internal_check_attn_args(const tpa_tree_view* tree, const tpa_blockmask_view* mask, int hq,
                                  int hkv, int d) {
