@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int G = p.hq / p.hkv;
   constexpr uint32_t T_DV = 256, T_DK = 256 + D;
-  constexpr int NCONS = 1 + 128 * kNWG;  // item consumers: MMA warp (elected lane) + compute threads
+  constexpr int NCONS = 1 + 4 * kNWG;  // item consumers: MMA warp (elected lane) + one per compute warp
   // region holding S^T of global step gs (dP^T goes to the other one)
   auto reg_s = [](int gs) -> uint32_t { return (gs & 1) ? 128u : 0u; };
 
@@ -299,11 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(s_full, 1);
     tc::mbar_init(dp_full, 1);
-    tc::mbar_init(p_ready, 128 * kNWG);
-    tc::mbar_init(dp_free, 128 * kNWG);
-    tc::mbar_init(ds_ready, 128 * kNWG);
+    // compute-side barriers take one arrival per warp (after __syncwarp): 512
+    // single-thread arrivals on one barrier word would queue up
+    tc::mbar_init(p_ready, 4 * kNWG);
+    tc::mbar_init(dp_free, 4 * kNWG);
+    tc::mbar_init(ds_ready, 4 * kNWG);
     tc::mbar_init(acc_full, 1);
-    tc::mbar_init(acc_free, 128 * kNWG);
+    tc::mbar_init(acc_free, 4 * kNWG);
     tc::mbar_init(drain, 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(item_full + s, 1);
@@ -326,6 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   auto wait_u = [&](uint64_t* b_, uint32_t par) {
     return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_bwd));
+  };
+  // one arrival for the warp, after every lane's own fences and stores
+  auto warp_arrive = [&](uint64_t* b_) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(b_);
   };
 
   if (warp == kWTma) {
@@ -509,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; ok; ++k) {
       if (!wait_u(item_full + (k & 1), (k >> 1) & 1)) break;
       const int it = item_ring[k & 1];
-      tc::mbar_arrive(item_empty + (k & 1));
+      warp_arrive(item_empty + (k & 1));
       if (it < 0) break;
       const KvItem I = decode_kv(p, it);
       const int krow = I.b * p.t_pad + I.kb * kB;
@@ -584,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st_wait();
         }
         tc::tc_fence_before();
-        tc::mbar_arrive(p_ready);
+        warp_arrive(p_ready);
         // ---- dS^T = P^T (dP^T - D)
         if (!wait_u(dp_full, gs & 1)) { ok = false; break; }
         tc::tc_fence_after();
@@ -593,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld32(tB, dpv);
           tc::tmem_ld_wait();
           tc::tc_fence_before();
-          tc::mbar_arrive(dp_free);  // B_t may take S^T of the next step now
+          warp_arrive(dp_free);  // B_t may take S^T of the next step now
           const float4* d4 = reinterpret_cast<const float4*>(sDv + sq * kB + kCW * w);
           uint32_t dw[kCW / 2];
 #pragma unroll
@@ -616,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st_wait();
         }
         tc::tc_fence_before();
-        tc::mbar_arrive(ds_ready);
+        warp_arrive(ds_ready);
       }
       if (!ok || !wait_u(acc_full, nk & 1)) { ok = false; break; }
       if (nk == 0) tc::grid_wait_prior();  // rows the preprocess zeroed are added into
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, p.scale, add, p.wide);
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(acc_free);
+      warp_arrive(acc_free);
       qs += I.n;
       ++nk;
     }
