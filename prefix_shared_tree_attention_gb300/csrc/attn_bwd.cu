@@ -31,8 +31,11 @@
 //      two SMs of a TPC with M = 256 MMAs (cta_group::2), each SM holding
 //      half of every B operand.
 // Both main kernels are persistent: one CTA per SM takes items from a counter
-// in the block-mask buffer, barrier phases run on across items, and the issuer
-// warps run converged with an elected lane issuing each copy, MMA and commit.
+// in the block-mask buffer and barrier phases run on across items.  The TMA
+// producer and MMA issuer warps run their whole loops on one elected thread:
+// a warp-level sync right after tcgen05.mma holds the warp until the queued
+// MMAs have entered the tensor pipe, which would leave the pipe idle for the
+// length of every wait between MMA groups.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

@@ -20,14 +20,15 @@
 //                     O is rescaled in TMEM only when the running max grows
 //                     by more than 2^8 (exact: numerator and denominator keep
 //                     the same stale max).
-//   warp 4*NH         TMA producer: Q of each item, then K and V tiles through
-//                     separate rings.
+//   warp 4*NH         TMA producer (one thread): Q of each item, then K and V
+//                     tiles through separate rings.
 //   warp 4*NH+1       MMA issuer (one thread).  Per key tile j and head h:
 //                     PV_h(j) then S_h(j+1), so head B's softmax runs while
 //                     head A's MMAs run (ping-pong) and the tensor core always
 //                     has the other head's work queued.
 // TMEM columns: S_h [128h, 128h+128) (P_h aliased on its first 64 columns),
-// O_h [128 NH + 128h, ...).
+// O_h [128 NH + 128h, ...).  O / l leaves through a 16 KB swizzled shared-
+// memory stage per head and bulk tensor stores.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
