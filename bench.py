@@ -308,8 +308,11 @@ def run_gpu(args, rank, world, local):
     logits = make_logits(4, rows, V, device=str(dev)) if run_lp else None
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
-    dq, dk, dv = (torch.empty(x.shape, dtype=torch.float32, device=dev) for x in (q, k, v))
-    ws = torch.empty(tpa.tree_attn_bwd_workspace_bytes(B, T, Hq, d), dtype=torch.uint8, device=dev)
+    # gradients in the dtype the workload fixes (bf16, as q/k/v); --grad-dtype fp32 times the
+    # fp32-output path, which splits long key columns into items that add into zeroed rows
+    gdt = torch.float32 if args.grad_dtype == "fp32" else torch.bfloat16
+    dq, dk, dv = (torch.empty(x.shape, dtype=gdt, device=dev) for x in (q, k, v))
+    ws = torch.empty(tpa.tree_attn_bwd_workspace_bytes(B, T, Hq, d, gdt), dtype=torch.uint8, device=dev)
     N = info.total_seq_tokens
     lp_out = (torch.empty((B, T), dtype=torch.float32, device=dev), torch.empty((B, T), dtype=torch.float32, device=dev),
               torch.empty(N, dtype=torch.float32, device=dev), torch.empty(N, dtype=torch.float32, device=dev))
@@ -324,7 +327,7 @@ def run_gpu(args, rank, world, local):
             tpa.tree_attn_fwd(dtree, mask, q, k, v, out=o, lse=lse)
         if ev: ev[2].record(stream)
         if run_attn:
-            tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv))
+            tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv), grad_dtype=gdt)
         if ev: ev[3].record(stream)
         if run_lp:
             tpa.tree_logprobs_entropy(dtree, logits, out=lp_out)
@@ -450,7 +453,7 @@ def run_gpu(args, rank, world, local):
                 lg_ready.record(side)
             tpa.block_classify(dt, out=mask)
             tpa.tree_attn_fwd(dt, mask, q, k, v, out=o, lse=lse)
-            tpa.tree_attn_bwd(dt, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv))
+            tpa.tree_attn_bwd(dt, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv), grad_dtype=gdt)
             for h_, d_ in zip(out_host, (o, dq, dk, dv)):
                 h_.copy_(d_, non_blocking=True)
             torch.cuda.current_stream(dev).wait_event(lg_ready)
@@ -557,7 +560,8 @@ def run_gpu(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "n_trees": B, "tree_tokens": rows, "original_tokens": int(N),
                    "tree_token_ratio": info.tree_token_ratio, "ancestor_pairs": pairs,
-                   "flops_per_step": flops_step, "l2": "inputs larger than L2 (129 MB); no flush",
+                   "flops_per_step": flops_step, "grad_dtype": args.grad_dtype,
+                   "l2": "inputs larger than L2 (129 MB); no flush",
                    "parallelism": (f"trees split over {world} ranks by KK balancing of ancestor pairs"
                                    if world > 1 else "single GPU")},
         "tree_tokens_per_s": job_rows / (ms_step / 1e3),
@@ -587,6 +591,8 @@ def main():
     ap.add_argument("--lm-head-hidden", type=int, default=4096,
                     help="hidden size of the fused LM-head measurement (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--grad-dtype", choices=["bf16", "fp32"], default="bf16",
+                    help="dtype of dQ, dK, dV (bf16 as the workload's tensors; fp32 for the split-column path)")
     ap.add_argument("--oracle-pairs", type=int, default=15000000,
                     help="ancestor pairs in the oracle's bounded sample")
     ap.add_argument("--only", choices=["all", "attn", "logprobs"], default="all",

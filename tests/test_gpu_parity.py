@@ -234,8 +234,9 @@ def test_attention_deterministic_forward(tpa):
 
 # ---------------------------------------------------------------- attention, full-size workloads (sampled)
 
-@pytest.mark.parametrize("cid", [2, 3, 5])
-def test_attention_workload_sampled(tpa, cid):
+@pytest.mark.parametrize("cid,grad", [(2, "fp32"), (3, "fp32"), (5, "fp32"), (2, "bf16")])
+def test_attention_workload_sampled(tpa, cid, grad):
+    # (2, "bf16") is the configuration bench.py times: bf16 gradients, one item per key column
     cfg, seqs = workload(cid)
     T = cfg.max_tokens_per_mb
     pk = oracle.tree_pack(seqs, T)
@@ -243,8 +244,10 @@ def test_attention_workload_sampled(tpa, cid):
     q, k, v, do = workload_tensors(cid, tree.n_trees, T)
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = tpa.tree_attn_fwd(dtree, mask, qd, kd, vd)
-    dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, qd, kd, vd, o, lse, dod)
+    gdt = torch.bfloat16 if grad == "bf16" else torch.float32
+    dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, qd, kd, vd, o, lse, dod, grad_dtype=gdt)
     tpa.sync_status()
+    close = assert_attn_close_bf16_out if grad == "bf16" else assert_attn_close
     trees = [0, pk.n_trees - 1] if pk.n_trees > 1 else [0]
     for b in trees:
         t = pk.trees[b]
@@ -256,9 +259,9 @@ def test_attention_workload_sampled(tpa, cid):
         assert_attn_close(lse[b].cpu()[:, rows], L[:, rows], f"cfg{cid} LSE tree {b}", max_abs=2e-3, rel_l2=1e-4)
         dQ, dK, dV = oracle.attn_backward(t, q[b], k[b], v[b], do[b], t_pad=T, nodes=leaves)
         lrows = node_rows(t, leaves)
-        assert_attn_close(dq[b].cpu()[lrows], dQ[lrows], f"cfg{cid} dQ tree {b}")
-        assert_attn_close(dk[b].cpu()[lrows], dK[lrows], f"cfg{cid} dK tree {b}")
-        assert_attn_close(dv[b].cpu()[lrows], dV[lrows], f"cfg{cid} dV tree {b}")
+        close(dq[b].cpu()[lrows], dQ[lrows], f"cfg{cid} {grad} dQ tree {b}")
+        close(dk[b].cpu()[lrows], dK[lrows], f"cfg{cid} {grad} dK tree {b}")
+        close(dv[b].cpu()[lrows], dV[lrows], f"cfg{cid} {grad} dV tree {b}")
         assert torch.all(o[b, t.n:] == 0) and torch.all(dk[b, t.n:] == 0)
 
 
