@@ -81,7 +81,15 @@ struct FwdCfg {
   static constexpr int NBAR = 2 + 4 * NS + 5 * NH + 2 + 4;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 32 + 1024;  // + alignment slack
-  static constexpr int THREADS = 128 * NH + 64;
+  // Two heads: three full warpgroups (the third holds the TMA and MMA warps and
+  // two idle ones) so that registers can move between warpgroups: launched at
+  // REG_LAUNCH a thread, the producer/issuer warpgroup drops to REG_LOW and the
+  // softmax warpgroups rise to REG_HIGH, within what the CTA was launched with
+  // (at 168 the softmax spilled; its code fits in 184 and the producer's and
+  // issuer's in 120).
+  static constexpr int THREADS = NH == 2 ? 384 : 128 * NH + 64;
+  static constexpr int REG_LAUNCH = 168, REG_LOW = 120, REG_HIGH = 184;
+  static_assert(NH != 2 || REG_HIGH * 256 + REG_LOW * 128 <= REG_LAUNCH * 384, "register split");
   static constexpr uint32_t TMEM_COLS = NH == 2 ? 512 : 256;
   static_assert(NS >= 1, "shared memory too small");
   static_assert(BYTES <= kSmemMax, "shared memory budget");
@@ -199,6 +207,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp >= W_TMA) {
+  // the producer/issuer warpgroup gives registers to the softmax warpgroups
+  // (all four of its warps execute this; two of them have no role)
+  if constexpr (NH == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_LOW));
   if (warp == W_TMA) {
     // ------------------------------------------------------------ producer
     // One thread runs the whole loop, like the MMA issuer: a warp-level sync
@@ -340,7 +352,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
     }
     }
     __syncwarp();
+  }
   } else {
+    if constexpr (NH == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_HIGH));
     // ------------------------------------------------------------ softmax (head h)
     const int h = warp >> 2;
     const int r = threadIdx.x & 127;   // query row within the tile = TMEM lane
@@ -535,6 +549,13 @@ int launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   prm.n_items = prm.n_blk * (prm.hq / NH) * n_trees;
   const int grid = prm.n_items < num_sms() ? prm.n_items : num_sms();
   TPA_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_kernel<D, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES));
+  if constexpr (NH == 2) {
+    // setmaxnreg.inc waits until the warpgroups' registers fit in what the CTA was
+    // launched with: launch only when the kernel was compiled to REG_LAUNCH a thread
+    cudaFuncAttributes fa;
+    TPA_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, NH>));
+    if (fa.numRegs != C::REG_LAUNCH) return TPA_ERR_CUDA;
+  }
   attn_fwd_kernel<D, NH><<<grid, C::THREADS, C::BYTES, st>>>(tq, tk, tv, to, prm);
   TPA_CUDA_TRY(cudaGetLastError());
   return TPA_OK;
