@@ -541,6 +541,10 @@ int num_sms() {
   return sms;
 }
 
+// launch_fwd_cfg<D, 2> returns this (not a library status) when the two-head
+// kernel was not compiled to the register count its setmaxnreg split assumes
+constexpr int kFwdRegsMismatch = 1;
+
 template <int D, int NH>
 int launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                    FwdParams prm,
@@ -552,9 +556,10 @@ int launch_fwd_cfg(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   if constexpr (NH == 2) {
     // setmaxnreg.inc waits until the warpgroups' registers fit in what the CTA was
     // launched with: launch only when the kernel was compiled to REG_LAUNCH a thread
+    // (the caller then runs the one-head kernel instead)
     cudaFuncAttributes fa;
     TPA_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_fwd_kernel<D, NH>));
-    if (fa.numRegs != C::REG_LAUNCH) return TPA_ERR_CUDA;
+    if (fa.numRegs != C::REG_LAUNCH) return kFwdRegsMismatch;
   }
   attn_fwd_kernel<D, NH><<<grid, C::THREADS, C::BYTES, st>>>(tq, tk, tv, to, prm);
   TPA_CUDA_TRY(cudaGetLastError());
@@ -584,7 +589,10 @@ int launch_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.hkv = hkv;
   prm.n_items = 0;
   prm.scale_log2 = scale * kLog2e;
-  if ((hq / hkv) % 2 == 0) return launch_fwd_cfg<D, 2>(tq, tk, tv, to, prm, tree->n_trees, st);
+  if ((hq / hkv) % 2 == 0) {
+    const int rc = launch_fwd_cfg<D, 2>(tq, tk, tv, to, prm, tree->n_trees, st);
+    if (rc != kFwdRegsMismatch) return rc;
+  }
   return launch_fwd_cfg<D, 1>(tq, tk, tv, to, prm, tree->n_trees, st);
 }
 
