@@ -163,45 +163,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWTma) {
     // ------------------------------------------------------------ producer
+    // The producer and the MMA issuer each run their whole loop on one elected
+    // thread: a warp-level sync right after tcgen05.mma (or a bulk copy) holds
+    // the warp until the queued operations have gone out, which would leave
+    // the tensor pipe idle for the length of every wait between k-stages.
     if (tc::elect_one()) {
       tc::tma_prefetch_desc(&tm_h);
       tc::tma_prefetch_desc(&tm_w);
-    }
-    __syncwarp();
-    int q = 0;  // stage loads issued
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
-      uint32_t u = 0;
-      if ((threadIdx.x & 31) == 0) u = atomicAdd(p.ctr, 1u);
-      u = __shfl_sync(0xffffffffu, u, 0);
-      const int it = u < uint32_t(p.n_items) ? int(u) : -1;
-      if (tc::elect_one()) {
+      auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_lmh); };
+      int q = 0;  // stage loads issued
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (!(ok = wait1(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+        const uint32_t u = atomicAdd(p.ctr, 1u);
+        const int it = u < uint32_t(p.n_items) ? int(u) : -1;
         item_ring[k & 1] = it;
         tc::mbar_arrive(item_full + (k & 1));
-      }
-      __syncwarp();
-      if (it < 0) break;
-      const LmhItem I = decode(p, it);
-      const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
-      for (int vt = I.vc * kVt; ok && vt < vt1; ++vt) {
-        for (int kc = 0; kc < n_k; ++kc, ++q) {
-          const int s = q % kStages;
-          if (!(ok = wait_u(empty + s, ((q / kStages) & 1) ^ 1))) break;
-          if (tc::elect_one()) {
+        if (it < 0) break;
+        const LmhItem I = decode(p, it);
+        const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
+        for (int vt = I.vc * kVt; ok && vt < vt1; ++vt) {
+          for (int kc = 0; kc < n_k; ++kc, ++q) {
+            const int s = q % kStages;
+            if (!(ok = wait1(empty + s, ((q / kStages) & 1) ^ 1))) break;
             uint8_t* dst = smem + s * kStage;
             tc::mbar_arrive_expect_tx(full + s, kStage);
             tc::tma_load_3d(dst, &tm_h, full + s, kc * kBK, 0, I.rt * kBM);
             tc::tma_load_3d(dst + kATile, &tm_w, full + s, kc * kBK, 0, vt * kBN);
           }
-          __syncwarp();
         }
       }
-    }
-    if (*abort_flag && tc::elect_one()) {  // let the copies already issued land before the CTA exits
-      volatile int never = 0;
-      for (int j = (q > kStages ? q - kStages : 0); j < q; ++j)
-        tc::mbar_wait(full + (j % kStages), (j / kStages) & 1, &never, &g_status_lmh, 100000000ull);
+      if (*abort_flag) {  // let the copies already issued land before the CTA exits
+        volatile int never = 0;
+        for (int j = (q > kStages ? q - kStages : 0); j < q; ++j)
+          tc::mbar_wait(full + (j % kStages), (j / kStages) & 1, &never, &g_status_lmh, 100000000ull);
+      }
     }
     __syncwarp();
   } else if (warp == kWMma) {
@@ -209,24 +205,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = tc::idesc_bf16(kBM, kBN, false, false);
     const uint64_t dA = tc::smem_desc(tc::smem_u32(smem), 16, 1024);
     const uint64_t dB = tc::smem_desc(tc::smem_u32(smem + kATile), 16, 1024);
-    int q = 0, nt = 0;  // stages consumed, tiles accumulated
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      if (!(ok = wait_u(item_full + (k & 1), (k >> 1) & 1))) break;
-      const int it = item_ring[k & 1];
-      if (tc::elect_one()) tc::mbar_arrive(item_empty + (k & 1));
-      __syncwarp();
-      if (it < 0) break;
-      const LmhItem I = decode(p, it);
-      const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
-      for (int vt = I.vc * kVt; ok && vt < vt1; ++vt, ++nt) {
-        const int ab = nt & 1;
-        if (nt >= 2 && !(ok = wait_u(acc_free + ab, ((nt >> 1) - 1) & 1))) break;
-        for (int kc = 0; kc < n_k; ++kc, ++q) {
-          const int s = q % kStages;
-          if (!(ok = wait_u(full + s, (q / kStages) & 1))) break;
-          tc::tc_fence_after();
-          if (tc::elect_one()) {
+    if (tc::elect_one()) {
+      auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_lmh); };
+      int q = 0, nt = 0;  // stages consumed, tiles accumulated
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        if (!(ok = wait1(item_full + (k & 1), (k >> 1) & 1))) break;
+        const int it = item_ring[k & 1];
+        tc::mbar_arrive(item_empty + (k & 1));
+        if (it < 0) break;
+        const LmhItem I = decode(p, it);
+        const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
+        for (int vt = I.vc * kVt; ok && vt < vt1; ++vt, ++nt) {
+          const int ab = nt & 1;
+          if (nt >= 2 && !(ok = wait1(acc_free + ab, ((nt >> 1) - 1) & 1))) break;
+          for (int kc = 0; kc < n_k; ++kc, ++q) {
+            const int s = q % kStages;
+            if (!(ok = wait1(full + s, (q / kStages) & 1))) break;
+            tc::tc_fence_after();
             const uint32_t so = (s * kStage) >> 4;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
@@ -235,14 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_commit(empty + s);
             if (kc + 1 == n_k) tc::mma_commit(acc_full + ab);
           }
-          __syncwarp();
         }
       }
-    }
-    if (*abort_flag && tc::elect_one()) {  // let issued MMAs finish before TMEM is released
-      volatile int never = 0;
-      tc::mma_commit(drain);
-      tc::mbar_wait(drain, 0, &never, &g_status_lmh, 100000000ull);
+      if (*abort_flag) {  // let issued MMAs finish before TMEM is released
+        volatile int never = 0;
+        tc::mma_commit(drain);
+        tc::mbar_wait(drain, 0, &never, &g_status_lmh, 100000000ull);
+      }
     }
     __syncwarp();
   } else {

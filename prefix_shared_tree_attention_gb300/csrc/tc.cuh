@@ -15,9 +15,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// True in exactly one lane of a converged warp.  Issuer warps run their
-// loops with all lanes (so addresses and descriptors stay warp-uniform) and
-// let the elected lane alone issue each TMA / MMA / commit.
+// True in exactly one lane of a converged warp (elect.sync).  The TMA
+// producers and MMA issuers enter their loops through it and run them on
+// that one thread: issued from a lane picked by lane index instead, a
+// tcgen05.mma takes about three times as long to issue.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile(
