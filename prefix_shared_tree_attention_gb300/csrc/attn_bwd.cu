@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
       tc::tma_prefetch_desc(&tm_do);
-      tc::grid_wait_prior();  // D, loaded with each dO stage, comes from the preprocess
+      tc::grid_wait_prior();  // D, loaded with each Q stage, comes from the preprocess
       auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_bwd); };
       int qs = 0, nk = 0, nq_half = 0;  // steps loaded, K/V loads, and a lone Q load in flight
       bool ok = true;
