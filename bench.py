@@ -248,15 +248,18 @@ def cpu_oracle_run(steps: int, warmup: int, budget_pairs: int):
             sum(int(t.node_end[n] - t.node_start[n] + 1) for n in nodes) / sec}
 
 
+def reference_budget(oracle_pairs: int, steps: int, warmup: int) -> int:
+    """Ancestor pairs of each reference step's sample: it shrinks with the
+    number of steps, so that a whole --steps K --warmup W run stays near
+    twelve full-size samples (a few minutes on the host cores)."""
+    n = max(1, steps + warmup)
+    return max(1, int(oracle_pairs * min(1.0, 12.0 / n)))
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    # Each step is a bounded sample whose size shrinks with the number of steps,
-    # so that the whole --steps K --warmup W run stays near twelve full-size
-    # samples (a few minutes on the host cores) whatever K and W are.
-    n = max(1, args.steps + args.warmup)
-    budget = max(1, int(args.oracle_pairs * min(1.0, 12.0 / n)))
-    r = cpu_oracle_run(args.steps, args.warmup, budget)
+    r = cpu_oracle_run(args.steps, args.warmup, reference_budget(args.oracle_pairs, args.steps, args.warmup))
     line = {
         "impl": "reference", "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["sec_per_step"] * 1e3,
