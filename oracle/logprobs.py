@@ -13,8 +13,10 @@ sequence by sequence with no caching:
         ent_s[t]  = - sum_v exp(ls_t[v]) ls_t[v]
 
 Readings: the last position of each sequence has no label and gets 0 (the
-rolled-label convention); entropy uses the natural log. ``row(g)`` is the
-logits row of tree position g: ``row_base[tree] + g``.
+rolled-label convention); entropy uses the natural log, and a vocabulary
+entry with p = 0 (a logit of -inf, e.g. a masked token) contributes 0 to it,
+the limit of p log p as p -> 0. ``row(g)`` is the logits row of tree
+position g: ``row_base[tree] + g``.
 """
 from __future__ import annotations
 
@@ -29,6 +31,13 @@ def _log_softmax64(rows: torch.Tensor) -> torch.Tensor:
     m = x.max(dim=-1, keepdim=True).values
     z = x - m
     return z - torch.log(torch.exp(z).sum(dim=-1, keepdim=True))
+
+
+def _entropy64(ls: torch.Tensor) -> torch.Tensor:
+    """-sum_v p_v log p_v over the last axis from log-probabilities ``ls``;
+    entries with p = 0 (ls = -inf) are left out of the sum (0 log 0 = 0)."""
+    plogp = torch.exp(ls) * ls
+    return -torch.where(torch.isneginf(ls), torch.zeros_like(plogp), plogp).sum(-1)
 
 
 def sequence_logprobs_entropy(pk: OraclePacking, seqs: list[list[int]], logits: torch.Tensor,
@@ -48,7 +57,7 @@ def sequence_logprobs_entropy(pk: OraclePacking, seqs: list[list[int]], logits: 
         if L > 1:
             nxt = torch.as_tensor(seqs[s][1:], dtype=torch.long)
             lp[:-1] = ls[torch.arange(L - 1), nxt].numpy()
-        ent = -(torch.exp(ls) * ls).sum(-1).numpy()
+        ent = _entropy64(ls).numpy()
         out_lp.append(lp)
         out_ent.append(ent)
     return out_lp, out_ent
@@ -66,7 +75,7 @@ def position_logprobs_entropy(pk: OraclePacking, logits: torch.Tensor, row_base:
     lp = np.zeros(len(pos))
     for u, p in enumerate(pos):
         ls = _log_softmax64(logits[row_base[tree] + p][None])[0]
-        ent[u] = float(-(torch.exp(ls) * ls).sum())
+        ent[u] = float(_entropy64(ls))
         par = int(t.parent[p])
         if par >= 0:
             lsp = _log_softmax64(logits[row_base[tree] + par][None])[0]

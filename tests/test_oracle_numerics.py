@@ -20,13 +20,12 @@ from synth import random_small_sequences
 
 
 def _gqa_causal(q, k, v, scale):
-    """Causal attention of one sequence via torch SDPA in fp64: q [L,Hq,d]."""
-    G = q.shape[1] // k.shape[1]
-    kk = k.repeat_interleave(G, dim=1)
-    vv = v.repeat_interleave(G, dim=1)
-    return F.scaled_dot_product_attention(q.transpose(0, 1)[None], kk.transpose(0, 1)[None],
-                                          vv.transpose(0, 1)[None], is_causal=True,
-                                          scale=scale)[0].transpose(0, 1)
+    """Causal attention of one sequence via torch SDPA in fp64: q [L,Hq,d],
+    k/v [L,Hkv,d].  The query-head to key/value-head mapping is torch's own
+    grouped-query attention (``enable_gqa``), not a repeat written here."""
+    return F.scaled_dot_product_attention(q.transpose(0, 1)[None], k.transpose(0, 1)[None],
+                                          v.transpose(0, 1)[None], is_causal=True, scale=scale,
+                                          enable_gqa=True)[0].transpose(0, 1)
 
 
 def _bf16_randn(shape, g):
@@ -146,6 +145,33 @@ def test_per_sequence_invariant_backward(seed, hq, hkv, d):
         assert torch.allclose(dv, dv_ref[b], atol=1e-10)
 
 
+@pytest.mark.parametrize("hq,hkv", [(4, 2), (6, 3), (8, 1), (6, 2)])
+def test_gqa_head_mapping_by_hand(hq, hkv):
+    # Query head h reads key/value head h // (hq // hkv): each head of a
+    # single-sequence tree is compared with a one-head causal attention whose
+    # key/value head is picked by that formula, one head at a time.
+    g = torch.Generator().manual_seed(40 + hq + hkv)
+    L, d = 70, 16
+    t = oracle.tree_pack([list(range(L))], 128).trees[0]
+    q = _bf16_randn((128, hq, d), g)
+    k = _bf16_randn((128, hkv, d), g)
+    v = _bf16_randn((128, hkv, d), g)
+    O, _ = oracle.attn_forward(t, q, k, v, t_pad=128)
+    group = hq // hkv
+    for h in range(hq):
+        kv = h // group
+        S = (q[:L, h] @ k[:L, kv].T) / math.sqrt(d)
+        S = S.masked_fill(~torch.tril(torch.ones(L, L, dtype=torch.bool)), float("-inf"))
+        ref = torch.softmax(S, -1) @ v[:L, kv]
+        assert torch.allclose(O[:L, h], ref, atol=1e-12), f"head {h}"
+        # and no other key/value head gives it (the heads' values differ)
+        for other in range(hkv):
+            if other != kv:
+                alt = torch.softmax(((q[:L, h] @ k[:L, other].T) / math.sqrt(d)).masked_fill(
+                    ~torch.tril(torch.ones(L, L, dtype=torch.bool)), float("-inf")), -1) @ v[:L, other]
+                assert not torch.allclose(O[:L, h], alt, atol=1e-6)
+
+
 def test_node_subset_matches_full():
     seqs, pk, q, k, v, dO = _random_case(11, 4, 2, 16, n=8)
     t = pk.trees[0]
@@ -206,3 +232,47 @@ def test_logprobs_vs_cross_entropy_and_cache(seed):
         plp, pent = oracle.position_logprobs_entropy(pk, logits, row_base, b, pk.seq_pos[s].tolist())
         assert np.allclose(pent, ent[s], atol=1e-12)
         assert np.allclose(plp[1:], lp[s][:-1], atol=1e-12)
+
+
+def test_logprobs_masked_entries_closed_form():
+    # k equal finite logits and the rest -inf: a uniform distribution over k
+    # entries, entropy log k; a label at a finite entry has log-prob -log k,
+    # a label at a masked entry -inf.
+    seqs = [[0, 3, 5, 3]]
+    pk = oracle.tree_pack(seqs, 128)
+    V = 9
+    logits = torch.full((4, V), float("-inf"), dtype=torch.float64)
+    logits[:, [1, 3, 4, 7]] = 0.5                   # k = 4 finite entries, token 5 masked
+    lp, ent = oracle.sequence_logprobs_entropy(pk, seqs, logits, [0])
+    assert np.allclose(ent[0], math.log(4))
+    assert lp[0][0] == pytest.approx(-math.log(4))    # label 3
+    assert lp[0][1] == float("-inf")                   # label 5 is masked
+    assert lp[0][2] == pytest.approx(-math.log(4)) and lp[0][3] == 0.0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_logprobs_masked_entries_vs_scipy_entr(seed):
+    # Random rows with scattered -inf entries (and one row whose first 16
+    # entries are all -inf): entropy equals scipy's entr (x log x with
+    # entr(0) = 0) summed over the softmax, and the finite log-probs equal
+    # those of the row with its masked columns removed.
+    special = pytest.importorskip("scipy.special")
+    g = torch.Generator().manual_seed(seed)
+    seqs = [[1, 2, 3, 4, 5, 6]]
+    pk = oracle.tree_pack(seqs, 128)
+    V = 40
+    logits = 2 * torch.randn((6, V), generator=g, dtype=torch.float64)
+    masked = torch.rand((6, V), generator=g) < 0.3
+    masked[:, 2] = False                                  # every label stays finite
+    masked[:, 3:7] = False
+    masked[0, :16] = True
+    masked[0, 2] = False
+    logits[masked] = float("-inf")
+    lp, ent = oracle.sequence_logprobs_entropy(pk, seqs, logits, [0])
+    p = torch.softmax(logits, -1).numpy()
+    assert np.allclose(ent[0], special.entr(p).sum(-1), atol=1e-12)
+    for t in range(5):
+        keep = ~masked[t]
+        sub = logits[t, keep]
+        col = int(keep[:seqs[0][t + 1]].sum())            # label's column among the kept ones
+        assert lp[0][t] == pytest.approx(float(torch.log_softmax(sub, -1)[col]), abs=1e-12)
