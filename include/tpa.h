@@ -65,6 +65,8 @@ typedef struct {
   int64_t ancestor_pairs;     /* sum over real positions of (depth + 1) */
   double tree_token_ratio;    /* total_tree_tokens / total_seq_tokens (§指标和监控) */
   uint64_t blob_bytes;        /* size of the metadata blob (host and device copies) */
+  int32_t max_token;          /* largest token id of any sequence: a logits row must be wider */
+  int32_t reserved_;
 } tpa_tree_info;
 
 /*
@@ -80,6 +82,8 @@ typedef struct {
   int32_t n_trees, t_pad, n_seqs, max_nodes;
   int64_t total_seq_tokens;
   int64_t total_tree_tokens;
+  int32_t max_token;          /* largest token id (the log-prob calls reject vocab <= max_token) */
+  int32_t reserved_;
   const int32_t* tokens;      /* [B*T_pad] token id; pad -1 */
   const int32_t* subtree_end; /* [B*T_pad] E[p]: last position of the subtree of p's node;
                                  key p is visible to query i iff p <= i <= E[p]; pad -1 */
@@ -342,7 +346,11 @@ uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32
  *   workspace: device buffer of tpa_tree_attn_bwd_workspace_bytes() bytes,
  *     256-byte aligned, contents overwritten
  * dK/dV (per key tile) and dQ (per query tile) are accumulated in tensor
- * memory by separate kernels without atomics: results are deterministic.
+ * memory by separate kernels.  With fp32 gradients, a key tile seen by more
+ * than 64 (query head, query tile) pairs is split into several work items
+ * whose partial sums are added into its dK/dV rows with atomic adds, so those
+ * rows can differ in the last bits between calls; every other output is
+ * deterministic.
  * Errors: as tpa_tree_attn_fwd, plus TPA_ERR_BUFFER_TOO_SMALL.
  */
 int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
@@ -369,7 +377,10 @@ int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
  *   Allocation: none (no cudaMalloc, no cudaFree, no allocating library call).
  *   Set-up: the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The cached address belongs to the
+ *     device's current context: after cudaDeviceReset (or anything else that
+ *     destroys the primary context) it is stale, so do not call this entry
+ *     point on that device again in the same process.
  *   Sharing: every call on a device uses the same array, which keeps the last
  *     call's contents (each call rewrites all of the scratch it reads, so
  *     nothing carries over).  Calls that overlap on the GPU — on different
@@ -405,8 +416,16 @@ enum { TPA_LOGITS_COMPACT = 0, TPA_LOGITS_PADDED = 1 };
  *   seq_logp    [total_seq_tokens] fp32: for sequence s at token t,
  *               pos_logp[next position of s] (t < L-1) and 0 at t = L-1
  *   seq_entropy [total_seq_tokens] fp32: pos_entropy at each token of s
- * All outputs are device buffers and are written completely.  Errors:
- * TPA_ERR_INVALID_ARG, TPA_ERR_CUDA.
+ * All outputs are device buffers and are written completely.  Every token id
+ * of the tree must be below `vocab`: a view whose max_token is >= vocab is
+ * refused (TPA_ERR_INVALID_ARG) before any launch.  Should a label still fall
+ * outside the row (a view edited by hand), the kernel does not read it: that
+ * position's log-prob is NaN and the next tpa_sync_status() returns
+ * TPA_ERR_INVALID_ARG.  Logits of -inf (masked vocabulary entries) are
+ * allowed: they add nothing to the entropy (p log p -> 0 as p -> 0), and a
+ * label at such an entry gets a log-prob of -inf; a row whose logits are all
+ * -inf has no distribution and gives NaN.  Errors: TPA_ERR_INVALID_ARG,
+ * TPA_ERR_CUDA.
  */
 int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* logits, int64_t row_stride,
                               int32_t layout, int32_t vocab, float* pos_logp, float* pos_entropy,
@@ -423,7 +442,9 @@ int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* logits, int
  *            row tok_base[b] + p is tree b, position p (compact rows)
  *   weight   [vocab, hidden_size] bf16, device, 16-byte aligned
  *   hidden_size a multiple of 64, <= 65536;  vocab >= 1;  every token id of the
- *            tree must be < vocab (a larger one yields NaN at its position)
+ *            tree must be < vocab (a view whose max_token is >= vocab is
+ *            refused with TPA_ERR_INVALID_ARG; a larger id in a view edited
+ *            by hand yields NaN at its position)
  *   workspace device buffer of tpa_lm_head_workspace_bytes() bytes, 256-byte
  *            aligned, contents overwritten (per-row softmax partials, label
  *            logits, a work counter)
@@ -442,7 +463,9 @@ int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const void* hidden, 
 /* ------------------------------------------------------------------------ */
 
 /* Synchronize `stream`, then read and clear the device status words of all
- * kernels: TPA_OK, TPA_ERR_DEVICE_TIMEOUT or TPA_ERR_CUDA. */
+ * kernels: TPA_OK, TPA_ERR_DEVICE_TIMEOUT (a bounded wait ran out),
+ * TPA_ERR_INVALID_ARG (a kernel met an input outside its range, such as a
+ * label id >= vocab, and skipped it) or TPA_ERR_CUDA. */
 int tpa_sync_status(void* stream);
 
 /* Diagnostic for the bounded waits above: launches one thread on `stream`

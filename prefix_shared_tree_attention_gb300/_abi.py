@@ -27,6 +27,7 @@ class TreeInfo(C.Structure):
         ("n_trees", C.c_int32), ("t_pad", C.c_int32), ("n_seqs", C.c_int32), ("max_nodes", C.c_int32),
         ("total_seq_tokens", C.c_int64), ("total_tree_tokens", C.c_int64), ("total_nodes", C.c_int64),
         ("ancestor_pairs", C.c_int64), ("tree_token_ratio", C.c_double), ("blob_bytes", C.c_uint64),
+        ("max_token", C.c_int32), ("reserved_", C.c_int32),
     ]
 
 
@@ -34,6 +35,7 @@ class TreeView(C.Structure):
     _fields_ = [
         ("n_trees", C.c_int32), ("t_pad", C.c_int32), ("n_seqs", C.c_int32), ("max_nodes", C.c_int32),
         ("total_seq_tokens", C.c_int64), ("total_tree_tokens", C.c_int64),
+        ("max_token", C.c_int32), ("reserved_", C.c_int32),
         ("tokens", C.c_void_p), ("subtree_end", C.c_void_p), ("parent", C.c_void_p), ("depth", C.c_void_p),
         ("node_id", C.c_void_p), ("child_off", C.c_void_p), ("child_pos", C.c_void_p),
         ("n_tokens", C.c_void_p), ("tok_base", C.c_void_p), ("node_info", C.c_void_p),

@@ -10,7 +10,8 @@
 // Codes written into a translation unit's device status word.
 enum : unsigned int {
   TPA_DEV_OK = 0,
-  TPA_DEV_TIMEOUT = 1,  // a bounded mbarrier wait ran out; the kernel returned early
+  TPA_DEV_TIMEOUT = 1,    // a bounded mbarrier wait ran out; the kernel returned early
+  TPA_DEV_BAD_INPUT = 4,  // an input was outside its range (e.g. a label id >= vocab); it was skipped
 };
 
 #define TPA_CUDA_TRY(expr)                        \
@@ -37,6 +38,7 @@ enum : unsigned int {
         return TPA_ERR_CUDA;                                                       \
       }                                                                            \
     }                                                                              \
+    if (v & TPA_DEV_BAD_INPUT) return TPA_ERR_INVALID_ARG;                         \
     return v == 0 ? TPA_OK : TPA_ERR_DEVICE_TIMEOUT;                               \
   }
 

@@ -7,7 +7,8 @@
 uint64_t tpa_internal_blob_bytes(const tpa_tree* tree);
 
 // Each CUDA translation unit keeps its own device status word; these read
-// (and clear) it.  They return TPA_OK, TPA_ERR_DEVICE_TIMEOUT or TPA_ERR_CUDA.
+// (and clear) it.  They return TPA_OK, TPA_ERR_DEVICE_TIMEOUT, TPA_ERR_INVALID_ARG
+// (an input outside its range was skipped) or TPA_ERR_CUDA.
 int tpa_internal_status_classify(bool clear);
 int tpa_internal_status_logprobs(bool clear);
 int tpa_internal_status_fwd(bool clear);

@@ -413,6 +413,7 @@ extern "C" int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const voi
   if (tree->n_trees < 1 || tree->t_pad < 1 || tree->n_seqs < 1 || tree->total_tree_tokens < 1)
     return TPA_ERR_INVALID_ARG;
   if (hidden_size < kBK || hidden_size % kBK != 0 || hidden_size > 65536 || vocab < 1) return TPA_ERR_INVALID_ARG;
+  if (tree->max_token < 0 || tree->max_token >= vocab) return TPA_ERR_INVALID_ARG;  // a label past the vocabulary
   if ((reinterpret_cast<uintptr_t>(hidden) | reinterpret_cast<uintptr_t>(weight)) & 15) return TPA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return TPA_ERR_INVALID_ARG;
   const int64_t rows = tree->total_tree_tokens;

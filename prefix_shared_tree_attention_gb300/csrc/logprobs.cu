@@ -10,6 +10,12 @@
 //   lse = m + log s,   entropy = lse - t / s   (= -sum p log p),
 //   pos_logp[c] = x[token c] - lse   for every child position c of the row.
 // HBM-bound: each logits element is read once.
+//
+// A logit of -inf (a masked vocabulary entry) has p = 0 and adds nothing to
+// s or t (p log p -> 0 as p -> 0); a row whose logits are all -inf has no
+// distribution, and its entropy and log-probs come out NaN.
+#include <cfloat>
+
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -45,7 +51,10 @@ __device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
   a.m = m;
 }
 
-// Fold 8 values (one 16-byte vector) into the accumulator.
+// Fold 8 values (one 16-byte vector) into the accumulator.  While every
+// value seen is -inf the running max stays -inf and nothing is added; the
+// t term multiplies e by x clamped to the finite range, so an x of -inf
+// (e = 0) adds 0 instead of 0 * -inf.
 __device__ __forceinline__ void acc_add8(Acc& a, const uint4 v) {
   float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                 bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
@@ -57,12 +66,13 @@ __device__ __forceinline__ void acc_add8(Acc& a, const uint4 v) {
     a.t *= c;
     a.m = mc;
   }
+  if (a.m == -INFINITY) return;
   const float mb = a.m * kLog2e;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float e = ex2(fmaf(x[i], kLog2e, -mb));
     a.s += e;
-    a.t = fmaf(e, x[i], a.t);
+    a.t = fmaf(e, fmaxf(x[i], -FLT_MAX), a.t);
   }
 }
 
@@ -73,9 +83,10 @@ __device__ __forceinline__ void acc_add1(Acc& a, float x) {
     a.t *= c;
     a.m = x;
   }
+  if (a.m == -INFINITY) return;
   const float e = ex2((x - a.m) * kLog2e);
   a.s += e;
-  a.t = fmaf(e, x, a.t);
+  a.t = fmaf(e, fmaxf(x, -FLT_MAX), a.t);
 }
 
 // grid (T_pad, B): CTA (p, b) handles tree position p of tree b.
@@ -149,8 +160,13 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(
   for (int c = c0 + threadIdx.x; c < c1; c += kRowThreads) {
     const int cp = child_pos[int64_t(b) * t_pad + c];
     const int tok = tokens[int64_t(b) * t_pad + cp];
-    const float xl = __uint_as_float(uint32_t(x[tok]) << 16);
-    pos_logp[int64_t(b) * t_pad + cp] = xl - lse_s;
+    if (uint32_t(tok) < uint32_t(vocab)) {
+      const float xl = __uint_as_float(uint32_t(x[tok]) << 16);
+      pos_logp[int64_t(b) * t_pad + cp] = xl - lse_s;
+    } else {  // a label outside the row: not read (the host refuses such trees)
+      pos_logp[int64_t(b) * t_pad + cp] = __uint_as_float(0x7fc00000u);
+      atomicOr(&g_status_logprobs, TPA_DEV_BAD_INPUT);
+    }
   }
 }
 
@@ -183,6 +199,7 @@ extern "C" int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* 
     return TPA_ERR_INVALID_ARG;
   if (layout != TPA_LOGITS_COMPACT && layout != TPA_LOGITS_PADDED) return TPA_ERR_INVALID_ARG;
   if (tree->n_trees < 1 || tree->t_pad < 1 || tree->n_seqs < 1) return TPA_ERR_INVALID_ARG;
+  if (tree->max_token < 0 || tree->max_token >= vocab) return TPA_ERR_INVALID_ARG;  // a label past the row
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   row_kernel<<<dim3(tree->t_pad, tree->n_trees), kRowThreads, 0, st>>>(
       static_cast<const uint16_t*>(logits), row_stride, layout, vocab, tree->t_pad, tree->n_tokens,

@@ -172,8 +172,11 @@ int pack_impl(const int32_t* tokens, const int64_t* offs, int32_t n_seqs, int32_
     if (len > mb) return TPA_ERR_SEQ_TOO_LONG;
   }
   const int64_t total = offs[n_seqs];
-  for (int64_t i = 0; i < total; ++i)
+  int32_t max_token = 0;
+  for (int64_t i = 0; i < total; ++i) {
     if (tokens[i] < 0) return TPA_ERR_INVALID_ARG;
+    max_token = std::max(max_token, tokens[i]);
+  }
 
   // Longest first; equal lengths keep input order.
   std::vector<int32_t> order(n_seqs);
@@ -239,6 +242,7 @@ int pack_impl(const int32_t* tokens, const int64_t* offs, int32_t n_seqs, int32_
   t->info.n_seqs = n_seqs;
   t->info.max_nodes = max_nodes;
   t->info.total_seq_tokens = total;
+  t->info.max_token = max_token;
   compute_layout(t);
   t->blob = static_cast<uint8_t*>(std::aligned_alloc(256, t->info.blob_bytes));
   if (!t->blob) { delete t; return TPA_ERR_NO_MEMORY; }
@@ -409,6 +413,8 @@ int tpa_tree_make_view(const tpa_tree* tree, const void* base, tpa_tree_view* v)
   v->max_nodes = tree->info.max_nodes;
   v->total_seq_tokens = tree->info.total_seq_tokens;
   v->total_tree_tokens = tree->info.total_tree_tokens;
+  v->max_token = tree->info.max_token;
+  v->reserved_ = 0;
   v->tokens = reinterpret_cast<const int32_t*>(b + o[kTokens]);
   v->subtree_end = reinterpret_cast<const int32_t*>(b + o[kSubtreeEnd]);
   v->parent = reinterpret_cast<const int32_t*>(b + o[kParent]);

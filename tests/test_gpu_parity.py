@@ -338,6 +338,84 @@ def test_logprobs_config4_sampled(tpa):
     _check_logprobs(tpa, pk, seqs, dtree, logits, "compact", row_base, seq_ids, pos)
 
 
+def _close_with_inf(got: np.ndarray, ref: np.ndarray, what: str) -> None:
+    """Equal infinities match; every finite reference within LOGP_ABS."""
+    inf = np.isinf(ref)
+    assert np.array_equal(np.isinf(got), inf) and np.array_equal(got[inf], ref[inf]), what
+    assert np.abs(got[~inf] - ref[~inf]).max() <= LOGP_ABS, what
+
+
+def test_logprobs_masked_vocabulary_entries(tpa):
+    # Logits of -inf (masked entries) add nothing to the entropy; a label at
+    # a masked entry has log-prob -inf.  Row 0's first 64 entries (the first
+    # vectors of several threads) are all -inf, and so are 25 % of the rest.
+    rng = np.random.default_rng(19)
+    seqs = random_small_sequences(rng, 8, 150, 3, min_len=2)
+    T = 256
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    V, stride = 1003, 1008
+    g = torch.Generator().manual_seed(23)
+    buf = (2 * torch.randn((pk.n_trees * T, stride), generator=g)).to(torch.bfloat16)
+    masked = torch.rand((pk.n_trees * T, stride), generator=g) < 0.25
+    masked[:, :3] = False            # labels 0, 1 finite; label 2 sometimes masked below
+    masked[::3, 2] = True
+    masked[0, :64] = True
+    buf[masked] = float("-inf")
+    logits = buf.cuda()[:, :V]
+    pl, pe, sl, se = tpa.tree_logprobs_entropy(dtree, logits, layout="padded")
+    tpa.sync_status()
+    row_base = [b * T for b in range(pk.n_trees)]
+    lp, ent = oracle.sequence_logprobs_entropy(pk, seqs, buf[:, :V], row_base)
+    offs = np.concatenate([[0], np.cumsum([len(s_) for s_ in seqs])])
+    sl_c, se_c = sl.cpu().double().numpy(), se.cpu().double().numpy()
+    assert np.isinf(np.concatenate(lp)).any()      # some label sits at a masked entry
+    for s_ in range(len(seqs)):
+        _close_with_inf(sl_c[offs[s_]:offs[s_ + 1]], lp[s_], f"seq {s_} logp")
+        _close_with_inf(se_c[offs[s_]:offs[s_ + 1]], ent[s_], f"seq {s_} entropy")
+    for b in range(pk.n_trees):
+        plp, pent = oracle.position_logprobs_entropy(pk, buf[:, :V], row_base, b)
+        n = pk.trees[b].n
+        _close_with_inf(pl[b, :n].cpu().double().numpy(), plp, f"tree {b} pos logp")
+        _close_with_inf(pe[b, :n].cpu().double().numpy(), pent, f"tree {b} pos entropy")
+
+
+def test_logprobs_label_outside_row_is_not_read(tpa):
+    # The host refuses a tree whose token ids reach the vocabulary width.  A
+    # view edited by hand gets past that check; the kernel then skips the
+    # out-of-row label, writes NaN there and reports TPA_ERR_INVALID_ARG.
+    # The row stride (64) exceeds every id (<= 45), so even the skipped read
+    # would have stayed inside the buffer.
+    import ctypes as C
+    seqs = [[3, 40, 7, 45], [3, 9, 1]]
+    T = 128
+    pk = oracle.tree_pack(seqs, T)
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    V, stride = 32, 64
+    buf = (2 * torch.randn((T, stride), generator=torch.Generator().manual_seed(5))).to(torch.bfloat16)
+    logits = buf.cuda()
+    outs = [torch.zeros(T, device="cuda"), torch.zeros(T, device="cuda"),
+            torch.zeros(7, device="cuda"), torch.zeros(7, device="cuda")]
+    L = tpa.lib()
+    args = (logits.data_ptr(), stride, 1, V, *[o.data_ptr() for o in outs], None)
+    assert L.tpa_tree_logprobs_entropy(C.byref(dtree.view), *args) == -1     # refused on the host
+    view = type(dtree.view).from_buffer_copy(dtree.view)
+    view.max_token = 0
+    assert L.tpa_tree_logprobs_entropy(C.byref(view), *args) == 0
+    with pytest.raises(tpa.TpaError) as e:
+        tpa.sync_status()
+    assert e.value.name == "TPA_ERR_INVALID_ARG"
+    tpa.sync_status()                                                         # cleared once read
+    t = pk.trees[0]
+    pl = outs[0].cpu().double().numpy()
+    outside = [p for p in range(t.n) if t.parent[p] >= 0 and t.tokens[p] >= V]
+    inside = [p for p in range(t.n) if p not in outside]
+    assert outside and np.all(np.isnan(pl[outside]))
+    plp, pent = oracle.position_logprobs_entropy(pk, buf[:, :V].float(), [0], 0, inside)
+    assert np.abs(pl[inside] - plp).max() <= LOGP_ABS
+    assert np.abs(outs[1].cpu().double().numpy()[inside] - pent).max() <= LOGP_ABS
+
+
 # ---------------------------------------------------------------- argument checks through the ABI
 
 def test_invalid_arguments(tpa):

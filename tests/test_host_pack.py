@@ -51,6 +51,8 @@ def _compare(seqs, mb, tpa):
     assert info.total_tree_tokens == pk.total_tree_tokens
     assert info.tree_token_ratio == pytest.approx(pk.tree_token_ratio, rel=0, abs=1e-15)
     assert info.ancestor_pairs == sum(ancestor_pairs(t) for t in pk.trees)
+    assert info.max_token == max(max(s) for s in seqs)
+    assert tree.host_view().max_token == info.max_token
     a = tree.arrays()
     for b, t in enumerate(pk.trees):
         n = t.n
@@ -143,3 +145,20 @@ def test_blockmask_layout(tpa):
     assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 64, 0) >= 4 * 128 * 4          # D only
     assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 64, 1) >= 4 * 128 * 4
     assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 64, 7) == 0
+
+
+def test_logprob_calls_refuse_labels_past_vocab(tpa):
+    # A tree holding token id 999 cannot be scored against logits rows of
+    # 999 or fewer entries: both log-prob entry points refuse the call before
+    # any launch (the pointers below are never dereferenced).
+    import ctypes as C
+    tree = tpa.tree_pack([[1, 2, 999], [1, 5]], 128)
+    assert tree.info.max_token == 999
+    view = tree.host_view()
+    L = tpa.lib()
+    fake = 1 << 20
+    for vocab in (999, 500, 1):
+        assert L.tpa_tree_logprobs_entropy(C.byref(view), fake, 1024, 0, vocab, fake, fake, fake, fake,
+                                           None) == -1
+        assert L.tpa_lm_head_logprobs_entropy(C.byref(view), fake, fake, 64, vocab, fake, 1 << 40, fake, fake,
+                                              fake, fake, None) == -1
