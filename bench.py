@@ -1,23 +1,30 @@
 """Benchmark of the tree-training hot path on GB300.
 
-One step = one pass of every device row of the path over the GRPO-shaped
-workload (8 prompts x 8 samples, bimodal responses, max_tokens_per_mb 8192,
-32 query / 8 kv heads, head_dim 128) with its log-prob pass over bf16 logits
-of width 151936 on the same packed trees:
+One step = one pass of every device row of the path over one synthetic
+workload (``--config``, default 2):
     block classification -> tree attention forward -> tree attention backward
-    -> log-softmax / entropy / label gather -> per-sequence regather.
+    [-> log-softmax / entropy / label gather -> per-sequence regather]
+Config 2 (the default, the headline line) is the GRPO-shaped workload
+(8 prompts x 8 samples, bimodal responses, max_tokens_per_mb 8192, 32 query /
+8 kv heads, head_dim 128) with its log-prob pass over bf16 logits of width
+151936 on the same packed trees (the log-prob workload).  Config 1 (tiny,
+with log-probs over a 1000-wide vocabulary), config 3 (agentic multi-turn,
+one deep tree) and config 5 (64K-token few-shot tree) time their attention
+forward and backward; configs 3 and 5 name no logits.
 The packed metadata and every input are resident in HBM when the timed
 region starts (``value``); ``e2e`` repeats the step through the public API
 from host buffers: host packing, metadata upload, host->device copies of
-q, k, v, dO and logits from pinned memory, the device work, and the
-device->host copies of O, dQ, dK, dV and the per-sequence log-probs and
-entropies.
+q, k, v, dO (and logits) from pinned memory, the device work, and the
+device->host copies of O, dQ, dK, dV (and the per-sequence log-probs and
+entropies).
 
 Metric: ancestor-pair attention FLOPs (FlashAttention convention, forward
 4 P d Hq, backward 2.5x, i.e. 14 P d Hq per step, P = sum of depth + 1 over
 tree tokens) per second of the whole step; tree tokens/s is reported beside
-it. Every input (q alone is 470 MB) is larger than the 129 MB L2, so no flush
-is needed between steps.
+it, and the strict count without the recomputed S (12 P d Hq).  Inputs of
+configs 2, 3 and 5 (q alone is 470 MB to 4.3 GB) are larger than the 129 MB
+L2, so no flush is needed between their steps; config 1 writes a 256 MB
+buffer between steps to flush the L2.
 
 ``--impl reference`` times the CPU oracle (fp64, host cores) on a bounded
 sample of the same workload and prints the same line with "impl": "reference".
@@ -39,9 +46,24 @@ if ROOT not in sys.path:
 
 METRIC = "tree-attn fwd+bwd TFLOP/s on ancestor pairs (% bf16 peak); tree tokens/s"
 UNIT = "TFLOP/s"
-WORKLOAD = ("GRPO-shaped: 8 prompts x 8 samples, prompts 256-1024, responses 70% 50-200 / 30% 800-2048 "
-            "tokens, vocab 32000, max_tokens_per_mb 8192, 32 q / 8 kv heads, head_dim 128, bf16; "
-            "log-probs over bf16 logits [tree tokens, 151936] on the same trees")
+WORKLOADS = {
+    1: ("Tiny tree-attn: 4 prompts x 4 samples, prompt 64 tokens, responses 16-64 tokens, vocab 1000, "
+        "max_tokens_per_mb 1024, 4 q / 4 kv heads, head_dim 64, bf16; log-probs over bf16 logits "
+        "[tree tokens, 1000]"),
+    2: ("GRPO-shaped: 8 prompts x 8 samples, prompts 256-1024, responses 70% 50-200 / 30% 800-2048 "
+        "tokens, vocab 32000, max_tokens_per_mb 8192, 32 q / 8 kv heads, head_dim 128, bf16; "
+        "log-probs over bf16 logits [tree tokens, 151936] on the same trees"),
+    3: ("Agentic multi-turn: shared 2048-token system prompt, 16 trajectories of 4-8 turns of 64-512 "
+        "tokens, branch factor 1-3, max_tokens_per_mb 32768, 16 q / 2 kv heads, head_dim 128, bf16 "
+        "fwd+bwd"),
+    5: ("Large few-shot tree: shared 4096-token prefix, 64 samples of 512-4096 tokens branching at up to "
+        "16 depths, max_tokens_per_mb 65536, 32 q / 8 kv heads, head_dim 128, bf16 fwd+bwd"),
+}
+WORKLOAD = WORKLOADS[2]
+NOMINAL_HBM_GBS = 8000.0   # the HBM figure the log-prob target is stated against
+# A timed region shorter than this runs at the burst clock; longer ones at the
+# clock the power cap settles to.
+SUSTAINED_AFTER_S = 1.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -57,12 +79,14 @@ def _peaks():
 # names the source file it was captured from and that file's sha256 prefix,
 # the tree tokens of the captured case, and "DRAM traffic (read + write) of
 # this launch: X GB".  A summary counts only while the source is unchanged;
-# attention traffic scales with the tree tokens processed (every Q, K, V, O,
-# dO and gradient row is read or written a fixed number of times).
+# attention and log-prob traffic scale with the tree tokens processed (every
+# Q, K, V, O, dO, gradient and logits row is read or written a fixed number
+# of times).  The summaries were taken on the GRPO-shaped workload (config 2).
 PROFILES = {
     "tpa_tree_attn_fwd": ["attn_fwd_grpo_3trees_ncu_full.md"],
     "tpa_tree_attn_bwd": ["bwd_pre_grpo_3trees_ncu_full.md", "attn_bwd_kv_grpo_3trees_ncu_full.md",
                           "attn_bwd_dq2_grpo_3trees_ncu_full.md"],
+    "tpa_tree_logprobs_entropy": ["logprobs_row_grpo_1tree_ncu.md"],
 }
 
 
@@ -87,21 +111,21 @@ def _profile_traffic(entry: str, tree_tokens: int):
     return total if total > 0 else None
 
 
-def rank_sequences(rank: int, world: int, tpa):
+def rank_sequences(rank: int, world: int, tpa, cid: int = 2):
     """The sequences rank ``rank`` of ``world`` processes.
 
-    One rank: the GRPO-shaped batch (seed 2).  N ranks: N such batches
-    (seeds 2 + 1000 r) are packed together on every rank (the packer is
-    deterministic), and the trees are split over the ranks by KK balancing of
-    each tree's ancestor pairs, the attention work; a rank keeps the
+    One rank: the workload's batch (seed = config id).  N ranks: N such
+    batches (seeds cid + 1000 r) are packed together on every rank (the packer
+    is deterministic), and the trees are split over the ranks by KK balancing
+    of each tree's ancestor pairs, the attention work; a rank keeps the
     sequences of its trees.  Per-rank work stays that of one batch (weak
     scaling) and the data path needs no collective."""
     from synth import CONFIGS, flatten_sequences, make_sequences
     if world == 1:
-        return make_sequences(2, seed=2)
-    seqs = [s for r in range(world) for s in make_sequences(2, seed=2 + 1000 * r)]
+        return make_sequences(cid, seed=cid)
+    seqs = [s for r in range(world) for s in make_sequences(cid, seed=cid + 1000 * r)]
     toks, offs = flatten_sequences(seqs)
-    tree = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=CONFIGS[2].max_tokens_per_mb)
+    tree = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=CONFIGS[cid].max_tokens_per_mb)
     arr = tree.arrays()
     depth, ntok = arr["depth"].reshape(tree.n_trees, -1), arr["n_tokens"]
     pairs = [int((depth[b, :ntok[b]] + 1).sum()) for b in range(tree.n_trees)]
@@ -147,7 +171,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
         return self
@@ -184,16 +208,27 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _pairs(tree_arrays, n_tokens):
-    d = tree_arrays["depth"]
-    return int(sum(int((d[b, :n] + 1).sum()) for b, n in enumerate(n_tokens)))
+def segment_stats(seg):
+    """Median and spread (min, p10, p90, max) of per-step segment times [ms]."""
+    import numpy as np
+    seg = np.asarray(seg, dtype=np.float64)
+    return {"median": float(np.median(seg)), "min": float(seg.min()), "p10": float(np.percentile(seg, 10)),
+            "p90": float(np.percentile(seg, 90)), "max": float(seg.max())}
+
+
+def pick_bf16_peak(peaks: dict, timed_s: float):
+    """The bf16 denominator for a kernel timed inside a region of ``timed_s``
+    seconds: the burst figure below SUSTAINED_AFTER_S, the sustained one above."""
+    if timed_s < SUSTAINED_AFTER_S or "bf16_tflops_sustained" not in peaks:
+        return peaks["bf16_tflops"], "bf16 burst"
+    return peaks["bf16_tflops_sustained"], "bf16 sustained"
 
 
 # ---------------------------------------------------------------- CPU oracle (reference arm / cpu_baseline)
 
 def _oracle_sample(cfg, seqs, budget_pairs: int):
     """Nodes of tree 0 (shortest first) whose ancestor pairs sum to about
-    ``budget_pairs``; returns (tree, nodes, pairs)."""
+    ``budget_pairs``; returns (packing, tree, nodes, pairs)."""
     import numpy as np
     import oracle
     pk = oracle.tree_pack(seqs, cfg.max_tokens_per_mb)
@@ -218,15 +253,15 @@ def _oracle_step(cfg, t, nodes, q, k, v, do):
     oracle.attn_backward(t, q, k, v, do, t_pad=cfg.max_tokens_per_mb, nodes=nodes)
 
 
-def cpu_oracle_run(steps: int, warmup: int, budget_pairs: int):
+def cpu_oracle_run(steps: int, warmup: int, budget_pairs: int, cid: int = 2):
     """Time the fp64 oracle's attention fwd+bwd on a bounded sample."""
     import torch
     from synth import CONFIGS, make_sequences
-    cfg = CONFIGS[2]
-    seqs = make_sequences(2)
+    cfg = CONFIGS[cid]
+    seqs = make_sequences(cid)
     pk, t, nodes, pairs = _oracle_sample(cfg, seqs, budget_pairs)
     T = cfg.max_tokens_per_mb
-    g = torch.Generator().manual_seed(2001)
+    g = torch.Generator().manual_seed(1000 * cid + 1)
     q = torch.randn((T, cfg.n_heads_q, cfg.head_dim), generator=g).to(torch.bfloat16)
     k = torch.randn((T, cfg.n_heads_kv, cfg.head_dim), generator=g).to(torch.bfloat16)
     v = torch.randn((T, cfg.n_heads_kv, cfg.head_dim), generator=g).to(torch.bfloat16)
@@ -240,12 +275,45 @@ def cpu_oracle_run(steps: int, warmup: int, budget_pairs: int):
         times.append(time.perf_counter() - t0)
     flops = 14.0 * pairs * cfg.head_dim * cfg.n_heads_q
     sec = sum(times) / len(times)
-    sample = (f"oracle fp64 attention fwd+bwd on {len(nodes)} nodes of tree 0 (shortest first), "
+    whole = pairs == int((t.depth[:t.n] + 1).sum()) and pk.n_trees == 1
+    sample = (f"oracle fp64 attention fwd+bwd on {len(nodes)} nodes of tree 0 "
+              f"({'the whole workload' if whole else 'shortest first'}), "
               f"{pairs} ancestor pairs x {cfg.n_heads_q} heads x d {cfg.head_dim}; "
               f"{sec:.2f} s per step")
     return {"value": flops / sec / 1e12, "sec_per_step": sec, "pairs": pairs, "nodes": len(nodes),
             "sample": sample, "cores": torch.get_num_threads(), "tree_tokens_per_s":
             sum(int(t.node_end[n] - t.node_start[n] + 1) for n in nodes) / sec}
+
+
+def cpu_oracle_side(cid: int, logits_vocab: int | None, n_rows: int = 64):
+    """The oracle packer on the whole workload, and the oracle log-prob pass
+    on ``n_rows`` tree rows (fp64 log-softmax + entropy + label gather)."""
+    import numpy as np
+    import torch
+    import oracle
+    from synth import CONFIGS, make_sequences
+    cfg = CONFIGS[cid]
+    seqs = make_sequences(cid)
+    t0 = time.perf_counter()
+    pk = oracle.tree_pack(seqs, cfg.max_tokens_per_mb)
+    pack_s = time.perf_counter() - t0
+    out = {"pack_s": pack_s, "pack_tokens_per_s": pk.total_seq_tokens / pack_s,
+           "pack_sample": f"oracle packer on the whole workload ({len(seqs)} sequences, "
+                          f"{pk.total_seq_tokens} tokens)"}
+    if logits_vocab:
+        t = pk.trees[0]
+        rows = min(n_rows, t.n)
+        logits = (2 * torch.randn((rows, logits_vocab), generator=torch.Generator().manual_seed(5))
+                  ).to(torch.bfloat16)
+        pos = list(range(rows))
+        t0 = time.perf_counter()
+        oracle.position_logprobs_entropy(pk, logits, [0] + [0] * (pk.n_trees - 1), 0,
+                                         [p for p in pos if t.parent[p] < rows])
+        lp_s = time.perf_counter() - t0
+        nbytes = rows * logits_vocab * 2
+        out.update({"logprobs_s": lp_s, "logprobs_gbs": nbytes / lp_s / 1e9,
+                    "logprobs_sample": f"oracle fp64 log-prob pass on {rows} tree rows x {logits_vocab}"})
+    return out
 
 
 def reference_budget(oracle_pairs: int, steps: int, warmup: int) -> int:
@@ -259,12 +327,13 @@ def reference_budget(oracle_pairs: int, steps: int, warmup: int) -> int:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    r = cpu_oracle_run(args.steps, args.warmup, reference_budget(args.oracle_pairs, args.steps, args.warmup))
+    r = cpu_oracle_run(args.steps, args.warmup, reference_budget(args.oracle_pairs, args.steps, args.warmup),
+                       args.config)
     line = {
         "impl": "reference", "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["sec_per_step"] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "bounded oracle sample"},
+        "data": "synthetic", "config": {"workload": WORKLOADS[args.config], "sample": "bounded oracle sample"},
         "cpu_baseline": {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                          "sample": r["sample"]},
         "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -287,10 +356,15 @@ def run_gpu(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     tpa.device_check()
-    cfg, lcfg = CONFIGS[2], CONFIGS[4]
-    seqs = rank_sequences(rank, world, tpa)  # weak scaling: one batch's worth of trees per rank
+    cid = args.config
+    cfg = CONFIGS[cid]
+    # logits of the log-prob pass: config 2 uses the log-prob workload (its
+    # trees, width 151936, seed 4); config 1 its own 1000-wide logits
+    lp_cid = {1: 1, 2: 4}.get(cid)
+    seqs = rank_sequences(rank, world, tpa, cid)  # weak scaling: one batch's worth of trees per rank
     toks, offs = flatten_sequences(seqs)
-    T, Hq, Hkv, d, V = cfg.max_tokens_per_mb, cfg.n_heads_q, cfg.n_heads_kv, cfg.head_dim, lcfg.logits_vocab
+    T, Hq, Hkv, d = cfg.max_tokens_per_mb, cfg.n_heads_q, cfg.n_heads_kv, cfg.head_dim
+    V = CONFIGS[lp_cid].logits_vocab if lp_cid else 0
 
     tree = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
     if args.max_trees and tree.n_trees > args.max_trees:
@@ -302,18 +376,20 @@ def run_gpu(args, rank, world, local):
     info = tree.info
     B = info.n_trees
     run_attn = args.only in ("all", "attn")
-    run_lp = args.only in ("all", "logprobs")
+    run_lp = args.only in ("all", "logprobs") and lp_cid is not None
     rows = info.total_tree_tokens
     pairs = int(info.ancestor_pairs)
     flops_fwd = 4.0 * pairs * d * Hq
-    flops_step = 14.0 * pairs * d * Hq
+    flops_bwd = 10.0 * pairs * d * Hq
+    flops_step = 14.0 * pairs * d * Hq if run_attn else 0.0
+    flops_strict = 12.0 * pairs * d * Hq if run_attn else 0.0
 
     dtree = tree.upload(dev)
     mask = tpa.BlockMask(B, T, dev)
-    qh, kh, vh = make_qkv(2, B, T, Hq, Hkv, d)
-    doh = make_dout(2, B, T, Hq, d)
+    qh, kh, vh = make_qkv(cid, B, T, Hq, Hkv, d)
+    doh = make_dout(cid, B, T, Hq, d)
     q, k, v, do = (x.to(dev) for x in (qh, kh, vh, doh))
-    logits = make_logits(4, rows, V, device=str(dev)) if run_lp else None
+    logits = make_logits(lp_cid, rows, V, device=str(dev)) if run_lp else None
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
     # gradients in the dtype the workload fixes (bf16, as q/k/v); --grad-dtype fp32 times the
@@ -325,9 +401,15 @@ def run_gpu(args, rank, world, local):
     lp_out = (torch.empty((B, T), dtype=torch.float32, device=dev), torch.empty((B, T), dtype=torch.float32, device=dev),
               torch.empty(N, dtype=torch.float32, device=dev), torch.empty(N, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream(dev)
-    n_launch_per_step = 3 + 1 + 3 + 2  # classify+csr+bit masks, fwd, bwd pre+KV+dQ, rows+regather
+    # inputs smaller than the L2 (config 1): flush it between steps, outside the segments
+    in_bytes = sum(x.numel() * x.element_size() for x in (q, k, v, do)) + (
+        logits.numel() * logits.element_size() if logits is not None else 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < (256 << 20) else None
+    n_launch_per_step = 3 + (1 + 3 if run_attn else 0) + (2 if run_lp else 0)
 
     def step(ev=None):
+        if flush is not None:
+            flush.fill_(1)
         if ev: ev[0].record(stream)
         tpa.block_classify(dtree, out=mask)
         if ev: ev[1].record(stream)
@@ -362,7 +444,15 @@ def run_gpu(args, rank, world, local):
     tpa.sync_status()
     total_ms = t_start.elapsed_time(t_end)
     seg = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)])
-    t_cls, t_fwd, t_bwd, t_lp = seg.mean(axis=0)
+    stats = {name: segment_stats(seg[:, j]) for j, name in
+             enumerate(("block_classify", "attn_fwd", "attn_bwd", "logprobs_entropy"))}
+    t_cls, t_fwd, t_bwd, t_lp = (stats[n]["median"] for n in
+                                 ("block_classify", "attn_fwd", "attn_bwd", "logprobs_entropy"))
+    # the step as a whole: the device time between the first and last events
+    # (a flush between steps, when there is one, is not part of it)
+    step_ms = np.array([evs[i][0].elapsed_time(evs[i][4]) for i in range(args.steps)])
+    if flush is not None:
+        total_ms = float(step_ms.sum())
     # whole job: work summed over the ranks, time of the slowest rank
     job_flops, job_rows, total_ms = reduce_job(flops_step, rows, total_ms)
     ms_step = total_ms / args.steps
@@ -372,7 +462,7 @@ def run_gpu(args, rank, world, local):
     # Not part of the step: the export a dense-mask consumer would run once
     # per micro-batch, timed alone on the same trees; bound by HBM writes.
     dmask = None
-    if args.only in ("all", "attn"):
+    if args.only in ("all", "attn") and not args.no_extras:
         dmask = {}
         for fmt in ("u8", "bits"):
             buf = tpa.dense_mask(dtree, fmt)
@@ -391,6 +481,8 @@ def run_gpu(args, rank, world, local):
             del buf
         tpa.sync_status()
 
+    peaks, peak_kind = _peaks()
+
     # ------------------------------------------------ LM head fused into the log-prob pass
     # The step upstream of the log-prob rows: logits = hidden @ W^T formed on
     # tcgen05 tiles and consumed in place.  Hidden size 4096 (a reading: the
@@ -399,7 +491,7 @@ def run_gpu(args, rank, world, local):
     # unfused route, a cuBLAS bf16 GEMM writing the logits then the HBM-bound
     # log-prob pass (context only: library GEMM, not part of this path).
     lmh = None
-    if run_lp and args.lm_head_hidden > 0:
+    if run_lp and cid == 2 and args.lm_head_hidden > 0 and not args.no_extras:
         Hh = args.lm_head_hidden
         hid = make_hidden(4, rows, Hh, str(dev))
         wlm = make_lm_weight(4, V, Hh, str(dev))
@@ -425,9 +517,10 @@ def run_gpu(args, rank, world, local):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ms_u = e0.elapsed_time(e1) / reps
+        lmh_peak, lmh_peak_kind = pick_bf16_peak(peaks, reps * ms_f / 1e3)
         lmh = {"rows": rows, "vocab": V, "hidden": Hh, "ms": ms_f, "tflops": fl / (ms_f / 1e3) / 1e12,
-               "frac_of_bf16_peak": fl / (ms_f / 1e3) / 1e12 / _peaks()[0]["bf16_tflops"],
-               "peak": "measured bf16 burst (the kernel is timed alone)",
+               "frac_of_bf16_peak": fl / (ms_f / 1e3) / 1e12 / lmh_peak,
+               "peak": f"{peak_kind} {lmh_peak_kind} (the kernel is timed alone, {reps} launches)",
                "logits_bytes_not_written": rows * V * 2,
                "unfused_cublas_gemm_plus_logprob_ms": ms_u}
         del hid, wlm, lws, lout
@@ -437,8 +530,10 @@ def run_gpu(args, rank, world, local):
     if not args.no_e2e and args.only == "all":
         pin = lambda x: x.pin_memory()
         qp, kp, vp, dop = pin(qh), pin(kh), pin(vh), pin(doh)
-        lg_host = torch.empty((rows, V), dtype=torch.bfloat16, pin_memory=True)
-        lg_host.copy_(logits)
+        lg_host = None
+        if run_lp:
+            lg_host = torch.empty((rows, V), dtype=torch.bfloat16, pin_memory=True)
+            lg_host.copy_(logits)
         out_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv)]
         seq_host = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(2)]
         blob_buf = torch.empty(int(info.blob_bytes), dtype=torch.uint8, device=dev)
@@ -447,27 +542,29 @@ def run_gpu(args, rank, world, local):
         lg_ready = torch.cuda.Event()
 
         # The host link moves ~210 GB/s either way whatever the stream count, so
-        # the 15.7 GB of logits set the pace: they stream in on a side stream
-        # while the attention inputs arrive, the attention runs and its
+        # the logits (15.7 GB on config 2) set the pace: they stream in on a side
+        # stream while the attention inputs arrive, the attention runs and its
         # gradients go back (the other direction of the link).
         def e2e_step():
             tr = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
             dt = tr.upload(dev, buffer=blob_buf)
             q.copy_(qp, non_blocking=True); k.copy_(kp, non_blocking=True)
             v.copy_(vp, non_blocking=True); do.copy_(dop, non_blocking=True)
-            side.wait_stream(torch.cuda.current_stream(dev))
-            with torch.cuda.stream(side):
-                logits.copy_(lg_host, non_blocking=True)
-                lg_ready.record(side)
+            if run_lp:
+                side.wait_stream(torch.cuda.current_stream(dev))
+                with torch.cuda.stream(side):
+                    logits.copy_(lg_host, non_blocking=True)
+                    lg_ready.record(side)
             tpa.block_classify(dt, out=mask)
             tpa.tree_attn_fwd(dt, mask, q, k, v, out=o, lse=lse)
             tpa.tree_attn_bwd(dt, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv), grad_dtype=gdt)
             for h_, d_ in zip(out_host, (o, dq, dk, dv)):
                 h_.copy_(d_, non_blocking=True)
-            torch.cuda.current_stream(dev).wait_event(lg_ready)
-            tpa.tree_logprobs_entropy(dt, logits, out=lp_out)
-            seq_host[0].copy_(lp_out[2], non_blocking=True)
-            seq_host[1].copy_(lp_out[3], non_blocking=True)
+            if run_lp:
+                torch.cuda.current_stream(dev).wait_event(lg_ready)
+                tpa.tree_logprobs_entropy(dt, logits, out=lp_out)
+                seq_host[0].copy_(lp_out[2], non_blocking=True)
+                seq_host[1].copy_(lp_out[3], non_blocking=True)
             torch.cuda.synchronize(dev)
             return tr
 
@@ -486,46 +583,55 @@ def run_gpu(args, rank, world, local):
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             e2e_sec = float(tt.item())
         tpa.sync_status()
-        h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, dop, lg_host)) + int(info.blob_bytes)
-        d2h = sum(x.numel() * x.element_size() for x in out_host) + 2 * 4 * N
+        h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, dop)) + int(info.blob_bytes) + (
+            lg_host.numel() * lg_host.element_size() if lg_host is not None else 0)
+        d2h = sum(x.numel() * x.element_size() for x in out_host) + (2 * 4 * N if run_lp else 0)
         e2e = {"value": job_flops / e2e_sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_sec * 1e3,
-               "includes": "host pack + metadata upload + pinned H2D of q,k,v,dO,logits + device step + "
-                           "D2H of O,dQ,dK,dV,seq log-probs/entropies; the logits H2D overlaps the attention "
-                           "and its gradients' D2H on a second stream"}
+               "includes": "host pack + metadata upload + pinned H2D of q,k,v,dO" + (",logits" if run_lp else "") +
+                           " + device step + D2H of O,dQ,dK,dV" +
+                           (",seq log-probs/entropies; the logits H2D overlaps the attention and its "
+                            "gradients' D2H on a second stream" if run_lp else "")}
 
-    peaks, peak_kind = _peaks()
-    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    timed_s = total_ms / 1e3
+    bf16_peak, bf16_kind = pick_bf16_peak(peaks, timed_s)
     rate = lambda work, ms: work / (ms / 1e3) if ms > 1e-6 else 0.0
     attn_tflops = rate(flops_step / 1e12, t_fwd + t_bwd)
-    bwd_tflops = rate(10.0 * pairs * d * Hq / 1e12, t_bwd)
+    bwd_tflops = rate(flops_bwd / 1e12, t_bwd)
     fwd_tflops = rate(flops_fwd / 1e12, t_fwd)
     lp_bytes = rows * V * 2 + 4 * 4 * B * T + 8 * N
     lp_gbs = rate(lp_bytes / 1e9, t_lp)
-    dominant = max((("tpa_tree_attn_bwd", t_bwd), ("tpa_tree_attn_fwd", t_fwd), ("tpa_tree_logprobs_entropy", t_lp)),
-                   key=lambda x: x[1])[0]
+    kernel_ms = {"tpa_tree_attn_bwd": t_bwd if run_attn else 0.0, "tpa_tree_attn_fwd": t_fwd if run_attn else 0.0,
+                 "tpa_tree_logprobs_entropy": t_lp if run_lp else 0.0}
+    dominant = max(kernel_ms.items(), key=lambda x: x[1])[0]
+
+    def tensor_roof(entry, achieved, work):
+        return {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "traffic": _profile_traffic(entry, rows),
+                "traffic_unit": "bytes per launch (ncu DRAM read + write, scaled by tree tokens)",
+                "kernel": entry, "peak_kind": f"{peak_kind} {bf16_kind} (timed region {timed_s:.2f} s)",
+                "algorithmic_per_launch": work}
+
+    lp_roof = None
+    if run_lp:
+        lp_roof = {"bound": "hbm", "achieved": lp_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": lp_gbs / peaks["hbm_gbs"], "frac_of_nominal_8tbs": lp_gbs / NOMINAL_HBM_GBS,
+                   "traffic": _profile_traffic("tpa_tree_logprobs_entropy", rows),
+                   "traffic_unit": "bytes per launch (ncu DRAM read + write, scaled by tree tokens)",
+                   "kernel": "tpa_tree_logprobs_entropy", "peak_kind": f"{peak_kind} HBM copy",
+                   "algorithmic_per_launch": lp_bytes}
     if dominant == "tpa_tree_logprobs_entropy":
-        roof = {"bound": "hbm", "achieved": lp_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": lp_gbs / peaks["hbm_gbs"], "traffic": None}
+        roof = lp_roof
     elif dominant == "tpa_tree_attn_bwd":
-        roof = {"bound": "tensor", "achieved": bwd_tflops, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": bwd_tflops / peak_sus, "traffic": None}
+        roof = tensor_roof(dominant, bwd_tflops, flops_bwd)
     else:
-        roof = {"bound": "tensor", "achieved": fwd_tflops, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": fwd_tflops / peak_sus, "traffic": None}
-    if dominant != "tpa_tree_logprobs_entropy":
-        roof["traffic"] = _profile_traffic(dominant, rows)
-        roof["traffic_unit"] = "bytes per launch (ncu DRAM read + write, scaled by tree tokens)"
-    roof.update({"kernel": dominant, "peak_kind": f"{peak_kind} bf16 sustained" if roof["unit"] == "TFLOP/s"
-                 else f"{peak_kind} HBM copy", "algorithmic_per_launch":
-                 (10.0 * pairs * d * Hq if dominant == "tpa_tree_attn_bwd" else
-                  flops_fwd if dominant == "tpa_tree_attn_fwd" else lp_bytes)})
+        roof = tensor_roof(dominant, fwd_tflops, flops_fwd)
 
     # Micro-batch / rank balancing (host): the blog post's experiment shape —
     # the workload's sequences split over 4 ranks with unbounded capacity —
     # FFD against KK spread, and the cost of one call.
     bal = None
-    if rank == 0:
+    if rank == 0 and not args.no_extras:
         lens = [len(s_) for s_ in seqs]
         bal = {"items": len(lens), "groups": 4}
         for algo in ("ffd", "kk"):
@@ -558,26 +664,39 @@ def run_gpu(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.only == "all":
-        r = cpu_oracle_run(1, 0, args.oracle_pairs)
-        cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
+        r = cpu_oracle_run(1, 0, args.oracle_pairs, cid)
+        side = cpu_oracle_side(cid, V if run_lp else None)
+        cpu = {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle", "sample": r["sample"],
+               "tree_tokens_per_s": r["tree_tokens_per_s"], **side}
 
     value = job_flops / (ms_step / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "n_trees": B, "tree_tokens": rows, "original_tokens": int(N),
-                   "tree_token_ratio": info.tree_token_ratio, "ancestor_pairs": pairs,
-                   "flops_per_step": flops_step, "grad_dtype": args.grad_dtype,
-                   "l2": "inputs larger than L2 (129 MB); no flush",
+        "config": {"workload": WORKLOADS[cid], "config_id": cid, "n_trees": B, "tree_tokens": rows,
+                   "original_tokens": int(N), "tree_token_ratio": info.tree_token_ratio, "ancestor_pairs": pairs,
+                   "flops_per_step": flops_step, "flops_per_step_strict_12PdHq": flops_strict,
+                   "grad_dtype": args.grad_dtype,
+                   "l2": ("inputs larger than L2 (129 MB); no flush" if flush is None else
+                          "256 MB buffer written between steps to flush the L2 (outside the timed segments)"),
                    "parallelism": (f"trees split over {world} ranks by KK balancing of ancestor pairs"
                                    if world > 1 else "single GPU")},
         "tree_tokens_per_s": job_rows / (ms_step / 1e3),
-        "frac_of_bf16_peak": value / peak_sus,
-        "breakdown_ms": {"block_classify": t_cls, "attn_fwd": t_fwd, "attn_bwd": t_bwd, "logprobs_entropy": t_lp},
-        "attn_fwd_bwd_tflops": attn_tflops, "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
-        "logprobs_gbs": lp_gbs, "logprobs_frac_hbm": lp_gbs / peaks["hbm_gbs"],
-        "roofline": roof, "clocks": clocks, "gpu_launches": n_launch_per_step * args.steps,
+        "original_token_equiv_per_s": N * (job_rows / max(rows, 1)) / (ms_step / 1e3),
+        "frac_of_bf16_peak": value / bf16_peak,
+        "breakdown_ms": {"block_classify": t_cls, "attn_fwd": t_fwd, "attn_bwd": t_bwd, "logprobs_entropy": t_lp,
+                         "stat": "median over the timed steps"},
+        "breakdown_spread_ms": stats,
+        "attn_fwd_bwd_tflops": attn_tflops, "attn_fwd_bwd_tflops_strict": rate(flops_strict / 1e12, t_fwd + t_bwd),
+        "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
+        "attn_fwd_bwd_frac_of_bf16_peak": attn_tflops / bf16_peak, "bf16_peak_used": bf16_kind,
+        "logprobs_gbs": lp_gbs if run_lp else None,
+        "logprobs_frac_hbm": lp_gbs / peaks["hbm_gbs"] if run_lp else None,
+        "logprobs_frac_nominal_8tbs": lp_gbs / NOMINAL_HBM_GBS if run_lp else None,
+        "roofline": roof, "roofline_logprobs": lp_roof, "clocks": clocks,
+        "attn_gcycles_at_median_clock": ((t_fwd + t_bwd) * clocks["sm_mhz"] / 1e6) if clocks["sm_mhz"] else None,
+        "gpu_launches": n_launch_per_step * args.steps,
         "e2e": e2e, "cpu_baseline": cpu, "balance": bal, "lm_head": lmh,
         "dense_mask": None if dmask is None else {
             **dmask, "frac_hbm_u8": dmask["u8"]["gbs"] / peaks["hbm_gbs"],
@@ -594,11 +713,16 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, choices=[1, 2, 3, 5], default=2,
+                    help="workload: 1 tiny, 2 GRPO-shaped with the log-prob pass (headline), 3 agentic, "
+                         "5 large few-shot")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--lm-head-hidden", type=int, default=4096,
                     help="hidden size of the fused LM-head measurement (0 skips it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the measurements outside the step (dense mask, LM head, balancing)")
     ap.add_argument("--grad-dtype", choices=["bf16", "fp32"], default="bf16",
                     help="dtype of dQ, dK, dV (bf16 as the workload's tensors; fp32 for the split-column path)")
     ap.add_argument("--oracle-pairs", type=int, default=15000000,

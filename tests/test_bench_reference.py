@@ -37,3 +37,25 @@ def test_reference_arm_json_line():
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert "workload" in line["config"]
+
+
+def test_segment_stats_and_peak_choice():
+    sys.path.insert(0, ROOT)
+    import bench
+    st = bench.segment_stats([3.0, 1.0, 2.0, 10.0, 2.0])
+    assert st["median"] == 2.0 and st["min"] == 1.0 and st["max"] == 10.0 and st["p10"] <= st["p90"]
+    peaks = {"bf16_tflops": 1919.3, "bf16_tflops_sustained": 1735.5, "hbm_gbs": 6682.2}
+    assert bench.pick_bf16_peak(peaks, 0.12) == (1919.3, "bf16 burst")
+    assert bench.pick_bf16_peak(peaks, 5.0) == (1735.5, "bf16 sustained")
+    assert bench.pick_bf16_peak({"bf16_tflops": 1900.0}, 5.0)[0] == 1900.0
+
+
+def test_reference_arm_other_config():
+    # the tiny workload: the oracle covers the whole tree in one sample
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "1",
+                          "--steps", "1", "--warmup", "0"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["config"]["workload"].startswith("Tiny") and line["value"] > 0
+    assert "the whole workload" in line["cpu_baseline"]["sample"]
