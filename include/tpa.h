@@ -424,7 +424,8 @@ enum { TPA_LOGITS_COMPACT = 0, TPA_LOGITS_PADDED = 1 };
  * TPA_ERR_INVALID_ARG.  Logits of -inf (masked vocabulary entries) are
  * allowed: they add nothing to the entropy (p log p -> 0 as p -> 0), and a
  * label at such an entry gets a log-prob of -inf; a row whose logits are all
- * -inf has no distribution and gives NaN.  Errors: TPA_ERR_INVALID_ARG,
+ * -inf (or all below -1e30) has no distribution and gives NaN.  Errors:
+ * TPA_ERR_INVALID_ARG,
  * TPA_ERR_CUDA.
  */
 int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* logits, int64_t row_stride,

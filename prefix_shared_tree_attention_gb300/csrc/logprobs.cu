@@ -14,8 +14,6 @@
 // A logit of -inf (a masked vocabulary entry) has p = 0 and adds nothing to
 // s or t (p log p -> 0 as p -> 0); a row whose logits are all -inf has no
 // distribution, and its entropy and log-probs come out NaN.
-#include <cfloat>
-
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -51,11 +49,29 @@ __device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
   a.m = m;
 }
 
-// Fold 8 values (one 16-byte vector) into the accumulator.  While every
-// value seen is -inf the running max stays -inf and nothing is added; the
-// t term multiplies e by x clamped to the finite range, so an x of -inf
-// (e = 0) adds 0 instead of 0 * -inf.
-__device__ __forceinline__ void acc_add8(Acc& a, const uint4 v) {
+// Masked entries: every bf16 value below -2^100 (-inf included; negative
+// bf16 values grow as unsigned bits) is clamped to -2^100 (0xF180) before it
+// is widened, with one unsigned 16x2 minimum per pair of values.  Next to any
+// real logit its exponential is then exactly 0 and its t term 0 * x = 0, so
+// it drops out of s and t as p log p -> 0 requires.  The clamp value is small
+// enough that m * log2e and a whole row's sum of e * x stay finite while a
+// thread has seen only masked entries (a row holds fewer than 2^27 entries).
+// The row's label logits are read unclamped.
+constexpr uint32_t kClampPair = 0xF180F180u;
+constexpr float kMaskedMax = -1.0e30f;  // a row max at or below this: every entry was masked
+
+__device__ __forceinline__ uint32_t clamp_neg_inf2(uint32_t w) {
+  uint32_t r;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(kClampPair));
+  return r;
+}
+
+// Fold 8 values (one 16-byte vector) into the accumulator.
+__device__ __forceinline__ void acc_add8(Acc& a, uint4 v) {
+  v.x = clamp_neg_inf2(v.x);
+  v.y = clamp_neg_inf2(v.y);
+  v.z = clamp_neg_inf2(v.z);
+  v.w = clamp_neg_inf2(v.w);
   float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
                 bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
   float mc = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
@@ -66,27 +82,26 @@ __device__ __forceinline__ void acc_add8(Acc& a, const uint4 v) {
     a.t *= c;
     a.m = mc;
   }
-  if (a.m == -INFINITY) return;
   const float mb = a.m * kLog2e;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float e = ex2(fmaf(x[i], kLog2e, -mb));
     a.s += e;
-    a.t = fmaf(e, fmaxf(x[i], -FLT_MAX), a.t);
+    a.t = fmaf(e, x[i], a.t);
   }
 }
 
-__device__ __forceinline__ void acc_add1(Acc& a, float x) {
+__device__ __forceinline__ void acc_add1(Acc& a, uint16_t raw) {
+  const float x = bf16_lo(clamp_neg_inf2(raw));
   if (x > a.m) {
     const float c = ex2((a.m - x) * kLog2e);
     a.s *= c;
     a.t *= c;
     a.m = x;
   }
-  if (a.m == -INFINITY) return;
   const float e = ex2((x - a.m) * kLog2e);
   a.s += e;
-  a.t = fmaf(e, fmaxf(x, -FLT_MAX), a.t);
+  a.t = fmaf(e, x, a.t);
 }
 
 // grid (T_pad, B): CTA (p, b) handles tree position p of tree b.
@@ -125,7 +140,7 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(
   }
   for (; i < nvec; i += kRowThreads) acc_add8(a, __ldcs(xv + i));
   for (int k = (nvec << 3) + threadIdx.x; k < vocab; k += kRowThreads)
-    acc_add1(a, __uint_as_float(uint32_t(x[k]) << 16));
+    acc_add1(a, x[k]);
 
   // block reduction of (m, s, t)
 #pragma unroll
@@ -148,7 +163,8 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(
       acc_merge(a, bo);
     }
     if (lane == 0) {
-      const float lse = a.m + __log2f(a.s) * kLn2;
+      // every entry -inf: no distribution, NaN entropy and log-probs
+      const float lse = a.m > kMaskedMax ? a.m + __log2f(a.s) * kLn2 : __uint_as_float(0x7fc00000u);
       lse_s = lse;
       pos_entropy[at] = lse - a.t / a.s;
       if (parent[at] < 0) pos_logp[at] = 0.f;  // no parent row: no label for this position
