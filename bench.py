@@ -396,7 +396,7 @@ def run_gpu(args, rank, world, local):
     # fp32-output path, which splits long key columns into items that add into zeroed rows
     gdt = torch.float32 if args.grad_dtype == "fp32" else torch.bfloat16
     dq, dk, dv = (torch.empty(x.shape, dtype=gdt, device=dev) for x in (q, k, v))
-    ws = torch.empty(tpa.tree_attn_bwd_workspace_bytes(B, T, Hq, d, gdt), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tpa.tree_attn_bwd_workspace_bytes(B, T, Hq, Hkv, d, gdt), dtype=torch.uint8, device=dev)
     N = info.total_seq_tokens
     lp_out = (torch.empty((B, T), dtype=torch.float32, device=dev), torch.empty((B, T), dtype=torch.float32, device=dev),
               torch.empty(N, dtype=torch.float32, device=dev), torch.empty(N, dtype=torch.float32, device=dev))

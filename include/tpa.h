@@ -84,6 +84,7 @@ typedef struct {
   int64_t total_tree_tokens;
   int32_t max_token;          /* largest token id (the log-prob calls reject vocab <= max_token) */
   int32_t reserved_;
+  int64_t ancestor_pairs;     /* sum over real positions of (depth + 1): sizes the backward's work items */
   const int32_t* tokens;      /* [B*T_pad] token id; pad -1 */
   const int32_t* subtree_end; /* [B*T_pad] E[p]: last position of the subtree of p's node;
                                  key p is visible to query i iff p <= i <= E[p]; pad -1 */
@@ -326,10 +327,12 @@ int tpa_tree_attn_fwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
 enum { TPA_GRAD_F32 = 0, TPA_GRAD_BF16 = 1 };
 
 /* Workspace bytes needed by tpa_tree_attn_bwd: fp32 D = rowsum(dO * O)
- * [B, Hq, T_pad] (the same for both gradient types).  0 on invalid
- * arguments. */
+ * [B, Hq, T_pad]; for TPA_GRAD_BF16 also fp32 staging rows for dK and dV
+ * ([B, T_pad, Hkv, d] each, used by key tiles whose column is split into
+ * several work items) and one 32-bit counter per (tree, kv head, key tile,
+ * compute warp).  0 on invalid arguments. */
 uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32_t n_heads_q,
-                                           int32_t head_dim, int32_t grad_dtype);
+                                           int32_t n_heads_kv, int32_t head_dim, int32_t grad_dtype);
 
 /*
  * tpa_tree_attn_bwd — gradients of <dO, O> for the forward above:
@@ -346,11 +349,13 @@ uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32
  *   workspace: device buffer of tpa_tree_attn_bwd_workspace_bytes() bytes,
  *     256-byte aligned, contents overwritten
  * dK/dV (per key tile) and dQ (per query tile) are accumulated in tensor
- * memory by separate kernels.  With fp32 gradients, a key tile seen by more
- * than 64 (query head, query tile) pairs is split into several work items
- * whose partial sums are added into its dK/dV rows with atomic adds, so those
- * rows can differ in the last bits between calls; every other output is
- * deterministic.
+ * memory by separate kernels.  A key tile seen by more (query head, query
+ * tile) pairs than one work item takes (a quarter of one SM's share of the
+ * tree's steps, estimated from view.ancestor_pairs, at least 64) is split into
+ * several items whose fp32 partial sums are added with atomic adds, into the
+ * dK/dV rows for fp32 gradients or into workspace rows that the last item
+ * converts to bf16; those rows can differ in the last bits between calls.
+ * Every other output is deterministic.
  * Errors: as tpa_tree_attn_fwd, plus TPA_ERR_BUFFER_TOO_SMALL.
  */
 int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
@@ -371,9 +376,11 @@ int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
  * the process exits.
  *   Arguments: as tpa_tree_attn_bwd, without workspace / workspace_bytes.
  *   Limit: the scratch of tpa_tree_attn_bwd_workspace_bytes() must fit in
- *     16 MiB: B * T_pad * Hq * 4 bytes (e.g. 8 trees of 8192 tokens with 64
- *     query heads, or one 65536-token tree with 64 query heads).  Larger
- *     problems return TPA_ERR_BUFFER_TOO_SMALL and enqueue nothing.
+ *     16 MiB: B * T_pad * Hq * 4 bytes for fp32 gradients (e.g. 8 trees of
+ *     8192 tokens with 64 query heads), plus B * T_pad * Hkv * d * 8 bytes and
+ *     the counters for bf16 gradients (e.g. 2 trees of 8192 tokens with 32
+ *     query and 2 kv heads of d 128).  Larger problems return
+ *     TPA_ERR_BUFFER_TOO_SMALL and enqueue nothing.
  *   Allocation: none (no cudaMalloc, no cudaFree, no allocating library call).
  *   Set-up: the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress with that device current) and caches it; make that

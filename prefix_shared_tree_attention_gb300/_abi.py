@@ -35,7 +35,7 @@ class TreeView(C.Structure):
     _fields_ = [
         ("n_trees", C.c_int32), ("t_pad", C.c_int32), ("n_seqs", C.c_int32), ("max_nodes", C.c_int32),
         ("total_seq_tokens", C.c_int64), ("total_tree_tokens", C.c_int64),
-        ("max_token", C.c_int32), ("reserved_", C.c_int32),
+        ("max_token", C.c_int32), ("reserved_", C.c_int32), ("ancestor_pairs", C.c_int64),
         ("tokens", C.c_void_p), ("subtree_end", C.c_void_p), ("parent", C.c_void_p), ("depth", C.c_void_p),
         ("node_id", C.c_void_p), ("child_off", C.c_void_p), ("child_pos", C.c_void_p),
         ("n_tokens", C.c_void_p), ("tok_base", C.c_void_p), ("node_info", C.c_void_p),
@@ -84,7 +84,7 @@ PROTOTYPES = {
                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
                                     C.c_float, C.c_void_p]),
     "tpa_tree_attn_bwd_workspace_bytes": (C.c_uint64, [C.c_int32, C.c_int32, C.c_int32, C.c_int32,
-                                                       C.c_int32]),
+                                                       C.c_int32, C.c_int32]),
     "tpa_tree_attn_bwd": (C.c_int, [C.POINTER(TreeView), C.POINTER(BlockMaskView), C.c_void_p, C.c_void_p,
                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                     C.c_void_p, C.c_void_p, C.c_uint64, C.c_int32, C.c_int32, C.c_int32,

@@ -278,9 +278,10 @@ def tree_attn_fwd(dtree: DeviceTree, mask: BlockMask, q: torch.Tensor, k: torch.
 _GRAD = {torch.float32: GRAD_F32, torch.bfloat16: GRAD_BF16}
 
 
-def tree_attn_bwd_workspace_bytes(n_trees: int, t_pad: int, n_heads_q: int, head_dim: int,
+def tree_attn_bwd_workspace_bytes(n_trees: int, t_pad: int, n_heads_q: int, n_heads_kv: int, head_dim: int,
                                   grad_dtype: torch.dtype = torch.float32) -> int:
-    return int(lib().tpa_tree_attn_bwd_workspace_bytes(n_trees, t_pad, n_heads_q, head_dim, _GRAD[grad_dtype]))
+    return int(lib().tpa_tree_attn_bwd_workspace_bytes(n_trees, t_pad, n_heads_q, n_heads_kv, head_dim,
+                                                       _GRAD[grad_dtype]))
 
 
 def tree_attn_bwd(dtree: DeviceTree, mask: BlockMask, q, k, v, o, lse, dout,
@@ -294,7 +295,7 @@ def tree_attn_bwd(dtree: DeviceTree, mask: BlockMask, q, k, v, o, lse, dout,
     if grad_dtype not in _GRAD:
         raise ValueError("grad_dtype must be torch.float32 or torch.bfloat16")
     if workspace is None:
-        nbytes = tree_attn_bwd_workspace_bytes(B, T, Hq, d, grad_dtype)
+        nbytes = tree_attn_bwd_workspace_bytes(B, T, Hq, Hkv, d, grad_dtype)
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     if out is None:
         out = tuple(torch.empty(x.shape, dtype=grad_dtype, device=x.device) for x in (q, k, v))

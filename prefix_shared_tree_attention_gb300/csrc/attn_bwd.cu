@@ -8,12 +8,14 @@
 // with dK/dV summed over the query heads of each key/value head.
 //
 // Three kernels, no atomics on the hot loop:
-//  (1) preprocess: D = rowsum(dO * O) in fp32 (and zeroed fp32 dK/dV rows of
-//      the key tiles whose long column is split into several items that add
-//      into them).
-//  (2) KV kernel: work items are (key tile, kv head, tree, chunk of up to 64
-//      steps of that key tile's column), a step being one (query head, query
-//      tile) pair of the per-key-block CSR.  Per step the MMA issuer runs
+//  (1) preprocess: D = rowsum(dO * O) in fp32 (and zeroed fp32 rows of the
+//      key tiles whose long column is split into several items that add into
+//      them: the dK/dV outputs for fp32 gradients, staging rows for bf16
+//      gradients, whose last adder converts them to bf16).
+//  (2) KV kernel: work items are (key tile, kv head, tree, chunk of that key
+//      tile's column, sized from the tree's ancestor pairs so that the items
+//      balance over the SMs), a step being one (query head, query tile) pair
+//      of the per-key-block CSR.  Per step the MMA issuer runs
 //      S^T = K Q^T and dP^T = V dO^T into two TMEM regions that swap roles
 //      every step; four compute warpgroups (thread r = key row r = TMEM lane
 //      r; warpgroup w = query columns [32w, 32w+32)) write P^T and dS^T back
@@ -60,7 +62,7 @@ constexpr int kNWG = 4;                    // compute warpgroups per CTA
 constexpr int kThreads = 128 * kNWG + 64;  // + TMA warp + MMA warp
 constexpr int kWTma = 4 * kNWG, kWMma = 4 * kNWG + 1;
 constexpr int kCW = kB / kNWG;             // query or key columns per warpgroup (32)
-constexpr int kKvChunk = 64;               // steps per KV work item (fp32 gradients)
+constexpr int kKvChunkMin = 64;            // fewest steps per KV work item of a split column
 
 struct BwdParams {
   const float* lse;     // [B, Hq, T]
@@ -76,6 +78,9 @@ struct BwdParams {
   const int32_t* q_idx;
   const uint4* qmask;
   uint32_t* sched;      // work counters: [2..3] KV kernel, [4..5] dQ kernel
+  float* stage_k;       // bf16 gradients: fp32 dK, dV rows of split key columns [B, T, Hkv, d]
+  float* stage_v;
+  uint32_t* kv_cnt;     // bf16 gradients: finished items per (tree, kv head, key tile, compute warp)
   int32_t t_pad, n_blk, cap, hq, hkv;
   int32_t n_trees, kv_chunk, kv_nchunk, kv_items, dq_items;
   int32_t wide;  // gradient outputs 32-byte aligned: fp32 rows stored 32 bytes at a time
@@ -632,18 +637,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nk == 0) tc::grid_wait_prior();  // rows the preprocess zeroed are added into
       // ---- dK, dV rows of this key tile (warpgroup w: head-dim columns [w d/4, (w+1) d/4))
       tc::tc_fence_after();
-      const bool add = F32OUT && (G * I.n_col > p.kv_chunk);  // several chunks add into one row
+      // A column longer than one item is split into several items that add
+      // into zeroed fp32 rows: the outputs themselves for fp32 gradients, the
+      // staging rows for bf16 gradients.
+      const bool split = G * I.n_col > p.kv_chunk;
+      const bool staged = !F32OUT && split;
+      const int64_t off32 = (int64_t(krow + r) * p.hkv + I.g) * D + w * DW;  // fp32 row offset
 #pragma unroll
       for (int c = 0; c < DW / 16; ++c) {
         uint32_t vv[16], kk[16];
         tc::tmem_ld16(tmem + lane_base + T_DV + w * DW + c * 16, vv);
         tc::tmem_ld16(tmem + lane_base + T_DK + w * DW + c * 16, kk);
         tc::tmem_ld_wait();
-        store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, add, p.wide);
-        store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, p.scale, add, p.wide);
+        if (staged) {
+          store_row16<true>(reinterpret_cast<uint8_t*>(p.stage_v + off32 + c * 16), vv, 1.f, true);
+          store_row16<true>(reinterpret_cast<uint8_t*>(p.stage_k + off32 + c * 16), kk, p.scale, true);
+        } else {
+          store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, F32OUT && split, p.wide);
+          store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, p.scale, F32OUT && split, p.wide);
+        }
       }
       tc::tc_fence_before();
       warp_arrive(acc_free);
+      if (staged) {
+        // Every item maps this warp to the same 32-row x DW-column block of
+        // the tile, so the warp that adds the column's last contribution to
+        // its block converts that block's fp32 sums to bf16.  Its adds and
+        // the other items' were made visible (fence) before each counted.
+        __threadfence();
+        __syncwarp();
+        const uint32_t n_items = uint32_t((G * I.n_col + p.kv_chunk - 1) / p.kv_chunk);
+        uint32_t done = 0;
+        if ((threadIdx.x & 31) == 0)
+          done = atomicAdd(p.kv_cnt + ((int64_t(I.b) * p.hkv + I.g) * p.n_blk + I.kb) * (4 * kNWG) + warp, 1u);
+        done = __shfl_sync(0xffffffffu, done, 0);
+        if (done == n_items - 1) {
+          __threadfence();
+#pragma unroll
+          for (int c = 0; c < DW / 16; ++c) {
+            uint32_t vv[16], kk[16];
+            const float4* sv = reinterpret_cast<const float4*>(p.stage_v + off32 + c * 16);
+            const float4* sk = reinterpret_cast<const float4*>(p.stage_k + off32 + c * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float4 a = __ldcg(sv + e), b = __ldcg(sk + e);
+              vv[4 * e] = __float_as_uint(a.x), vv[4 * e + 1] = __float_as_uint(a.y);
+              vv[4 * e + 2] = __float_as_uint(a.z), vv[4 * e + 3] = __float_as_uint(a.w);
+              kk[4 * e] = __float_as_uint(b.x), kk[4 * e + 1] = __float_as_uint(b.y);
+              kk[4 * e + 2] = __float_as_uint(b.z), kk[4 * e + 3] = __float_as_uint(b.w);
+            }
+            store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, false);
+            store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, 1.f, false);  // scaled when added
+          }
+        }
+      }
       qs += I.n;
       ++nk;
     }
@@ -1692,11 +1739,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
 // D[b, h, i] = sum_d dO * O (fp32) for real rows, 0 for pad rows.  The
 // [B*T*Hq, D] bf16 rows of O and dO are read with 16-byte loads, four per
 // lane in flight: a warp covers 128 * 32 / D rows per pass, D / 8 lanes per
-// row, and sums each row with shuffles.  With fp32 gradients it also zeroes
-// the dK and dV rows of the key tiles whose column is split into several
-// work items of the KV kernel (they add into those rows) and of the key tiles
-// no query sees (no item visits them); every other row is written whole by
-// its single item.
+// row, and sums each row with shuffles.  It also zeroes the fp32 rows that
+// the KV kernel's split columns add into: with fp32 gradients the dK and dV
+// rows themselves (and those of the key tiles no query sees, which no item
+// visits), with bf16 gradients the staging rows and the per-warp item
+// counters; every other row is written whole by its single item.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                      const __nv_bfloat16* __restrict__ dout,
@@ -1705,7 +1752,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                      float4* __restrict__ dk, float4* __restrict__ dv,
                                                      const int32_t* __restrict__ k_ptr, int32_t n_trees,
                                                      int32_t n_blk, int32_t hkv, int32_t group,
-                                                     int32_t kv_chunk) {
+                                                     int32_t kv_chunk, int32_t zero_unseen,
+                                                     uint32_t* __restrict__ kv_cnt, int64_t n_cnt) {
   tc::grid_launch_dependents();     // the KV kernel waits for this one where it reads D or the zeroed rows
   constexpr int LPR = D / 8;        // lanes per row (16 bytes each)
   constexpr int RPL = 32 / LPR;     // rows per warp load
@@ -1763,14 +1811,17 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       }
     }
   }
+  for (int64_t x = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; x < n_cnt; x += int64_t(gridDim.x) * blockDim.x)
+    kv_cnt[x] = 0u;  // bf16 gradients: per-warp item counters of split columns
   if (dk == nullptr) return;
-  // zero the rows of split key columns: one (tree, key tile) unit per block pass
+  // zero the rows of split key columns (and with zero_unseen those of key
+  // tiles no query sees): one (tree, key tile) unit per block pass
   const int64_t per_tile4 = int64_t(kB) * hkv * D / 4;  // float4s of one key tile's rows
   for (int u = blockIdx.x; u < n_trees * n_blk; u += gridDim.x) {
     const int b = u / n_blk, kb = u % n_blk;
     const int32_t* kp = k_ptr + b * (n_blk + 1);
     const int n_col = kp[kb + 1] - kp[kb];
-    if (n_col > 0 && group * n_col <= kv_chunk) continue;  // written whole by its one item
+    if (n_col == 0 ? !zero_unseen : group * n_col <= kv_chunk) continue;  // written whole by one item
     const int64_t base = (int64_t(b) * t_pad + int64_t(kb) * kB) * hkv * D / 4;
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t x = threadIdx.x; x < per_tile4; x += blockDim.x) {
@@ -1791,21 +1842,64 @@ int num_sms() {
   return sms;
 }
 
+// Workspace of the backward: D [B, Hq, T] fp32, and for bf16 gradients the
+// fp32 staging rows of split key columns (dK, dV: [B, T, Hkv, d] each) and the
+// per-warp item counters [B, Hkv, T/128, 16].
+struct BwdWs {
+  uint64_t d, stage_k, stage_v, cnt, n_cnt, total;
+};
+
+BwdWs bwd_ws_layout(int64_t n_trees, int64_t t_pad, int64_t hq, int64_t hkv, int64_t d, bool f32) {
+  BwdWs L{};
+  uint64_t o = 0;
+  L.d = o;
+  o = align256(o + uint64_t(n_trees * hq * t_pad) * 4);
+  if (!f32) {
+    const uint64_t rows = uint64_t(n_trees * t_pad * hkv * d) * 4;
+    L.stage_k = o;
+    o = align256(o + rows);
+    L.stage_v = o;
+    o = align256(o + rows);
+    L.cnt = o;
+    L.n_cnt = uint64_t(n_trees * hkv * ((t_pad + kB - 1) / kB) * 4 * kNWG);
+    o = align256(o + L.n_cnt * 4);
+  }
+  L.total = o;
+  return L;
+}
+
+// Steps per KV work item: a quarter of one SM's share of the (query head,
+// query tile) steps, estimated from the ancestor pairs (a full tile holds
+// 128 x 128 of them), and at least kKvChunkMin, so that the longest key
+// columns (the shared prefixes') are split just enough for the items to
+// balance over the SMs.
+int kv_chunk_for(const tpa_tree_view* tree, int hq, int group, int n_blk, int sms) {
+  const int64_t est_steps = tree->ancestor_pairs * hq / (int64_t(kB) * kB);
+  int64_t chunk = est_steps / (int64_t(sms) * 4);
+  if (chunk < kKvChunkMin) chunk = kKvChunkMin;
+  if (chunk > int64_t(group) * n_blk) chunk = int64_t(group) * n_blk;
+  return int(chunk);
+}
+
 template <int D, bool F32OUT>
 int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const void* q, const void* k,
                const void* v, const void* o, const float* lse, const void* dout, void* dq, void* dk,
                void* dv, void* ws, int hq, int hkv, float scale, cudaStream_t st) {
   const int64_t rows = int64_t(tree->n_trees) * tree->t_pad;
-  float* dvec = static_cast<float*>(ws);  // workspace: D [B, Hq, T] fp32
+  const BwdWs L = bwd_ws_layout(tree->n_trees, tree->t_pad, hq, hkv, D, F32OUT);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* dvec = reinterpret_cast<float*>(wsb + L.d);
+  float* stage_k = F32OUT ? nullptr : reinterpret_cast<float*>(wsb + L.stage_k);
+  float* stage_v = F32OUT ? nullptr : reinterpret_cast<float*>(wsb + L.stage_v);
+  uint32_t* kv_cnt = F32OUT ? nullptr : reinterpret_cast<uint32_t*>(wsb + L.cnt);
   const int64_t n_rows = rows * hq;
   const int G = hq / hkv;
-  // fp32 gradients: long key columns are split into items of kKvChunk steps
-  // that add into zeroed rows; bf16 gradients: one item per column
-  const int kv_chunk = F32OUT ? kKvChunk : G * mask->n_blk;
+  const int kv_chunk = kv_chunk_for(tree, hq, G, mask->n_blk, num_sms());
   bwd_pre_kernel<D><<<num_sms() * 8, 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), tree->n_tokens,
-      tree->t_pad, hq, n_rows, dvec, F32OUT ? static_cast<float4*>(dk) : nullptr,
-      F32OUT ? static_cast<float4*>(dv) : nullptr, mask->k_ptr, tree->n_trees, mask->n_blk, hkv, G, kv_chunk);
+      tree->t_pad, hq, n_rows, dvec, static_cast<float4*>(F32OUT ? dk : static_cast<void*>(stage_k)),
+      static_cast<float4*>(F32OUT ? dv : static_cast<void*>(stage_v)), mask->k_ptr, tree->n_trees, mask->n_blk,
+      hkv, G, kv_chunk, F32OUT ? 1 : 0, kv_cnt, int64_t(L.n_cnt));
   TPA_CUDA_TRY(cudaGetLastError());
 
   CUtensorMap tq, tk, tv, tdo;
@@ -1826,6 +1920,9 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
   prm.q_idx = mask->q_idx;
   prm.qmask = reinterpret_cast<const uint4*>(mask->qmask);
   prm.sched = mask->sched;
+  prm.stage_k = stage_k;
+  prm.stage_v = stage_v;
+  prm.kv_cnt = kv_cnt;
   prm.t_pad = tree->t_pad;
   prm.n_blk = mask->n_blk;
   prm.cap = mask->cap;
@@ -1892,10 +1989,10 @@ int launch_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const 
 TPA_DEFINE_STATUS_READER(tpa_internal_status_bwd, g_status_bwd)
 
 extern "C" uint64_t tpa_tree_attn_bwd_workspace_bytes(int32_t n_trees, int32_t t_pad, int32_t n_heads_q,
-                                                      int32_t head_dim, int32_t grad_dtype) {
-  if (n_trees < 1 || t_pad < 1 || n_heads_q < 1 || head_dim < 1) return 0;
+                                                      int32_t n_heads_kv, int32_t head_dim, int32_t grad_dtype) {
+  if (n_trees < 1 || t_pad < 1 || n_heads_q < 1 || n_heads_kv < 1 || head_dim < 1) return 0;
   if (grad_dtype != TPA_GRAD_F32 && grad_dtype != TPA_GRAD_BF16) return 0;
-  return align256(uint64_t(n_trees) * uint64_t(t_pad) * uint64_t(n_heads_q) * 4);
+  return bwd_ws_layout(n_trees, t_pad, n_heads_q, n_heads_kv, head_dim, grad_dtype == TPA_GRAD_F32).total;
 }
 
 extern "C" int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_view* mask, const void* q,
@@ -1914,7 +2011,7 @@ extern "C" int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_
   if ((al & 15) || (reinterpret_cast<uintptr_t>(workspace) & 255)) return TPA_ERR_INVALID_ARG;
   if (grad_dtype != TPA_GRAD_F32 && grad_dtype != TPA_GRAD_BF16) return TPA_ERR_INVALID_ARG;
   if (workspace_bytes <
-      tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, head_dim, grad_dtype))
+      tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, n_heads_kv, head_dim, grad_dtype))
     return TPA_ERR_BUFFER_TOO_SMALL;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(float(head_dim));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1978,8 +2075,8 @@ extern "C" int tpa_tree_attn_bwd_noalloc(const tpa_tree_view* tree, const tpa_bl
                                          int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
                                          float softmax_scale, int32_t grad_dtype, void* stream) {
   if (!tree) return TPA_ERR_INVALID_ARG;
-  const uint64_t need =
-      tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, head_dim, grad_dtype);
+  const uint64_t need = tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, n_heads_kv,
+                                                         head_dim, grad_dtype);
   if (need == 0) return TPA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return TPA_ERR_BUFFER_TOO_SMALL;
   void* scratch = nullptr;

@@ -415,6 +415,7 @@ int tpa_tree_make_view(const tpa_tree* tree, const void* base, tpa_tree_view* v)
   v->total_tree_tokens = tree->info.total_tree_tokens;
   v->max_token = tree->info.max_token;
   v->reserved_ = 0;
+  v->ancestor_pairs = tree->info.ancestor_pairs;
   v->tokens = reinterpret_cast<const int32_t*>(b + o[kTokens]);
   v->subtree_end = reinterpret_cast<const int32_t*>(b + o[kSubtreeEnd]);
   v->parent = reinterpret_cast<const int32_t*>(b + o[kParent]);

@@ -3,11 +3,11 @@
 On a packed tree the keys of a shared prefix are seen by every query below
 them (tree training page, §树构建过程: shared prefixes are computed once), so
 their dK/dV rows sum contributions from whole subtrees.  In the KV kernel
-such a key tile has a long column of (query head, query tile) steps; with
-fp32 gradients a column of more than 64 steps is split into several work
-items that add into rows the preprocess zeroed, and with bf16 gradients one
-work item walks the whole column.  These tests compare EVERY dQ, dK and dV
-row of such trees with the oracle, element by element:
+such a key tile has a long column of (query head, query tile) steps; a
+column longer than one work item is split into several items that add into
+rows the preprocess zeroed: the outputs for fp32 gradients, fp32 staging rows
+that the last item converts for bf16 gradients.  These tests compare EVERY
+dQ, dK and dV row of such trees with the oracle, element by element:
 
 * a mid-size tree with a 3072-token shared prefix and four branches, at d 128
   (CTA-pair dQ kernel) and d 64 (single-CTA dQ kernel), fp32 and bf16
@@ -29,7 +29,15 @@ from _pipeline import (assert_attn_close, assert_attn_close_bf16_out, pack_and_u
 
 pytestmark = pytest.mark.gpu
 
-KV_CHUNK = 64   # steps per KV work item of the fp32-gradient path
+
+def kv_chunk(pk, hq: int, group: int, t_pad: int) -> int:
+    """Steps per KV work item, by the rule tpa.h states: a quarter of one SM's
+    share of the estimated steps (ancestor pairs of all trees x Hq / 128^2),
+    at least 64, at most a whole column (group x T_pad / 128)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = sum(int((t.depth[:t.n] + 1).sum()) for t in pk.trees)
+    est = pairs * hq // (128 * 128)
+    return int(min(max(est // (sms * 4), 64), group * (t_pad // 128)))
 
 
 @pytest.fixture(scope="module")
@@ -59,8 +67,9 @@ def test_shared_prefix_every_row(tpa, hq, hkv, d):
     pk = oracle.tree_pack(seqs, T)
     assert pk.n_trees == 1 and pk.trees[0].n == T
     # the prefix's first key tile is seen by all 32 query tiles: G * 32 steps,
-    # more than one fp32 work item, so the split-and-add path runs
-    assert (hq // hkv) * _longest_column(pk.trees[0], T) > KV_CHUNK
+    # more than one work item, so the split-and-add paths run (fp32 outputs,
+    # bf16 staging rows)
+    assert (hq // hkv) * _longest_column(pk.trees[0], T) > kv_chunk(pk, hq, hq // hkv, T)
     tree, dtree, mask = pack_and_upload(tpa, seqs, T)
     t = pk.trees[0]
     bufs = {gdt: tuple(torch.full(x, float("nan"), dtype=gdt, device="cuda")
@@ -93,7 +102,7 @@ def test_workload_first_tree_one_kv_group(tpa, cid):
     G = cfg.n_heads_q // cfg.n_heads_kv
     pk = oracle.tree_pack(seqs, T)
     t = pk.trees[0]
-    assert G * _longest_column(t, T) > KV_CHUNK
+    assert G * _longest_column(t, T) > kv_chunk(pk, cfg.n_heads_q, G, T)
     tree, dtree, mask = pack_and_upload(tpa, seqs, T)
     q, k, v, do = workload_tensors(cid, tree.n_trees, T)
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()

@@ -53,6 +53,7 @@ def _compare(seqs, mb, tpa):
     assert info.ancestor_pairs == sum(ancestor_pairs(t) for t in pk.trees)
     assert info.max_token == max(max(s) for s in seqs)
     assert tree.host_view().max_token == info.max_token
+    assert tree.host_view().ancestor_pairs == info.ancestor_pairs
     a = tree.arrays()
     for b, t in enumerate(pk.trees):
         n = t.n
@@ -142,9 +143,14 @@ def test_blockmask_layout(tpa):
     assert L.tpa_blockmask_bytes(0, 128) == 0
     assert L.tpa_blockmask_bytes(1, 100) == 0
     assert L.tpa_blockmask_bytes(2, 1024) > 2 * 8 * 8
-    assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 64, 0) >= 4 * 128 * 4          # D only
-    assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 64, 1) >= 4 * 128 * 4
-    assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 64, 7) == 0
+    # fp32 gradients: D [B, Hq, T] fp32 only
+    assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 2, 64, 0) == 4 * 128 * 4
+    # bf16 gradients: + fp32 staging dK, dV [B, T, Hkv, d] + counters [B, Hkv, T/128, 16]
+    ws = L.tpa_tree_attn_bwd_workspace_bytes(2, 256, 4, 2, 64, 1)
+    assert ws >= 2 * 4 * 256 * 4 + 2 * (2 * 256 * 2 * 64 * 4) + 2 * 2 * 2 * 16 * 4
+    assert ws < 2 * 4 * 256 * 4 + 2 * (2 * 256 * 2 * 64 * 4) + 2 * 2 * 2 * 16 * 4 + 4 * 256
+    assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 2, 64, 7) == 0
+    assert L.tpa_tree_attn_bwd_workspace_bytes(1, 128, 4, 0, 64, 0) == 0
 
 
 def test_logprob_calls_refuse_labels_past_vocab(tpa):
