@@ -107,6 +107,7 @@ PROTOTYPES = {
 }
 
 _LIB = None
+_DEBUG_LIB = None
 
 
 class TpaError(RuntimeError):
@@ -133,6 +134,27 @@ def lib(build_if_missing: bool = True) -> C.CDLL:
         f.restype = res
         f.argtypes = args
     _LIB = L
+    return L
+
+
+def debug_lib(build_if_missing: bool = True) -> C.CDLL:
+    """The TPA_DEBUG variant, libtpa_debug.so: the same ABI, with kernels that
+    check every metadata index they read from a tree view before using it as
+    an address (a bad one makes tpa_sync_status return TPA_ERR_INVALID_ARG)."""
+    global _DEBUG_LIB
+    if _DEBUG_LIB is not None:
+        return _DEBUG_LIB
+    path = _build.DEBUG_LIB_PATH
+    if build_if_missing and (_build.is_stale(path) or not os.path.exists(path)):
+        _build.build(debug=True)
+    if not os.path.exists(path):
+        raise ImportError(f"libtpa_debug.so not found at {path}; run prefix_shared_tree_attention_gb300.build --debug")
+    L = C.CDLL(path)
+    for name, (res, args) in PROTOTYPES.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _DEBUG_LIB = L
     return L
 
 

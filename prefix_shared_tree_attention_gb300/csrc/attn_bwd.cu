@@ -2000,6 +2000,7 @@ extern "C" int tpa_tree_attn_bwd(const tpa_tree_view* tree, const tpa_blockmask_
                                  const void* dout, void* dq, void* dk, void* dv, void* workspace,
                                  uint64_t workspace_bytes, int32_t n_heads_q, int32_t n_heads_kv,
                                  int32_t head_dim, float softmax_scale, int32_t grad_dtype, void* stream) {
+  TPA_NVTX_RANGE("tpa_tree_attn_bwd");
   const int rc = tpa_internal_check_attn_args(tree, mask, n_heads_q, n_heads_kv, head_dim);
   if (rc != TPA_OK) return rc;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return TPA_ERR_INVALID_ARG;
@@ -2074,6 +2075,7 @@ extern "C" int tpa_tree_attn_bwd_noalloc(const tpa_tree_view* tree, const tpa_bl
                                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
                                          int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
                                          float softmax_scale, int32_t grad_dtype, void* stream) {
+  TPA_NVTX_RANGE("tpa_tree_attn_bwd_noalloc");
   if (!tree) return TPA_ERR_INVALID_ARG;
   const uint64_t need = tpa_tree_attn_bwd_workspace_bytes(tree->n_trees, tree->t_pad, n_heads_q, n_heads_kv,
                                                          head_dim, grad_dtype);

@@ -647,6 +647,7 @@ extern "C" int tpa_tree_attn_fwd(const tpa_tree_view* tree, const tpa_blockmask_
                                  const void* q, const void* k, const void* v, void* o, float* lse,
                                  int32_t n_heads_q, int32_t n_heads_kv, int32_t head_dim,
                                  float softmax_scale, void* stream) {
+  TPA_NVTX_RANGE("tpa_tree_attn_fwd");
   const int rc = tpa_internal_check_attn_args(tree, mask, n_heads_q, n_heads_kv, head_dim);
   if (rc != TPA_OK) return rc;
   if (!q || !k || !v || !o || !lse) return TPA_ERR_INVALID_ARG;

@@ -27,6 +27,7 @@
 #include <vector>
 
 #include "tpa.h"
+#include "internal.h"
 
 namespace {
 
@@ -183,6 +184,7 @@ int kk(const int64_t* w, int32_t n, int64_t capacity, int32_t min_groups, int32_
 extern "C" int tpa_balance(const int64_t* weights, int32_t n, int64_t capacity, int32_t min_groups,
                            int32_t groups_divisor, int32_t algorithm, int32_t* group_of, int32_t* n_groups,
                            int32_t* algorithm_used) {
+  TPA_NVTX_RANGE("tpa_balance");
   if (!group_of || !n_groups) return TPA_ERR_INVALID_ARG;
   if (algorithm != TPA_BALANCE_FFD && algorithm != TPA_BALANCE_KK) return TPA_ERR_INVALID_ARG;
   int rc = check_args(weights, n, capacity, min_groups, groups_divisor);

@@ -138,6 +138,7 @@ TPA_DEFINE_STATUS_READER(tpa_internal_status_classify, g_status_classify)
 
 extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask_view* mask,
                                   void* stream) {
+  TPA_NVTX_RANGE("tpa_block_classify");
   if (!tree || !mask || !tree->subtree_end || !tree->n_tokens || !mask->cls || !mask->q_ptr ||
       !mask->q_idx || !mask->k_ptr || !mask->k_idx || !mask->qmask || !mask->sched)
     return TPA_ERR_INVALID_ARG;

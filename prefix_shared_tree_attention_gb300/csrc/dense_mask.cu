@@ -105,6 +105,7 @@ extern "C" uint64_t tpa_dense_mask_bytes(int32_t n_trees, int32_t t_pad, int32_t
 
 extern "C" int tpa_dense_mask(const tpa_tree_view* tree, void* out, uint64_t out_bytes, int32_t format,
                               int32_t invert, void* stream) {
+  TPA_NVTX_RANGE("tpa_dense_mask");
   if (!tree || !out || !tree->subtree_end || tree->n_trees < 1 || tree->n_trees > 65535 || tree->t_pad < 1 ||
       tree->t_pad % TPA_BLOCK_SIZE != 0)
     return TPA_ERR_INVALID_ARG;

@@ -14,6 +14,28 @@ enum : unsigned int {
   TPA_DEV_BAD_INPUT = 4,  // an input was outside its range (e.g. a label id >= vocab); it was skipped
 };
 
+// Debug builds (TPA_DEBUG=1, libtpa_debug.so) check every metadata index a
+// kernel reads from a tree view before using it as an address: a bad one is
+// recorded in the translation unit's status word (TPA_DEV_BAD_INPUT, which
+// tpa_sync_status reports as TPA_ERR_INVALID_ARG) and its access is skipped.
+// Release builds compile the checks away (dbg_ok is always true there).
+#ifndef TPA_DEBUG
+#define TPA_DEBUG 0
+#endif
+
+__device__ __forceinline__ bool dbg_ok(bool ok, unsigned int* status) {
+#if TPA_DEBUG
+  if (!ok) {
+    atomicOr(status, TPA_DEV_BAD_INPUT);
+    return false;
+  }
+#else
+  (void)ok;
+  (void)status;
+#endif
+  return true;
+}
+
 #define TPA_CUDA_TRY(expr)                        \
   do {                                            \
     if ((expr) != cudaSuccess) {                  \

@@ -4,6 +4,23 @@
 
 #include "tpa.h"
 
+// NVTX range around a library call, named after it, so that a timeline
+// profiler shows where each call starts and ends on the host (header-only
+// NVTX v3; without a profiler attached it costs a load and a branch).  Host
+// builds without the CUDA headers get no ranges.
+#if __has_include(<nvtx3/nvToolsExt.h>)
+#include <nvtx3/nvToolsExt.h>
+struct TpaNvtxRange {
+  explicit TpaNvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~TpaNvtxRange() { nvtxRangePop(); }
+  TpaNvtxRange(const TpaNvtxRange&) = delete;
+  TpaNvtxRange& operator=(const TpaNvtxRange&) = delete;
+};
+#define TPA_NVTX_RANGE(name) TpaNvtxRange tpa_nvtx_range_(name)
+#else
+#define TPA_NVTX_RANGE(name) ((void)0)
+#endif
+
 uint64_t tpa_internal_blob_bytes(const tpa_tree* tree);
 
 // Each CUDA translation unit keeps its own device status word; these read

@@ -261,8 +261,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         row_to_pos(p, row, b, pos);
         c0 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos];
         c1 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos + 1];
+        if (!dbg_ok(c0 >= 0 && c0 <= c1 && c1 <= p.t_pad, &g_status_lmh)) c1 = c0;
         for (int c = c0; c < c1; ++c) {
-          const int tok = p.tokens[int64_t(b) * p.t_pad + p.child_pos[int64_t(b) * p.t_pad + c]];
+          const int cp = p.child_pos[int64_t(b) * p.t_pad + c];
+          if (!dbg_ok(cp > pos && cp < p.t_pad, &g_status_lmh)) {
+            c1 = c;  // labels from here on are not read
+            break;
+          }
+          const int tok = p.tokens[int64_t(b) * p.t_pad + cp];
           lmin = min(lmin, tok);
           lmax = max(lmax, tok);
         }
@@ -364,6 +370,7 @@ __global__ void __launch_bounds__(256) lmh_combine_kernel(const LmhParams p, con
     return;
   }
   const int64_t row = p.tok_base[b] + pos;
+  if (!dbg_ok(row >= 0 && row < p.rows, &g_status_lmh)) return;
   Stats a{-INFINITY, 0.f, 0.f};
   for (int vc = 0; vc < p.n_vc; ++vc) {
     const float4 o = p.part[row * p.n_vc + vc];
@@ -374,8 +381,10 @@ __global__ void __launch_bounds__(256) lmh_combine_kernel(const LmhParams p, con
   if (parent[at] < 0) pos_logp[at] = 0.f;  // no parent row: no label
   const int c0 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos];
   const int c1 = p.child_off[int64_t(b) * (p.t_pad + 1) + pos + 1];
+  if (!dbg_ok(c0 >= 0 && c0 <= c1 && c1 <= p.t_pad, &g_status_lmh)) return;
   for (int c = c0; c < c1; ++c) {
     const int cp = p.child_pos[int64_t(b) * p.t_pad + c];
+    if (!dbg_ok(cp > pos && cp < p.n_tokens[b], &g_status_lmh)) continue;
     const int tok = p.tokens[int64_t(b) * p.t_pad + cp];
     pos_logp[int64_t(b) * p.t_pad + cp] =
         (tok >= 0 && tok < p.vocab) ? p.pair_logit[int64_t(b) * p.t_pad + cp] - lse : __int_as_float(0x7fc00000);
@@ -408,6 +417,7 @@ extern "C" int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const voi
                                             int32_t hidden_size, int32_t vocab, void* workspace,
                                             uint64_t workspace_bytes, float* pos_logp, float* pos_entropy,
                                             float* seq_logp, float* seq_entropy, void* stream) {
+  TPA_NVTX_RANGE("tpa_lm_head_logprobs_entropy");
   if (!tree || !hidden || !weight || !workspace || !pos_logp || !pos_entropy || !seq_logp || !seq_entropy)
     return TPA_ERR_INVALID_ARG;
   if (tree->n_trees < 1 || tree->t_pad < 1 || tree->n_seqs < 1 || tree->total_tree_tokens < 1)

@@ -107,13 +107,15 @@ __device__ __forceinline__ void acc_add1(Acc& a, uint16_t raw) {
 // grid (T_pad, B): CTA (p, b) handles tree position p of tree b.
 __global__ void __launch_bounds__(kRowThreads) row_kernel(
     const uint16_t* __restrict__ logits, int64_t row_stride, int32_t layout, int32_t vocab,
-    int32_t t_pad, const int32_t* __restrict__ n_tokens, const int64_t* __restrict__ tok_base,
-    const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
-    const int32_t* __restrict__ child_off, const int32_t* __restrict__ child_pos,
-    float* __restrict__ pos_logp, float* __restrict__ pos_entropy) {
+    int32_t t_pad, int64_t total_rows, const int32_t* __restrict__ n_tokens,
+    const int64_t* __restrict__ tok_base, const int32_t* __restrict__ tokens,
+    const int32_t* __restrict__ parent, const int32_t* __restrict__ child_off,
+    const int32_t* __restrict__ child_pos, float* __restrict__ pos_logp,
+    float* __restrict__ pos_entropy) {
   const int p = blockIdx.x, b = blockIdx.y;
   const int64_t at = int64_t(b) * t_pad + p;
   const int n = n_tokens[b];
+  if (!dbg_ok(n >= 0 && n <= t_pad, &g_status_logprobs)) return;
   if (p >= n) {  // padding position
     if (threadIdx.x == 0) {
       pos_logp[at] = 0.f;
@@ -122,6 +124,7 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(
     return;
   }
   const int64_t row = (layout == TPA_LOGITS_COMPACT) ? tok_base[b] + p : int64_t(b) * t_pad + p;
+  if (layout == TPA_LOGITS_COMPACT && !dbg_ok(row >= 0 && row < total_rows, &g_status_logprobs)) return;
   const uint16_t* x = logits + row * row_stride;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int nvec = vocab >> 3;
@@ -173,8 +176,10 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(
   __syncthreads();
   const int c0 = child_off[int64_t(b) * (t_pad + 1) + p];
   const int c1 = child_off[int64_t(b) * (t_pad + 1) + p + 1];
+  if (!dbg_ok(c0 >= 0 && c0 <= c1 && c1 <= t_pad, &g_status_logprobs)) return;
   for (int c = c0 + threadIdx.x; c < c1; c += kRowThreads) {
     const int cp = child_pos[int64_t(b) * t_pad + c];
+    if (!dbg_ok(cp > p && cp < n, &g_status_logprobs)) continue;  // a child follows its parent
     const int tok = tokens[int64_t(b) * t_pad + cp];
     if (uint32_t(tok) < uint32_t(vocab)) {
       const float xl = __uint_as_float(uint32_t(x[tok]) << 16);
@@ -189,16 +194,23 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(
 // grid (n_seqs): per input sequence s at token t,
 //   seq_entropy[t] = pos_entropy[g_t],  seq_logp[t] = pos_logp[g_{t+1}] (0 at the end).
 __global__ void __launch_bounds__(256) seq_gather_kernel(
-    int32_t t_pad, const int32_t* __restrict__ seq_tree, const int64_t* __restrict__ seq_off,
+    int32_t t_pad, int32_t n_trees, int64_t total_seq_tokens, const int32_t* __restrict__ n_tokens,
+    const int32_t* __restrict__ seq_tree, const int64_t* __restrict__ seq_off,
     const int32_t* __restrict__ seq_pos, const float* __restrict__ pos_logp,
     const float* __restrict__ pos_entropy, float* __restrict__ seq_logp,
     float* __restrict__ seq_entropy) {
   const int s = blockIdx.x;
   const int64_t o0 = seq_off[s], o1 = seq_off[s + 1];
-  const int64_t base = int64_t(seq_tree[s]) * t_pad;
+  const int tr = seq_tree[s];
+  if (!dbg_ok(tr >= 0 && tr < n_trees && o0 >= 0 && o0 <= o1 && o1 <= total_seq_tokens, &g_status_logprobs))
+    return;
+  const int64_t base = int64_t(tr) * t_pad;
+  const int n = TPA_DEBUG ? n_tokens[tr] : t_pad;
   for (int64_t i = o0 + threadIdx.x; i < o1; i += blockDim.x) {
-    seq_entropy[i] = pos_entropy[base + seq_pos[i]];
-    seq_logp[i] = (i + 1 < o1) ? pos_logp[base + seq_pos[i + 1]] : 0.f;
+    const int g0 = seq_pos[i], g1 = (i + 1 < o1) ? seq_pos[i + 1] : 0;
+    if (!dbg_ok(g0 >= 0 && g0 < n && g1 >= 0 && g1 < n, &g_status_logprobs)) continue;
+    seq_entropy[i] = pos_entropy[base + g0];
+    seq_logp[i] = (i + 1 < o1) ? pos_logp[base + g1] : 0.f;
   }
 }
 
@@ -210,6 +222,7 @@ extern "C" int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* 
                                          int64_t row_stride, int32_t layout, int32_t vocab,
                                          float* pos_logp, float* pos_entropy, float* seq_logp,
                                          float* seq_entropy, void* stream) {
+  TPA_NVTX_RANGE("tpa_tree_logprobs_entropy");
   if (!tree || !logits || !pos_logp || !pos_entropy || !seq_logp || !seq_entropy) return TPA_ERR_INVALID_ARG;
   if (vocab < 1 || row_stride < vocab || (row_stride & 7) || (reinterpret_cast<uintptr_t>(logits) & 15))
     return TPA_ERR_INVALID_ARG;
@@ -218,8 +231,8 @@ extern "C" int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* 
   if (tree->max_token < 0 || tree->max_token >= vocab) return TPA_ERR_INVALID_ARG;  // a label past the row
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   row_kernel<<<dim3(tree->t_pad, tree->n_trees), kRowThreads, 0, st>>>(
-      static_cast<const uint16_t*>(logits), row_stride, layout, vocab, tree->t_pad, tree->n_tokens,
-      tree->tok_base, tree->tokens, tree->parent, tree->child_off, tree->child_pos, pos_logp,
+      static_cast<const uint16_t*>(logits), row_stride, layout, vocab, tree->t_pad, tree->total_tree_tokens,
+      tree->n_tokens, tree->tok_base, tree->tokens, tree->parent, tree->child_off, tree->child_pos, pos_logp,
       pos_entropy);
   TPA_CUDA_TRY(cudaGetLastError());
   return tpa_internal_seq_gather(tree, pos_logp, pos_entropy, seq_logp, seq_entropy, stream);
@@ -228,9 +241,9 @@ extern "C" int tpa_tree_logprobs_entropy(const tpa_tree_view* tree, const void* 
 int tpa_internal_seq_gather(const tpa_tree_view* tree, const float* pos_logp, const float* pos_entropy,
                             float* seq_logp, float* seq_entropy, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  seq_gather_kernel<<<tree->n_seqs, 256, 0, st>>>(tree->t_pad, tree->seq_tree, tree->seq_off,
-                                                  tree->seq_pos, pos_logp, pos_entropy, seq_logp,
-                                                  seq_entropy);
+  seq_gather_kernel<<<tree->n_seqs, 256, 0, st>>>(tree->t_pad, tree->n_trees, tree->total_seq_tokens,
+                                                  tree->n_tokens, tree->seq_tree, tree->seq_off, tree->seq_pos,
+                                                  pos_logp, pos_entropy, seq_logp, seq_entropy);
   TPA_CUDA_TRY(cudaGetLastError());
   return TPA_OK;
 }

@@ -350,6 +350,7 @@ extern "C" {
 
 int tpa_tree_pack(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
                   int32_t max_tokens_per_mb, tpa_tree** out) {
+  TPA_NVTX_RANGE("tpa_tree_pack");
   try {
     return pack_impl(tokens, seq_offsets, n_seqs, max_tokens_per_mb, out);
   } catch (const std::bad_alloc&) {
@@ -379,6 +380,7 @@ int tpa_extract_sequences(const int32_t* input_ids, const uint8_t* attention_mas
 
 int tpa_tree_pack_padded(const int32_t* input_ids, const uint8_t* attention_mask, int32_t n_rows,
                          int32_t row_len, int32_t max_tokens_per_mb, tpa_tree** out) {
+  TPA_NVTX_RANGE("tpa_tree_pack_padded");
   if (out) *out = nullptr;
   if (!input_ids || !attention_mask || !out || n_rows < 1 || row_len < 1) return TPA_ERR_INVALID_ARG;
   try {

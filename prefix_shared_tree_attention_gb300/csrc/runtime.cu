@@ -61,6 +61,7 @@ int tpa_device_check(void) {
 }
 
 int tpa_tree_upload(const tpa_tree* tree, void* dev_blob, uint64_t dev_bytes, void* stream) {
+  TPA_NVTX_RANGE("tpa_tree_upload");
   if (!tree || !dev_blob || (reinterpret_cast<uintptr_t>(dev_blob) & 255)) return TPA_ERR_INVALID_ARG;
   const uint64_t need = tpa_internal_blob_bytes(tree);
   if (dev_bytes < need) return TPA_ERR_BUFFER_TOO_SMALL;
@@ -95,6 +96,7 @@ int tpa_blockmask_make_view(void* base, int32_t n_trees, int32_t t_pad, tpa_bloc
 }
 
 int tpa_sync_status(void* stream) {
+  TPA_NVTX_RANGE("tpa_sync_status");
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     (void)cudaGetLastError();
     return TPA_ERR_CUDA;

@@ -45,6 +45,30 @@ def assert_attn_close_bf16_out(got: torch.Tensor, ref: torch.Tensor, what: str) 
     assert excess <= 0 and rel <= ATTN_REL_L2, f"{what}: excess {excess:.3e}, rel-L2 {rel:.3e}"
 
 
+# Canary guard bands: an output buffer is allocated with GUARD elements on
+# each side holding a fixed bit pattern, the call writes the interior view,
+# and check_guards() verifies afterwards that no kernel wrote past either end.
+GUARD = 4096
+_PATTERN = {1: (torch.uint8, 0xA5), 2: (torch.int16, 0x7FA5), 4: (torch.int32, 0x7FA5A5A5)}
+
+
+def guarded(shape, dtype, device="cuda"):
+    """(backing buffer, interior view of ``shape``) with canaries on both sides."""
+    n = 1
+    for x in shape:
+        n *= int(x)
+    buf = torch.empty(n + 2 * GUARD, dtype=dtype, device=device)
+    ity, pat = _PATTERN[buf.element_size()]
+    buf.view(ity).fill_(pat)
+    return buf, buf[GUARD:GUARD + n].view(tuple(shape))
+
+
+def check_guards(buf: torch.Tensor, what: str) -> None:
+    ity, pat = _PATTERN[buf.element_size()]
+    raw = buf.view(ity)
+    assert torch.all(raw[:GUARD] == pat) and torch.all(raw[-GUARD:] == pat), f"{what}: write outside the buffer"
+
+
 def pack_and_upload(tpa, seqs, mb, device="cuda"):
     tree = tpa.tree_pack(seqs, mb)
     dtree = tree.upload(device)

@@ -8,7 +8,7 @@ import torch
 import oracle
 from oracle.mask import _mask_rows, dense_mask
 from synth import random_small_sequences
-from _pipeline import pack_and_upload, workload
+from _pipeline import check_guards, guarded, pack_and_upload, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -30,10 +30,17 @@ def _bits_to_bool(words: np.ndarray) -> np.ndarray:
 def _check_all(tpa, seqs, mb):
     pk = oracle.tree_pack(seqs, mb)
     tree, dtree, _ = pack_and_upload(tpa, seqs, mb)
-    u8 = tpa.dense_mask(dtree, "u8").cpu().numpy()
-    u8i = tpa.dense_mask(dtree, "u8", invert=True).cpu().numpy()
-    bits = _bits_to_bool(tpa.dense_mask(dtree, "bits").cpu().numpy())
-    bitsi = _bits_to_bool(tpa.dense_mask(dtree, "bits", invert=True).cpu().numpy())
+    B = tree.n_trees
+    got = {}
+    for fmt, shape, dt in (("u8", (B, mb, mb), torch.uint8), ("bits", (B, mb, mb // 32), torch.int32)):
+        for inv in (False, True):
+            buf, view = guarded(shape, dt)           # inside canary guard bands
+            tpa.dense_mask(dtree, fmt, invert=inv, out=view)
+            torch.cuda.synchronize()
+            check_guards(buf, f"{fmt} invert={inv}")
+            got[fmt, inv] = view.cpu().numpy()
+    u8, u8i = got["u8", False], got["u8", True]
+    bits, bitsi = _bits_to_bool(got["bits", False]), _bits_to_bool(got["bits", True])
     for b, t in enumerate(pk.trees):
         ref = dense_mask(t, mb)
         assert np.array_equal(u8[b], ref.astype(np.uint8)), f"tree {b}: u8"

@@ -13,8 +13,8 @@ import torch
 import oracle
 from oracle.mask import _mask_rows, block_classes, block_csr
 from synth import CONFIGS, make_logits, random_small_sequences
-from _pipeline import (LOGP_ABS, assert_attn_close, assert_attn_close_bf16_out, leaf_nodes, node_rows, pack_and_upload,
-                       random_inputs, workload, workload_tensors)
+from _pipeline import (LOGP_ABS, assert_attn_close, assert_attn_close_bf16_out, check_guards, guarded, leaf_nodes,
+                       node_rows, pack_and_upload, random_inputs, workload, workload_tensors)
 
 pytestmark = pytest.mark.gpu
 
@@ -126,10 +126,17 @@ def _run_full_case(tpa, seqs, T, hq, hkv, d, seed, check_bwd=True):
     tree, dtree, mask = pack_and_upload(tpa, seqs, T)
     B = tree.n_trees
     (q, k, v, do), (qc, kc, vc, doc) = random_inputs(B, T, hq, hkv, d, seed)
-    o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    # every output inside canary guard bands
+    ob, o = guarded(q.shape, torch.bfloat16)
+    lb, lse = guarded((B, hq, T), torch.float32)
+    tpa.tree_attn_fwd(dtree, mask, q, k, v, out=o, lse=lse)
+    gb = []
     if check_bwd:
-        dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do)
+        gb = [guarded(x.shape, torch.float32) for x in (q, k, v)]
+        dq, dk, dv = tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, out=tuple(g[1] for g in gb))
     tpa.sync_status()
+    for name, (buf, _) in zip(("O", "LSE", "dQ", "dK", "dV"), [(ob, o), (lb, lse)] + gb):
+        check_guards(buf, name)
     for b, t in enumerate(pk.trees):
         O, L = oracle.attn_forward(t, qc[b], kc[b], vc[b], t_pad=T)
         assert_attn_close(o[b], O, f"O tree {b}")
@@ -268,8 +275,12 @@ def test_attention_workload_sampled(tpa, cid, grad):
 # ---------------------------------------------------------------- log-probs / entropy
 
 def _check_logprobs(tpa, pk, seqs, dtree, logits, layout, row_base, seq_ids, pos_sample):
-    pl, pe, sl, se = tpa.tree_logprobs_entropy(dtree, logits, layout=layout)
+    B, T, N = dtree.info.n_trees, dtree.info.t_pad, dtree.info.total_seq_tokens
+    outs = [guarded(s_, torch.float32) for s_ in ((B, T), (B, T), (N,), (N,))]
+    pl, pe, sl, se = tpa.tree_logprobs_entropy(dtree, logits, layout=layout, out=tuple(g[1] for g in outs))
     tpa.sync_status()
+    for name, (buf, _) in zip(("pos_logp", "pos_entropy", "seq_logp", "seq_entropy"), outs):
+        check_guards(buf, name)
     rows_needed = sorted({int(row_base[int(pk.seq_tree[s])] + p) for s in seq_ids for p in pk.seq_pos[s]} |
                          {int(row_base[b] + p) for b, ps in pos_sample.items() for p in ps} |
                          {int(row_base[b] + pk.trees[b].parent[p]) for b, ps in pos_sample.items() for p in ps

@@ -24,8 +24,8 @@ import torch
 
 import oracle
 from oracle.mask import block_classes
-from _pipeline import (assert_attn_close, assert_attn_close_bf16_out, pack_and_upload, random_inputs,
-                       workload, workload_tensors)
+from _pipeline import (assert_attn_close, assert_attn_close_bf16_out, check_guards, guarded, pack_and_upload,
+                       random_inputs, workload, workload_tensors)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,15 +72,22 @@ def test_shared_prefix_every_row(tpa, hq, hkv, d):
     assert (hq // hkv) * _longest_column(pk.trees[0], T) > kv_chunk(pk, hq, hq // hkv, T)
     tree, dtree, mask = pack_and_upload(tpa, seqs, T)
     t = pk.trees[0]
-    bufs = {gdt: tuple(torch.full(x, float("nan"), dtype=gdt, device="cuda")
-                       for x in ((1, T, hq, d), (1, T, hkv, d), (1, T, hkv, d)))
-            for gdt in (torch.float32, torch.bfloat16)}
+    # outputs start as NaN (rows no item writes would show) inside canary guard bands
+    guards = {gdt: [guarded(x, gdt) for x in ((1, T, hq, d), (1, T, hkv, d), (1, T, hkv, d))]
+              for gdt in (torch.float32, torch.bfloat16)}
+    for gs in guards.values():
+        for _, view in gs:
+            view.fill_(float("nan"))
+    bufs = {gdt: tuple(view for _, view in gs) for gdt, gs in guards.items()}
     for call, seed in enumerate((31, 32)):   # same output buffers, new inputs
         (q, k, v, do), (qc, kc, vc, doc) = random_inputs(1, T, hq, hkv, d, seed)
         o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
         got = {gdt: tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, grad_dtype=gdt, out=bufs[gdt])
                for gdt in bufs}
         tpa.sync_status()
+        for gdt, gs in guards.items():
+            for name, (buf, _) in zip(("dQ", "dK", "dV"), gs):
+                check_guards(buf, f"{gdt} {name}")
         O, _ = oracle.attn_forward(t, qc[0], kc[0], vc[0], t_pad=T)
         assert_attn_close(o[0], O, f"call {call} O")
         ref = oracle.attn_backward(t, qc[0], kc[0], vc[0], doc[0], t_pad=T)
