@@ -1164,14 +1164,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // MMA; the copies of both CTAs complete on its barriers, its MMA completions
 // are multicast to both CTAs, and each compute warp signals it once.
 //
-// TMEM (per CTA): S in [0, 128), dP in [128, 256), packed dS in two 64-column
-// buffers [256, 384), the dQ accumulator in [384, 512).  S(j+1) is issued as
-// soon as the compute warps have read S(j), at the start of step j's
-// exponentials, dP(j+1) once they have read dP(j), and dQ(j) once dS(j) is
-// packed; an MMA's completion is only seen a few hundred cycles after its
-// issue, and this order keeps the next step's S and dP ahead of the compute
-// warps, so that the tensor pipe, not that latency, sets the pace.  S and dP
-// are issued by one warp, dQ by another.
+// TMEM (per CTA): S in [0, 128), dP in [128, 256), packed dS in [256, 320),
+// the item's dO tile in [320, 384) and the dQ accumulator in [384, 512).
+// S(j+1) is issued as soon as the compute warps have read S(j), at the
+// start of step j's exponentials, dP(j+1) once they have read dP(j), and
+// dQ(j) once dS(j) is packed; an MMA's completion is only seen a few hundred
+// cycles after its issue, and this order keeps the next step's S and dP
+// ahead of the compute warps, so that the tensor pipe, not that latency,
+// sets the pace.  S and dP are issued by one warp, dQ by another.  At an
+// item's start its dO tile is copied from shared memory into TMEM (the A
+// operand of its dP MMAs), which frees the single shared-memory dO buffer at
+// once: the next item's dO is loaded a whole item ahead, and an item's first
+// dP does not wait for it.
 
 constexpr int kNWarpsC = 4 * kNWG;  // compute warps per CTA
 // One MMA takes 64 cycles of the pair's tensor pipes but about as long to
@@ -1249,8 +1253,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
   uint64_t* dp_full = s_full + 1;
   uint64_t* s_free = s_full + 2;
   uint64_t* dp_free = s_full + 3;
-  uint64_t* ds_ready = s_full + 4;  // [2]
-  uint64_t* ds_free = s_full + 6;   // [2]
+  uint64_t* ds_ready = s_full + 4;  // (one packed-dS buffer: slot 5 is unused)
+  uint64_t* ds_free = s_full + 6;   // (slot 7 is unused)
   uint64_t* dq_final = s_full + 8;
   uint64_t* dq_free = s_full + 9;
   uint64_t* drain = s_full + 10;              // [2]: one per issuing warp
@@ -1263,7 +1267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.hq / p.hkv;
-  constexpr uint32_t T_S = 0, T_DP = 128, T_DS = 256, T_DQ = 384;
+  constexpr uint32_t T_S = 0, T_DP = 128, T_DS = 256, T_DO = 320, T_DQ = 384;
   // item-slot consumers, all arriving on the even CTA: its two MMA warps and
   // compute warps, the odd CTA's producer and compute warps
   constexpr int NCONS2 = 2 * (1 + kNWarpsC) + 1;
@@ -1392,37 +1396,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
       ++nq;
       return true;
     };
+    // dO of an item goes into the one shared-memory buffer, which frees as
+    // soon as the item's start has copied it into TMEM.
+    auto load_do = [&](const Item& X) -> bool {
+      int xb, xhp, xqb;
+      dq2_coords(p, X.it, xb, xhp, xqb);
+      if (!wait1(do_empty, (nd & 1) ^ 1)) return false;
+      if (lead) tc::mbar_arrive_expect_tx(do_full, 2 * TILE);  // dO of both CTAs
+      const uint32_t lb = tc::peer_addr(do_full, 0);
+      for (int c = 0; c < 2; ++c)
+        tc::tma_load_3d_pair(sDO + c * kChunk, &tm_do, lb, c * 64, 2 * xhp + int(crank), xb * p.t_pad + xqb * kB);
+      ++nd;
+      return true;
+    };
     Item I, J;
     ok = lead ? take(0, I) : read(0, I);
-    if (ok && I.it >= 0 && I.n > 0) ok = load_q(I);
+    if (ok && I.it >= 0 && I.n > 0) ok = load_q(I) && load_do(I);
     for (int k = 0; ok && I.it >= 0; ++k) {
       int b, hp, qb;
       dq2_coords(p, I.it, b, hp, qb);
-      const int h = 2 * hp + int(crank);
       const int g = (2 * hp) / G;
-      // dO(k) and the next item's Q after this item's first K and V tiles:
-      // dO waits for the previous item's last dP, and the first S and dP of
-      // this item should not wait behind that.
-      auto load_do_and_next = [&]() -> bool {
-        if (I.n > 0) {
-          if (!wait1(do_empty, (nd & 1) ^ 1)) return false;
-          if (lead) tc::mbar_arrive_expect_tx(do_full, 2 * TILE);  // dO of both CTAs
-          const uint32_t lb = tc::peer_addr(do_full, 0);
-          for (int c = 0; c < 2; ++c)
-            tc::tma_load_3d_pair(sDO + c * kChunk, &tm_do, lb, c * 64, h, b * p.t_pad + qb * kB);
-          ++nd;
-        }
+      // The next item's Q and dO after this item's first K and V tiles, so
+      // that this item's first S and dP do not wait behind them.
+      auto load_next = [&]() -> bool {
         if (!(lead ? take(k + 1, J) : read(k + 1, J))) return false;
-        if (J.it >= 0 && J.n > 0) {
-          if (!load_q(J)) return false;
-          int nb, nhp, nqb;  // and its dO into L2 for when the buffer frees
-          dq2_coords(p, J.it, nb, nhp, nqb);
-          for (int c = 0; c < 2; ++c)
-            tc::tma_prefetch_3d(&tm_do, c * 64, 2 * nhp + int(crank), nb * p.t_pad + nqb * kB);
-        }
+        if (J.it >= 0 && J.n > 0 && !(load_q(J) && load_do(J))) return false;
         return true;
       };
-      if (I.n == 0 && !(ok = load_do_and_next())) break;
+      if (I.n == 0 && !(ok = load_next())) break;
       const int32_t* list = p.q_idx + int64_t(b) * p.cap + I.e0;
       int entry = I.n > 0 ? list[0] : 0;
       for (int j = 0; ok && j < I.n; ++j) {
@@ -1452,7 +1453,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
           tc::tma_load_3d_pair(st + PIECE, &tm_v64, lb, 64, g, mine);
         }
         ++gv;
-        if (j == 0 && !(ok = load_do_and_next())) break;
+        if (j == 0 && !(ok = load_next())) break;
       }
       if (!ok) break;
       I = J;
@@ -1487,13 +1488,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         tc::mma2_commit_both(s_full);
         return true;
       };
-      auto issue_dp = [&](int gt) -> bool {  // dP(gt) = dO V^T over the pair
+      auto issue_dp = [&](int gt) -> bool {  // dP(gt) = dO V^T over the pair, dO in TMEM
         const int sv = gt % NSV;
         if (!wait1(v_full + sv, (gt / NSV) & 1)) return false;
         tc::tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          tc::mma2_ss(tmem + T_DP, dDO_ + kslice(k), dVx + ((sv * VST) >> 4) + kslice(k, PIECE), idesc_s, k > 0);
+          tc::mma2_ts(tmem + T_DP, tmem + T_DO + 8 * k, dVx + ((sv * VST) >> 4) + kslice(k, PIECE), idesc_s, k > 0);
         tc::mma2_commit_both(dp_full);
         tc::mma2_commit_both(v_empty + sv);
         return true;
@@ -1512,9 +1513,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         const int qs = nq % NSQ;
         if (!(ok = wait1(q_full + qs, (nq / NSQ) & 1))) break;
         if (!(ok = issue_s(gt, qs))) break;
-        if (n == 1) commit(q_empty + qs);  // Q is read by S only, dO by dP only
-        if (!(ok = wait1(do_full, nq & 1) && issue_dp(gt))) break;
-        if (n == 1) commit(do_empty);
+        if (n == 1) commit(q_empty + qs);  // Q is read by S only
+        // dO(k) into TMEM: the previous item's last dP has been read (dp_free
+        // below), so the region its A operand came from is free
+        if (!(ok = wait1(do_full, nq & 1))) break;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) tc::tmem_cp2_128x256b(tmem + T_DO + 8 * kk, dDO_ + kslice(kk));
+        commit(do_empty);  // the buffer takes the next item's dO once the copy is done
+        if (!(ok = issue_dp(gt))) break;
         for (int j = 0; ok && j < n; ++j) {
           const int g = gt + j;
           if (!(ok = wait1(s_free, g & 1))) break;
@@ -1523,10 +1530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
             if (j + 2 == n) commit(q_empty + qs);
           }
           if (!(ok = wait1(dp_free, g & 1))) break;
-          if (j + 1 < n) {
-            if (!(ok = issue_dp(g + 1))) break;
-            if (j + 2 == n) commit(do_empty);
-          }
+          if (j + 1 < n && !(ok = issue_dp(g + 1))) break;
         }
         if (!ok) break;
         gt += n;
@@ -1556,14 +1560,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         if (n == 0) continue;
         for (int j = 0; ok && j < n; ++j) {
           const int g = gt + j, sk = g % NSK;
-          if (!(ok = wait1(ds_ready + (g & 1), (g >> 1) & 1))) break;
+          if (!(ok = wait1(ds_ready, g & 1))) break;
           if (j == 0 && nq > 0 && !(ok = wait1(dq_free, (nq - 1) & 1))) break;
           tc::tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K over the pair, dS packed in T_DS[g&1]
-            tc::mma2_ts(tmem + T_DQ, tmem + T_DS + 64 * (g & 1) + 8 * kk,
-                        dKy + ((sk * KST) >> 4) + ((kk * 2048) >> 4), idesc_q, (j > 0 || kk > 0) ? 1u : 0u);
-          tc::mma2_commit_both(ds_free + (g & 1));
+          for (int kk = 0; kk < kB / 16; ++kk)  // dQ += dS K over the pair, dS packed in T_DS
+            tc::mma2_ts(tmem + T_DQ, tmem + T_DS + 8 * kk, dKy + ((sk * KST) >> 4) + ((kk * 2048) >> 4), idesc_q,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma2_commit_both(ds_free);
           tc::mma2_commit_both(k_empty + sk);  // S(g) was read before dS(g) existed
         }
         if (!ok) break;
@@ -1708,14 +1712,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
                      y0, y1);
             dw[e] = tc::pack_bf16(y0, y1);
           }
-          // dS(g) goes where dS(g-2) was: wait until dQ(g-2) has read it
-          if (g >= 2 && !wait_u(ds_free + (g & 1), ((g >> 1) - 1) & 1)) { ok = false; break; }
+          // dS(g) goes where dS(g-1) was: wait until dQ(g-1) has read it
+          if (g >= 1 && !wait_u(ds_free, (g - 1) & 1)) { ok = false; break; }
           tc::tc_fence_after();
-          tc::tmem_st16(tmem + lane_base + T_DS + 64 * (g & 1) + 16 * w, dw);
+          tc::tmem_st16(tmem + lane_base + T_DS + 16 * w, dw);
           tc::tmem_st_wait();
         }
         tc::tc_fence_before();
-        warp_arrive_lead(ds_ready + (g & 1));
+        warp_arrive_lead(ds_ready);
       }
       if (!ok || !prefetch(k + 1, nx)) { ok = false; break; }
       pend_row = dq_row;

@@ -440,6 +440,15 @@ __device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Shared memory -> TMEM copy over the pair: in each CTA, the 128 rows x 256
+// bits (16 bf16) that `sdesc` describes in its own shared memory (the same
+// offset in both) go to its own TMEM lanes 0-127, 8 columns from `taddr`.
+// An MMA issued after it by the same thread reads the copied values (the
+// copy and the MMA are executed in issue order).
+__device__ __forceinline__ void tmem_cp2_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive on `bar` (same offset) in both CTAs of the pair once the pair's
 // previously issued tcgen05 ops are done.
 __device__ __forceinline__ void mma2_commit_both(uint64_t* bar) {
