@@ -76,10 +76,13 @@ def test_lm_head_config1_full(tpa):
     _check_full(pk, seqs, hid, w, out)
 
 
-def test_lm_head_qwen_vocab_sampled(tpa):
-    # the logits workload's vocabulary on the GRPO-shaped trees, sampled positions
+@pytest.mark.parametrize("H", [1024, 4096])
+def test_lm_head_qwen_vocab_sampled(tpa, H):
+    # the logits workload's vocabulary on the GRPO-shaped trees: sampled
+    # positions of every tree, and every position of the two shortest
+    # sequences; H 4096 is the hidden size bench.py times
     cfg, seqs = workload(2)
-    V, H = 151936, 1024
+    V = 151936
     pk, tree, hid, w, out = _run(tpa, seqs, cfg.max_tokens_per_mb, V, H, 4)
     pl, pe, sl, se = out
     lg = LazyLogits(hid, w)
@@ -92,6 +95,14 @@ def test_lm_head_qwen_vocab_sampled(tpa):
         assert np.abs(pl[b, pos].numpy() - plp).max() <= LOGP_ABS, f"tree {b} pos_logp"
         assert np.abs(pe[b, pos].numpy() - pen).max() <= LOGP_ABS, f"tree {b} pos_entropy"
         assert (pl[b, t.n:] == 0).all() and (pe[b, t.n:] == 0).all()
+    shortest = sorted(range(len(seqs)), key=lambda s_: len(seqs[s_]))[:2]
+    lp, ent = sequence_logprobs_entropy(pk, seqs, lg, rb, shortest)
+    offs = np.concatenate([[0], np.cumsum([len(s_) for s_ in seqs])])
+    for u, s_ in enumerate(shortest):
+        got_lp = sl[offs[s_]:offs[s_ + 1]].numpy().astype(np.float64)
+        got_ent = se[offs[s_]:offs[s_ + 1]].numpy().astype(np.float64)
+        assert np.abs(got_lp - lp[u]).max() <= LOGP_ABS, f"seq {s_} logp"
+        assert np.abs(got_ent - ent[u]).max() <= LOGP_ABS, f"seq {s_} entropy"
     assert torch.isfinite(sl).all() and torch.isfinite(se).all()
 
 
