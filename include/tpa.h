@@ -253,6 +253,8 @@ typedef struct {
   uint32_t* sched;            /* [16] work counters of the attention kernels: zeroed by
                                  tpa_block_classify and left at zero by every attention call, so
                                  attention calls that use the same mask must not overlap on the GPU */
+  int32_t* line_count;        /* [B][2][n_blk] scratch of tpa_block_classify: non-empty tiles per
+                                 query block (row) and per key block (column) */
 } tpa_blockmask_view;
 
 /* Bytes of one device buffer holding a block mask for (n_trees, t_pad). */
@@ -263,7 +265,7 @@ uint64_t tpa_blockmask_bytes(int32_t n_trees, int32_t t_pad);
 int tpa_blockmask_make_view(void* base, int32_t n_trees, int32_t t_pad, tpa_blockmask_view* view);
 
 /* Classify every tile of every tree from the device subtree_end array and
- * build both CSR lists (two kernels on `stream`).  `tree` must be a view of
+ * build both CSR lists and the partial-tile bit rows (four kernels on `stream`).  `tree` must be a view of
  * the DEVICE blob; `mask` a view of a device buffer.  Integer only; results
  * are deterministic.  Errors: TPA_ERR_INVALID_ARG, TPA_ERR_CUDA. */
 int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask_view* mask, void* stream);

@@ -48,6 +48,7 @@ class BlockMaskView(C.Structure):
         ("n_trees", C.c_int32), ("n_blk", C.c_int32), ("cap", C.c_int32), ("pad_", C.c_int32),
         ("cls", C.c_void_p), ("q_ptr", C.c_void_p), ("q_idx", C.c_void_p),
         ("k_ptr", C.c_void_p), ("k_idx", C.c_void_p), ("qmask", C.c_void_p), ("sched", C.c_void_p),
+        ("line_count", C.c_void_p),
     ]
 
 

@@ -8,7 +8,8 @@
 // q0 = 128 qb, q1 = q0 + 127; the tile is EMPTY when cnt = 0, FULL when
 // cnt = 128 * 128 and PARTIAL otherwise.  Two CSR lists follow: per query
 // block its non-empty key blocks (forward), per key block its non-empty
-// query blocks (backward), each entry 2 * block + (FULL ? 1 : 0).  A third
+// query blocks (backward), each entry 2 * block + (FULL ? 1 : 0), built by a
+// count pass and a fill pass with one warp per line.  A third
 // kernel writes, for every PARTIAL entry of the per-query-block list, the
 // 128x128 visibility bits the forward applies (one 16-byte row per query).
 #include <cuda_runtime.h>
@@ -62,41 +63,68 @@ __global__ void __launch_bounds__(128) classify_kernel(const int32_t* __restrict
   }
 }
 
-// grid (B, 2), blockDim >= n_blk: direction 0 builds the per-query-block CSR,
-// direction 1 the per-key-block CSR.  Thread `line` owns one row / column.
-__global__ void __launch_bounds__(1024) csr_kernel(const uint8_t* __restrict__ cls, int32_t n_blk,
-                                                    int32_t cap, int32_t* __restrict__ q_ptr,
-                                                    int32_t* __restrict__ q_idx,
-                                                    int32_t* __restrict__ k_ptr,
-                                                    int32_t* __restrict__ k_idx,
-                                                    uint32_t* __restrict__ sched) {
-  __shared__ int scan_s[1024];
-  const int b = blockIdx.x, dir = blockIdx.y;
-  const int line = threadIdx.x;
-  const uint8_t* c = cls + int64_t(b) * n_blk * n_blk;
-  const int64_t s_line = dir == 0 ? n_blk : 1;   // stride between lines
-  const int64_t s_elem = dir == 0 ? 1 : n_blk;   // stride along a line
-  int cnt = 0;
-  if (line < n_blk)
-    for (int o = 0; o < n_blk; ++o) cnt += c[line * s_line + o * s_elem] != TPA_BLOCK_EMPTY;
-  scan_s[line] = cnt;
-  __syncthreads();
-  for (int off = 1; off < blockDim.x; off <<= 1) {   // inclusive Hillis-Steele scan
-    const int add = line >= off ? scan_s[line - off] : 0;
-    __syncthreads();
-    scan_s[line] += add;
-    __syncthreads();
-  }
-  if (b == 0 && dir == 0 && line < 16) sched[line] = 0;  // work counters of the attention kernels
+// The two CSR lists, one warp per line (direction 0: the row of a query
+// block, its non-empty key blocks; direction 1: the column of a key block,
+// its non-empty query blocks).  csr_count_kernel counts each line's
+// non-empty tiles; csr_fill_kernel takes a line's offset as the sum of the
+// counts before it, and writes its entries in ascending order, 32 at a time
+// with a ballot.  grid (ceil(n_blk / 8), B, 2), 256 threads: warp w of CTA x
+// handles line 8x + w.
+constexpr int kLinesPerCta = 8;
+
+__device__ __forceinline__ uint8_t tile_of(const uint8_t* c, int n_blk, int dir, int line, int o) {
+  return dir == 0 ? c[int64_t(line) * n_blk + o] : c[int64_t(o) * n_blk + line];
+}
+
+__global__ void __launch_bounds__(256) csr_count_kernel(const uint8_t* __restrict__ cls, int32_t n_blk,
+                                                         int32_t* __restrict__ line_count) {
+  const int b = blockIdx.y, dir = blockIdx.z;
+  const int lane = threadIdx.x & 31;
+  const int line = blockIdx.x * kLinesPerCta + (threadIdx.x >> 5);
   if (line >= n_blk) return;
+  const uint8_t* c = cls + int64_t(b) * n_blk * n_blk;
+  int cnt = 0;
+  for (int o = lane; o < n_blk; o += 32) cnt += tile_of(c, n_blk, dir, line, o) != TPA_BLOCK_EMPTY;
+  cnt = warp_sum(cnt);
+  if (lane == 0) line_count[(int64_t(b) * 2 + dir) * n_blk + line] = cnt;
+}
+
+__global__ void __launch_bounds__(256) csr_fill_kernel(const uint8_t* __restrict__ cls, int32_t n_blk,
+                                                        int32_t cap, const int32_t* __restrict__ line_count,
+                                                        int32_t* __restrict__ q_ptr, int32_t* __restrict__ q_idx,
+                                                        int32_t* __restrict__ k_ptr, int32_t* __restrict__ k_idx,
+                                                        uint32_t* __restrict__ sched) {
+  __shared__ int part_s[8];
+  const int b = blockIdx.y, dir = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int line0 = blockIdx.x * kLinesPerCta;
+  const int32_t* cnt = line_count + (int64_t(b) * 2 + dir) * n_blk;
+  if (b == 0 && dir == 0 && blockIdx.x == 0 && tid < 16) sched[tid] = 0;  // work counters of the attention kernels
+  // entries of the lines before this CTA's first one
+  int part = 0;
+  for (int i = tid; i < line0; i += blockDim.x) part += cnt[i];
+  part = warp_sum(part);
+  if (lane == 0) part_s[warp] = part;
+  __syncthreads();
+  int off = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) off += part_s[w];
+  const int line = line0 + warp;
+  if (line >= n_blk) return;
+  for (int w = 0; w < warp; ++w) off += cnt[line0 + w];
   int32_t* ptr = (dir == 0 ? q_ptr : k_ptr) + int64_t(b) * (n_blk + 1);
   int32_t* idx = (dir == 0 ? q_idx : k_idx) + int64_t(b) * cap;
-  int pos = scan_s[line] - cnt;
-  ptr[line] = pos;
-  if (line == n_blk - 1) ptr[n_blk] = scan_s[line];
-  for (int o = 0; o < n_blk; ++o) {
-    const uint8_t v = c[line * s_line + o * s_elem];
-    if (v != TPA_BLOCK_EMPTY) idx[pos++] = 2 * o + (v == TPA_BLOCK_FULL ? 1 : 0);
+  if (lane == 0) {
+    ptr[line] = off;
+    if (line == n_blk - 1) ptr[n_blk] = off + cnt[line];
+  }
+  const uint8_t* c = cls + int64_t(b) * n_blk * n_blk;
+  for (int o0 = 0; o0 < n_blk; o0 += 32) {
+    const int o = o0 + lane;
+    const uint8_t v = o < n_blk ? tile_of(c, n_blk, dir, line, o) : uint8_t(TPA_BLOCK_EMPTY);
+    const unsigned mask = __ballot_sync(0xffffffffu, v != TPA_BLOCK_EMPTY);
+    if (v != TPA_BLOCK_EMPTY) idx[off + __popc(mask & ((1u << lane) - 1u))] = 2 * o + (v == TPA_BLOCK_FULL ? 1 : 0);
+    off += __popc(mask);
   }
 }
 
@@ -140,7 +168,7 @@ extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask
                                   void* stream) {
   TPA_NVTX_RANGE("tpa_block_classify");
   if (!tree || !mask || !tree->subtree_end || !tree->n_tokens || !mask->cls || !mask->q_ptr ||
-      !mask->q_idx || !mask->k_ptr || !mask->k_idx || !mask->qmask || !mask->sched)
+      !mask->q_idx || !mask->k_ptr || !mask->k_idx || !mask->qmask || !mask->sched || !mask->line_count)
     return TPA_ERR_INVALID_ARG;
   if (tree->t_pad % kB || mask->n_blk != tree->t_pad / kB || mask->n_trees != tree->n_trees ||
       mask->n_blk > 1024 || tree->n_trees < 1)
@@ -150,9 +178,11 @@ extern "C" int tpa_block_classify(const tpa_tree_view* tree, const tpa_blockmask
   classify_kernel<<<dim3(n_blk, tree->n_trees), 128, 0, st>>>(tree->subtree_end, tree->n_tokens,
                                                               tree->t_pad, n_blk, mask->cls);
   TPA_CUDA_TRY(cudaGetLastError());
-  const int threads = n_blk <= 32 ? 32 : ((n_blk + 31) / 32) * 32;
-  csr_kernel<<<dim3(tree->n_trees, 2), threads, 0, st>>>(mask->cls, n_blk, mask->cap, mask->q_ptr,
-                                                         mask->q_idx, mask->k_ptr, mask->k_idx, mask->sched);
+  const dim3 lines((n_blk + kLinesPerCta - 1) / kLinesPerCta, tree->n_trees, 2);
+  csr_count_kernel<<<lines, 256, 0, st>>>(mask->cls, n_blk, mask->line_count);
+  TPA_CUDA_TRY(cudaGetLastError());
+  csr_fill_kernel<<<lines, 256, 0, st>>>(mask->cls, n_blk, mask->cap, mask->line_count, mask->q_ptr, mask->q_idx,
+                                         mask->k_ptr, mask->k_idx, mask->sched);
   TPA_CUDA_TRY(cudaGetLastError());
   qmask_kernel<<<dim3(n_blk, tree->n_trees), 128, 0, st>>>(tree->subtree_end, tree->n_tokens, tree->t_pad,
                                                            n_blk, mask->cap, mask->q_ptr, mask->q_idx,

@@ -15,9 +15,9 @@
 // block attention.
 //
 // The export is bound by HBM writes.  A CTA takes kRows query rows and a
-// chunk of keys; each thread keeps len_j of its keys in registers (E is read
-// once per CTA) and writes 16 bytes (U8: 16 keys) or 4 bytes (BITS: 32 keys)
-// per row, the writes of a warp to one row being contiguous.
+// chunk of keys; each thread keeps its keys' E in registers (read once per
+// CTA) and writes 16 bytes (U8: 16 keys) or 4 bytes (BITS: 32 keys) per row,
+// the writes of a warp to one row being contiguous.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -62,6 +62,14 @@ __global__ void __launch_bounds__(kThreadsDm) dense_mask_u8_kernel(const int32_t
   }
 }
 
+// Bit-packed form.  For query row i, the 32 keys j0 + c of a thread's word
+// are visible iff c <= i - j0 (a prefix of the word, one shift) and
+// E[j0 + c] >= i.  Over a CTA's rows [i0, i1] the second set only shrinks:
+// keys with E >= i1 stay in it, keys with E < i0 are never in it, and the
+// others leave it after row E.  Keys of one compressed node share their E,
+// so they leave in a few groups: the thread keeps the running set `cur` and
+// peels off the group with the next-smallest E when that row is passed (a
+// 32-key scan per group, once per CTA), instead of 32 compares per word.
 __global__ void __launch_bounds__(kThreadsDm) dense_mask_bits_kernel(const int32_t* __restrict__ subtree_end,
                                                                     int32_t t_pad, uint32_t* __restrict__ out,
                                                                     uint32_t invert) {
@@ -70,26 +78,52 @@ __global__ void __launch_bounds__(kThreadsDm) dense_mask_bits_kernel(const int32
   const int j0 = word * 32;
   if (j0 >= t_pad) return;
   const int32_t* e = subtree_end + int64_t(b) * t_pad + j0;
-  uint32_t len[32];
+  int ev[32];
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int4 v = reinterpret_cast<const int4*>(e)[q];
-    const int ev[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int j = j0 + 4 * q + c;
-      len[4 * q + c] = ev[c] >= j ? uint32_t(ev[c] - j + 1) : 0u;
-    }
+    ev[4 * q] = v.x, ev[4 * q + 1] = v.y, ev[4 * q + 2] = v.z, ev[4 * q + 3] = v.w;
   }
+  const int i0 = blockIdx.y * kRows, i1 = i0 + kRows - 1;
+  uint32_t always = 0u, dying = 0u;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {  // a pad key has E = -1 and is in neither set
+    if (ev[c] >= i1) always |= 1u << c;
+    else if (ev[c] >= i0) dying |= 1u << c;
+  }
+  uint32_t cur = always | dying;
+  // the group of dying keys with the smallest E (e_next = INT_MAX when none)
+  int e_next = 0x7fffffff;
+  uint32_t g_next = 0u;
+  auto next_group = [&]() {
+    e_next = 0x7fffffff;
+    g_next = 0u;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if ((dying >> c) & 1u) {
+        if (ev[c] < e_next) {
+          e_next = ev[c];
+          g_next = 1u << c;
+        } else if (ev[c] == e_next) {
+          g_next |= 1u << c;
+        }
+      }
+    }
+  };
+  next_group();
   const uint32_t inv = invert ? 0xffffffffu : 0u;
   const int words = t_pad / 32;
-  uint32_t* dst = out + (int64_t(b) * t_pad + int64_t(blockIdx.y) * kRows) * words + word;
+  uint32_t* dst = out + (int64_t(b) * t_pad + int64_t(i0)) * words + word;
   for (int r = 0; r < kRows; ++r) {
-    const int i = blockIdx.y * kRows + r;
-    uint32_t x = 0;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) x |= uint32_t(uint32_t(i - (j0 + c)) < len[c]) << c;
-    dst[int64_t(r) * words] = x ^ inv;
+    const int i = i0 + r;
+    const int d = i - j0;  // keys j0 .. j0 + d are at or before row i
+    const uint32_t pre = d < 0 ? 0u : (d >= 31 ? 0xffffffffu : (2u << d) - 1u);
+    dst[int64_t(r) * words] = (pre & cur) ^ inv;
+    while (e_next == i) {  // these keys are seen by no row after i
+      cur &= ~g_next;
+      dying &= ~g_next;
+      next_group();
+    }
   }
 }
 

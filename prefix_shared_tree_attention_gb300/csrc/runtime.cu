@@ -11,7 +11,7 @@ namespace {
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
 struct MaskLayout {
-  uint64_t cls, q_ptr, q_idx, k_ptr, k_idx, qmask, sched, total;
+  uint64_t cls, q_ptr, q_idx, k_ptr, k_idx, qmask, sched, line_count, total;
 };
 
 bool mask_layout(int32_t n_trees, int32_t t_pad, MaskLayout* L) {
@@ -26,6 +26,7 @@ bool mask_layout(int32_t n_trees, int32_t t_pad, MaskLayout* L) {
   L->k_idx = o; o = align256(o + 4 * B * cap);
   L->qmask = o; o = align256(o + 2048 * B * cap);
   L->sched = o; o = align256(o + 4 * 16);
+  L->line_count = o; o = align256(o + 4 * B * 2 * n);
   L->total = o;
   return true;
 }
@@ -92,6 +93,7 @@ int tpa_blockmask_make_view(void* base, int32_t n_trees, int32_t t_pad, tpa_bloc
   v->k_idx = reinterpret_cast<int32_t*>(b + L.k_idx);
   v->qmask = reinterpret_cast<uint32_t*>(b + L.qmask);
   v->sched = reinterpret_cast<uint32_t*>(b + L.sched);
+  v->line_count = reinterpret_cast<int32_t*>(b + L.line_count);
   return TPA_OK;
 }
 
