@@ -241,9 +241,10 @@ def test_attention_deterministic_forward(tpa):
 
 # ---------------------------------------------------------------- attention, full-size workloads (sampled)
 
-@pytest.mark.parametrize("cid,grad", [(2, "fp32"), (3, "fp32"), (5, "fp32"), (2, "bf16")])
+@pytest.mark.parametrize("cid,grad", [(2, "fp32"), (3, "fp32"), (5, "fp32"), (2, "bf16"), (3, "bf16"), (5, "bf16")])
 def test_attention_workload_sampled(tpa, cid, grad):
-    # (2, "bf16") is the configuration bench.py times: bf16 gradients, one item per key column
+    # bf16 gradients are what bench.py times; long key columns are then split
+    # into items that add into fp32 staging rows the last item converts
     cfg, seqs = workload(cid)
     T = cfg.max_tokens_per_mb
     pk = oracle.tree_pack(seqs, T)
