@@ -593,6 +593,61 @@ def run_gpu(args, rank, world, local):
                            (",seq log-probs/entropies; the logits H2D overlaps the attention and its "
                             "gradients' D2H on a second stream" if run_lp else "")}
 
+    # ------------------------------------------------ end to end with the fused LM head
+    # The same attention work, but the log-prob pass starts from hidden states
+    # (0.42 GB a step from pinned host memory) and the LM-head weight, resident
+    # on the device like any model parameter, instead of uploading 15.7 GB of
+    # logits: what a training step that owns its model would move.  Reported
+    # beside `e2e` (which keeps the logits workload); it also does the LM-head
+    # GEMM, which the metric does not count.
+    e2e_lmh = None
+    if (not args.no_e2e and args.only == "all" and run_lp and cid == 2 and args.lm_head_hidden > 0
+            and not args.no_extras):
+        Hh = args.lm_head_hidden
+        hid_h = make_hidden(4, rows, Hh, "cpu").pin_memory()
+        hid_d = torch.empty_like(hid_h, device=dev)
+        wlm = make_lm_weight(4, V, Hh, str(dev))
+        lws = torch.empty(tpa.lm_head_workspace_bytes(rows, V, B, T), dtype=torch.uint8, device=dev)
+        pin = lambda x: x.pin_memory()
+        qp, kp, vp, dop = pin(qh), pin(kh), pin(vh), pin(doh)
+        out_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv)]
+        seq_host = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+        blob_buf = torch.empty(int(info.blob_bytes), dtype=torch.uint8, device=dev)
+
+        def e2e_lmh_step():
+            tr = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
+            dt = tr.upload(dev, buffer=blob_buf)
+            for d_, h_ in zip((q, k, v, do, hid_d), (qp, kp, vp, dop, hid_h)):
+                d_.copy_(h_, non_blocking=True)
+            tpa.block_classify(dt, out=mask)
+            tpa.tree_attn_fwd(dt, mask, q, k, v, out=o, lse=lse)
+            tpa.tree_attn_bwd(dt, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv), grad_dtype=gdt)
+            for h_, d_ in zip(out_host, (o, dq, dk, dv)):
+                h_.copy_(d_, non_blocking=True)
+            tpa.lm_head_logprobs_entropy(dt, hid_d, wlm, out=lp_out, workspace=lws)
+            seq_host[0].copy_(lp_out[2], non_blocking=True)
+            seq_host[1].copy_(lp_out[3], non_blocking=True)
+            torch.cuda.synchronize(dev)
+            return tr
+
+        n_e = max(1, min(args.steps, args.e2e_steps))
+        for _ in range(max(1, min(args.warmup, 2))):
+            e2e_lmh_step()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n_e):
+            e2e_lmh_step()
+        sec = (time.perf_counter() - t0) / n_e
+        tpa.sync_status()
+        h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp, dop, hid_h)) + int(info.blob_bytes)
+        d2h = sum(x.numel() * x.element_size() for x in out_host) + 2 * 4 * N
+        e2e_lmh = {"value": job_flops / sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "steps": n_e, "ms_per_step": sec * 1e3, "hidden": Hh,
+                   "includes": "host pack + metadata upload + pinned H2D of q,k,v,dO and hidden states + device "
+                               "step with the fused LM-head log-prob pass (weight resident) + D2H of O,dQ,dK,dV, "
+                               "seq log-probs/entropies"}
+        del hid_h, hid_d, wlm, lws
+
     timed_s = total_ms / 1e3
     bf16_peak, bf16_kind = pick_bf16_peak(peaks, timed_s)
     rate = lambda work, ms: work / (ms / 1e3) if ms > 1e-6 else 0.0
@@ -697,7 +752,7 @@ def run_gpu(args, rank, world, local):
         "roofline": roof, "roofline_logprobs": lp_roof, "clocks": clocks,
         "attn_gcycles_at_median_clock": ((t_fwd + t_bwd) * clocks["sm_mhz"] / 1e6) if clocks["sm_mhz"] else None,
         "gpu_launches": n_launch_per_step * args.steps,
-        "e2e": e2e, "cpu_baseline": cpu, "balance": bal, "lm_head": lmh,
+        "e2e": e2e, "e2e_lm_head": e2e_lmh, "cpu_baseline": cpu, "balance": bal, "lm_head": lmh,
         "dense_mask": None if dmask is None else {
             **dmask, "frac_hbm_u8": dmask["u8"]["gbs"] / peaks["hbm_gbs"],
             "note": "write-only export of the [B, T, T] ancestor mask (u8) and its bit-packed form; "
