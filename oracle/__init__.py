@@ -35,7 +35,7 @@ first-fit (creation order) versus lightest-fit tree choice; see ``pack``.
 """
 from .pack import OraclePacking, OracleTree, tree_pack, PackError  # noqa: F401
 from .mask import dense_mask, block_classes, block_csr  # noqa: F401
-from .attention import attn_forward, attn_backward  # noqa: F401
+from .attention import attn_forward, attn_backward, attn_rows  # noqa: F401
 from .logprobs import sequence_logprobs_entropy, position_logprobs_entropy  # noqa: F401
 from .balance import ffd_allocate, kk_allocate, packing_metrics, BalanceError  # noqa: F401
 from .extract import extract_sequences  # noqa: F401

@@ -21,7 +21,9 @@ and for an upstream gradient dO the exact gradient of <dO, O>:
     dQ_i = scale sum_j dS_ij k_j,   dK_j += scale dS_ij q_i
 
 (dK, dV summed over the query heads that share a key/value head). Padding
-rows give O = 0, LSE = 0 and zero gradients.
+rows give O = 0, LSE = 0 and zero gradients.  ``attn_rows`` computes the same
+quantities one query row at a time, for trees too large for the node-level
+functions (a 131072-token chain); it is pinned against them on small trees.
 
 Computation is organised node by node: the queries of one compressed node
 share their root path, so A(i) is a prefix of that path (all ancestor nodes'
@@ -134,3 +136,60 @@ def attn_backward(tree: OracleTree, q: torch.Tensor, k: torch.Tensor, v: torch.T
     dK = dKh.view(T, Hkv, G, d).sum(2)
     dV = dVh.view(T, Hkv, G, d).sum(2)
     return dQ, dK, dV
+
+
+def _ancestors_of(tree: OracleTree, i: int) -> np.ndarray:
+    """Positions query i sees, in ascending order: the tokens of every
+    ancestor node of node(i), then node(i)'s own tokens up to i."""
+    nid = int(tree.node_id[i])
+    path = _root_path(tree, nid)
+    return path[path <= i] if path.size and path[-1] > i else path
+
+
+def attn_rows(tree: OracleTree, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rows,
+              dO: torch.Tensor | None = None, scale: float | None = None):
+    """fp64 attention of selected query positions, one row at a time (for
+    trees too large for the node-level functions above).
+
+    Returns O ``[len(rows), Hq, d]`` and LSE ``[Hq, len(rows)]``; with ``dO``
+    also dQ of those rows ``[len(rows), Hq, d]`` and the contributions of
+    those query rows to dK and dV, summed per key/value head, as dicts
+    position -> ``[Hkv, d]`` over the keys they see.  When ``rows`` holds every
+    query that sees a key, that key's dK/dV entries are complete."""
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    rows = [int(r) for r in rows]
+    O = torch.zeros((len(rows), Hq, d), dtype=torch.float64)
+    LSE = torch.zeros((Hq, len(rows)), dtype=torch.float64)
+    dQ = torch.zeros((len(rows), Hq, d), dtype=torch.float64)
+    dK: dict[int, torch.Tensor] = {}
+    dV: dict[int, torch.Tensor] = {}
+    for u, i in enumerate(rows):
+        if i >= tree.n:
+            continue
+        anc = torch.from_numpy(_ancestors_of(tree, i))
+        qi = _as64(q[i])                                          # [Hq, d]
+        kp = _as64(k[anc]).repeat_interleave(G, dim=1)            # [P, Hq, d]
+        vp = _as64(v[anc]).repeat_interleave(G, dim=1)
+        S = torch.einsum("hd,phd->hp", qi, kp) * scale
+        lse = torch.logsumexp(S, dim=-1)
+        P = torch.exp(S - lse[:, None])                           # [Hq, P]
+        O[u] = torch.einsum("hp,phd->hd", P, vp)
+        LSE[:, u] = lse
+        if dO is None:
+            continue
+        doi = _as64(dO[i])
+        Di = (doi * O[u]).sum(-1)                                  # [Hq]
+        dP = torch.einsum("hd,phd->hp", doi, vp)
+        dS = P * (dP - Di[:, None])
+        dQ[u] = scale * torch.einsum("hp,phd->hd", dS, kp)
+        dk = (scale * torch.einsum("hp,hd->phd", dS, qi)).view(-1, Hkv, G, d).sum(2)
+        dv = torch.einsum("hp,hd->phd", P, doi).view(-1, Hkv, G, d).sum(2)
+        for t, j in enumerate(anc.tolist()):
+            dK[j] = dK.get(j, 0) + dk[t]
+            dV[j] = dV.get(j, 0) + dv[t]
+    if dO is None:
+        return O, LSE
+    return O, LSE, dQ, dK, dV

@@ -276,3 +276,23 @@ def test_logprobs_masked_entries_vs_scipy_entr(seed):
         sub = logits[t, keep]
         col = int(keep[:seqs[0][t + 1]].sum())            # label's column among the kept ones
         assert lp[0][t] == pytest.approx(float(torch.log_softmax(sub, -1)[col]), abs=1e-12)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d", [(21, 4, 2, 16), (22, 2, 2, 8), (23, 6, 3, 8)])
+def test_row_oracle_equals_node_oracle(seed, hq, hkv, d):
+    # attn_rows (one query row at a time) against the node-level forward and
+    # backward: O, LSE and dQ of every row, and dK/dV once every row is given
+    seqs, pk, q, k, v, dO = _random_case(seed, hq, hkv, d, n=8)
+    t = pk.trees[0]
+    O, L = oracle.attn_forward(t, q[0], k[0], v[0], t_pad=128)
+    dQ, dK, dV = oracle.attn_backward(t, q[0], k[0], v[0], dO[0], t_pad=128)
+    rows = list(range(t.n))
+    Or, Lr, dQr, dKr, dVr = oracle.attn_rows(t, q[0], k[0], v[0], rows, dO=dO[0])
+    assert torch.allclose(Or, O[:t.n], atol=1e-12) and torch.allclose(Lr, L[:, :t.n], atol=1e-12)
+    assert torch.allclose(dQr, dQ[:t.n], atol=1e-12)
+    for j in rows:
+        assert torch.allclose(dKr[j], dK[j], atol=1e-12) and torch.allclose(dVr[j], dV[j], atol=1e-12)
+    # a subset of rows gives those rows' values unchanged
+    sub = rows[::5]
+    Os, Ls = oracle.attn_rows(t, q[0], k[0], v[0], sub)
+    assert torch.allclose(Os, O[sub], atol=1e-12)
