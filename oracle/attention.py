@@ -153,43 +153,42 @@ def attn_rows(tree: OracleTree, q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
 
     Returns O ``[len(rows), Hq, d]`` and LSE ``[Hq, len(rows)]``; with ``dO``
     also dQ of those rows ``[len(rows), Hq, d]`` and the contributions of
-    those query rows to dK and dV, summed per key/value head, as dicts
-    position -> ``[Hkv, d]`` over the keys they see.  When ``rows`` holds every
-    query that sees a key, that key's dK/dV entries are complete."""
+    those query rows to dK and dV ``[T, Hkv, d]`` (summed over the query heads
+    of each key/value head).  When ``rows`` holds every query that sees a
+    key, that key's dK/dV rows are complete."""
+    T = q.shape[0]
     Hq, d = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
     G = Hq // Hkv
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     rows = [int(r) for r in rows]
+    k64, v64 = _as64(k), _as64(v)
     O = torch.zeros((len(rows), Hq, d), dtype=torch.float64)
     LSE = torch.zeros((Hq, len(rows)), dtype=torch.float64)
     dQ = torch.zeros((len(rows), Hq, d), dtype=torch.float64)
-    dK: dict[int, torch.Tensor] = {}
-    dV: dict[int, torch.Tensor] = {}
+    dK = torch.zeros((T, Hkv, d), dtype=torch.float64)
+    dV = torch.zeros((T, Hkv, d), dtype=torch.float64)
     for u, i in enumerate(rows):
         if i >= tree.n:
             continue
         anc = torch.from_numpy(_ancestors_of(tree, i))
-        qi = _as64(q[i])                                          # [Hq, d]
-        kp = _as64(k[anc]).repeat_interleave(G, dim=1)            # [P, Hq, d]
-        vp = _as64(v[anc]).repeat_interleave(G, dim=1)
-        S = torch.einsum("hd,phd->hp", qi, kp) * scale
+        qi = _as64(q[i]).view(Hkv, G, d)                          # query heads of each kv head
+        kp, vp = k64[anc], v64[anc]                               # [P, Hkv, d]
+        S = torch.einsum("hgd,phd->hgp", qi, kp) * scale
         lse = torch.logsumexp(S, dim=-1)
-        P = torch.exp(S - lse[:, None])                           # [Hq, P]
-        O[u] = torch.einsum("hp,phd->hd", P, vp)
-        LSE[:, u] = lse
+        P = torch.exp(S - lse[..., None])                         # [Hkv, G, P]
+        Oi = torch.einsum("hgp,phd->hgd", P, vp)
+        O[u] = Oi.reshape(Hq, d)
+        LSE[:, u] = lse.reshape(Hq)
         if dO is None:
             continue
-        doi = _as64(dO[i])
-        Di = (doi * O[u]).sum(-1)                                  # [Hq]
-        dP = torch.einsum("hd,phd->hp", doi, vp)
-        dS = P * (dP - Di[:, None])
-        dQ[u] = scale * torch.einsum("hp,phd->hd", dS, kp)
-        dk = (scale * torch.einsum("hp,hd->phd", dS, qi)).view(-1, Hkv, G, d).sum(2)
-        dv = torch.einsum("hp,hd->phd", P, doi).view(-1, Hkv, G, d).sum(2)
-        for t, j in enumerate(anc.tolist()):
-            dK[j] = dK.get(j, 0) + dk[t]
-            dV[j] = dV.get(j, 0) + dv[t]
+        doi = _as64(dO[i]).view(Hkv, G, d)
+        Di = (doi * Oi).sum(-1)                                    # [Hkv, G]
+        dP = torch.einsum("hgd,phd->hgp", doi, vp)
+        dS = P * (dP - Di[..., None])
+        dQ[u] = (scale * torch.einsum("hgp,phd->hgd", dS, kp)).reshape(Hq, d)
+        dK.index_add_(0, anc, scale * torch.einsum("hgp,hgd->phd", dS, qi))
+        dV.index_add_(0, anc, torch.einsum("hgp,hgd->phd", P, doi))
     if dO is None:
         return O, LSE
     return O, LSE, dQ, dK, dV
