@@ -69,6 +69,58 @@ def check_guards(buf: torch.Tensor, what: str) -> None:
     assert torch.all(raw[:GUARD] == pat) and torch.all(raw[-GUARD:] == pat), f"{what}: write outside the buffer"
 
 
+def bf16_operand_bounds(tree, q, k, v, dO, t_pad: int):
+    """Per-element bounds on the gradient error that the backward's bf16
+    roundings alone cause, as FlashAttention-style kernels have them: the
+    tensor cores take P (for dV) and dS (for dQ and dK) as bf16 operands, and
+    D = rowsum(dO * O) is formed from the bf16 O the forward returned.
+    Rounding to bf16 changes a value by at most 2^-8 of it; with u = 2^-7
+    (twice that, for margin):
+        e_D_i  = u sum_d |dO_id| |O_id|,   e_dS_ij = u |dS_ij| + P_ij e_D_i
+        dQ_i: scale sum_j e_dS_ij |k_j|,  dK_j: scale sum_i e_dS_ij |q_i|,
+        dV_j: u sum_i P_ij |dO_i|,
+    from the fp64 reference's own P, dS and O.  Returns (bq [T,Hq,d], bk, bv [T,Hkv,d])."""
+    from oracle.attention import _root_path
+    Hq, d = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    sc = 1.0 / math.sqrt(d)
+    u = 2.0 ** -7
+    q64, k64, v64, do64 = (x.detach().to("cpu", torch.float64) for x in (q, k, v, dO))
+    bq = torch.zeros((t_pad, Hq, d), dtype=torch.float64)
+    bkh = torch.zeros((t_pad, Hq, d), dtype=torch.float64)
+    bvh = torch.zeros((t_pad, Hq, d), dtype=torch.float64)
+    for nid in range(len(tree.node_start)):
+        path = torch.from_numpy(_root_path(tree, nid))
+        s0, s1 = int(tree.node_start[nid]), int(tree.node_end[nid])
+        base = path.numel() - (s1 - s0 + 1)
+        kp, vp = k64[path].repeat_interleave(G, 1), v64[path].repeat_interleave(G, 1)
+        qi, doi = q64[s0:s1 + 1], do64[s0:s1 + 1]
+        S = torch.einsum("mhd,phd->hmp", qi, kp) * sc
+        rows = torch.arange(s1 - s0 + 1) + base
+        S = S.masked_fill(~(torch.arange(path.numel())[None, :] <= rows[:, None])[None], float("-inf"))
+        P = torch.softmax(S, -1)
+        Oi = torch.einsum("hmp,phd->mhd", P, vp)
+        Di = (doi * Oi).sum(-1).transpose(0, 1)                           # [Hq, m]
+        eD = u * (doi.abs() * Oi.abs()).sum(-1).transpose(0, 1)            # [Hq, m]
+        dS = P * (torch.einsum("mhd,phd->hmp", doi, vp) - Di[..., None])
+        edS = u * dS.abs() + P * eD[..., None]
+        bq[s0:s1 + 1] = sc * torch.einsum("hmp,phd->mhd", edS, kp.abs())
+        bkh.index_add_(0, path, sc * torch.einsum("hmp,mhd->phd", edS, qi.abs()))
+        bvh.index_add_(0, path, u * torch.einsum("hmp,mhd->phd", P, doi.abs()))
+    return bq, bkh.view(t_pad, Hkv, G, d).sum(2), bvh.view(t_pad, Hkv, G, d).sum(2)
+
+
+def assert_grad_close_with_operand_rounding(got, ref, bound, what):
+    """max-abs 2e-2 plus the bf16-rounding bound, element by element; rel-L2 5e-3."""
+    g = got.detach().to("cpu", torch.float64)
+    r = ref.detach().to("cpu", torch.float64)
+    assert torch.isfinite(g).all(), f"{what}: non-finite values"
+    excess = ((g - r).abs() - (ATTN_MAX_ABS + bound)).max().item()
+    rel = (g - r).norm().item() / max(r.norm().item(), 1e-30)
+    assert excess <= 0 and rel <= ATTN_REL_L2, f"{what}: excess {excess:.3e}, rel-L2 {rel:.3e}"
+
+
 def pack_and_upload(tpa, seqs, mb, device="cuda"):
     tree = tpa.tree_pack(seqs, mb)
     dtree = tree.upload(device)

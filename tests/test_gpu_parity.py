@@ -13,8 +13,9 @@ import torch
 import oracle
 from oracle.mask import _mask_rows, block_classes, block_csr
 from synth import CONFIGS, make_logits, random_small_sequences
-from _pipeline import (LOGP_ABS, assert_attn_close, assert_attn_close_bf16_out, check_guards, guarded, leaf_nodes,
-                       node_rows, pack_and_upload, random_inputs, workload, workload_tensors)
+from _pipeline import (LOGP_ABS, assert_attn_close, assert_attn_close_bf16_out,
+                       assert_grad_close_with_operand_rounding, bf16_half_ulp, bf16_operand_bounds, check_guards,
+                       guarded, leaf_nodes, node_rows, pack_and_upload, random_inputs, workload, workload_tensors)
 
 pytestmark = pytest.mark.gpu
 
@@ -208,6 +209,50 @@ def test_attention_single_chain_minimal(tpa):
 def test_attention_duplicates_and_singletons(tpa):
     seqs = [[5, 6, 7, 8]] * 4 + [[9]] + [[5, 6]] + [list(range(100, 300))]
     _run_full_case(tpa, seqs, 256, 4, 2, 128, 8)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_attention_star(tpa, d):
+    # One root token with 1000 single-token children: nearly every tile is
+    # PARTIAL, and each child sees only the root and itself, so its attention
+    # is concentrated on two keys (P ~ 0.5), |dQ| reaches ~5 and the root's
+    # dK/dV sum 1000 such terms.  Rounding P and dS to bf16 for the tensor
+    # cores alone then moves dQ by up to ~0.018 and the root's dK/dV by up to
+    # ~0.12 / ~0.11 (a CPU emulation of those roundings, and of D formed from
+    # the bf16 O, shows it), beyond the 2e-2 any such backward could keep.
+    # Gradients are therefore held to 2e-2 plus twice the worst case of those
+    # roundings, computed from the fp64 reference's own P, dS and O
+    # (_pipeline.bf16_operand_bounds), and rel-L2 keeps 5e-3; O and LSE keep
+    # their usual bounds.
+    seqs = [[7, 100 + i] for i in range(1000)]
+    T, hq, hkv = 1024, 4, 2
+    pk = oracle.tree_pack(seqs, T)
+    t = pk.trees[0]
+    tree, dtree, mask = pack_and_upload(tpa, seqs, T)
+    (q, k, v, do), (qc, kc, vc, doc) = random_inputs(1, T, hq, hkv, d, 40 + d)
+    o, lse = tpa.tree_attn_fwd(dtree, mask, q, k, v)
+    grads = {gdt: tpa.tree_attn_bwd(dtree, mask, q, k, v, o, lse, do, grad_dtype=gdt)
+             for gdt in (torch.float32, torch.bfloat16)}
+    tpa.sync_status()
+    O, L = oracle.attn_forward(t, qc[0], kc[0], vc[0], t_pad=T)
+    assert_attn_close(o[0], O, "O")
+    assert_attn_close(lse[0], L, "LSE", max_abs=2e-3, rel_l2=1e-4)
+    ref = oracle.attn_backward(t, qc[0], kc[0], vc[0], doc[0], t_pad=T)
+    bounds = bf16_operand_bounds(t, qc[0], kc[0], vc[0], doc[0], T)
+    for gdt, (dq, dk, dv) in grads.items():
+        for name, g, r, bd in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref, bounds):
+            extra = bd if gdt == torch.float32 else bd + bf16_half_ulp(r)
+            assert_grad_close_with_operand_rounding(g[0], r, extra, f"{gdt} {name}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_attention_comb(tpa, d):
+    # each sequence branches off the previous one 7 tokens deeper: a deep
+    # nest of short nodes, every node a child of the one before it
+    rng = np.random.default_rng(41)
+    base = rng.integers(0, 1000, size=600).tolist()
+    seqs = [base[:7 * i] + [5000 + i] * 9 for i in range(1, 80)]
+    _run_full_case(tpa, seqs, 1536, 4, 1, d, 50 + d)
 
 
 def test_attention_config1_full(tpa):
