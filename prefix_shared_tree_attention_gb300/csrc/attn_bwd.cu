@@ -83,7 +83,7 @@ struct BwdParams {
   uint32_t* kv_cnt;     // bf16 gradients: finished items per (tree, kv head, key tile, compute warp)
   int32_t t_pad, n_blk, cap, hq, hkv;
   int32_t n_trees, kv_chunk, kv_nchunk, kv_items, dq_items;
-  int32_t wide;  // gradient outputs 32-byte aligned: fp32 rows stored 32 bytes at a time
+  int32_t wide;  // gradient outputs 32-byte aligned: rows stored 32 bytes (one sector) at a time
   float scale, scale_log2;
 };
 
@@ -110,9 +110,9 @@ __device__ __forceinline__ void st_v8(void* addr, const uint32_t (&v)[8]) {
 }
 
 // Writes 16 fp32 values of one row as fp32 or bf16 (with a scale), or adds
-// them into an fp32 row.  `wide`: the row is 32-byte aligned and fp32 rows
-// go out as two 32-byte stores (one full sector each) instead of four
-// 16-byte stores.
+// them into an fp32 row.  `wide`: the row is 32-byte aligned and goes out in
+// 32-byte stores (one full sector each: two for fp32, one for bf16) instead
+// of 16-byte ones.
 template <bool F32OUT>
 __device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16], float scale, bool add,
                                             bool wide = false) {
@@ -147,6 +147,10 @@ __device__ __forceinline__ void store_row16(uint8_t* dst, const uint32_t (&v)[16
 #pragma unroll
     for (int u = 0; u < 8; ++u)
       w[u] = tc::pack_bf16(__uint_as_float(v[2 * u]) * scale, __uint_as_float(v[2 * u + 1]) * scale);
+    if (wide) {  // one full 32-byte sector per store
+      st_v8(dst, w);
+      return;
+    }
     uint4* d4 = reinterpret_cast<uint4*>(dst);
     d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
     d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -686,8 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               kk[4 * e] = __float_as_uint(b.x), kk[4 * e + 1] = __float_as_uint(b.y);
               kk[4 * e + 2] = __float_as_uint(b.z), kk[4 * e + 3] = __float_as_uint(b.w);
             }
-            store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, false);
-            store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, 1.f, false);  // scaled when added
+            store_row16<F32OUT>(dv_row + c * 16 * ESZ, vv, 1.f, false, p.wide);
+            store_row16<F32OUT>(dk_row + c * 16 * ESZ, kk, 1.f, false, p.wide);  // scaled when added
           }
         }
       }
