@@ -4,16 +4,23 @@
 // tile by tile on tcgen05 tensor cores and consumed in place — online
 // softmax statistics and the labels of the row — so they never reach HBM.
 //
-// Kernel 1 (lmh_kernel), persistent, one CTA per SM.  A work item is a
-// (128-row tile, chunk of kVt 256-wide vocab tiles) pair; items run in row
-// groups so the hidden rows of a group stay in L2 while its vocab chunks
-// stream past.  Roles:
+// Kernel 1 (lmh_kernel), persistent, on CTA pairs: the two CTAs of a
+// cluster (the two SMs of a TPC) take a work item, a (256-row tile, chunk of
+// kVt 256-wide vocab tiles) pair, CTA c holding rows [128c, 128c+128) of the
+// tile; every MMA runs once over the pair with M = 256 (tcgen05
+// cta_group::2), each CTA loading its own 128 hidden rows and half of the
+// 256 weight rows of the vocab tile, so a weight tile crosses L2 once per 256
+// rows (a third fewer bytes per FLOP than single-CTA 128-row tiles).  Items
+// run in row groups so the hidden rows of a group stay in L2 while its vocab
+// chunks stream past.  Roles (in each CTA):
 //   warp 16        TMA producer: per vocab tile and 64-wide slice of H, the
-//                  128x64 hidden tile and the 256x64 weight tile into a
-//                  4-stage ring (48 KB a stage).
-//   warp 17        MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16, into
-//                  one of two 256-column TMEM accumulators, so a tile's
-//                  epilogue overlaps the next tile's MMAs.
+//                  CTA's 128x64 hidden tile and 128x64 weight half-tile into
+//                  a 6-stage ring (32 KB a stage); the even CTA takes the
+//                  items and writes them into both CTAs' rings.
+//   warp 17        MMA issuer (even CTA): tcgen05.mma kind::f16, M=256 N=256
+//                  K=16, into one of two 256-column TMEM accumulators (each
+//                  CTA's own 128 rows), so a tile's epilogue overlaps the
+//                  next tile's MMAs.
 //   warps 0-15     epilogue: thread r of warpgroup w reads columns
 //                  [64w, 64w+64) of row r, keeps the row's running max m,
 //                  s = sum exp(x - m) and t = sum exp(x - m) x over its
@@ -41,11 +48,11 @@ namespace {
 
 __device__ unsigned int g_status_lmh = 0;
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kBM = 128, kBN = 256, kBK = 64;      // kBM: rows of one CTA (a pair takes 2 kBM)
 constexpr int kVt = 8;                               // vocab tiles per work item
-constexpr int kStages = 4;
-constexpr uint32_t kATile = kBM * kBK * 2;           // 16 KB
-constexpr uint32_t kBTile = kBN * kBK * 2;           // 32 KB
+constexpr int kStages = 6;
+constexpr uint32_t kATile = kBM * kBK * 2;           // 16 KB: this CTA's hidden rows
+constexpr uint32_t kBTile = kBN / 2 * kBK * 2;       // 16 KB: this CTA's half of the weight tile
 constexpr uint32_t kStage = kATile + kBTile;
 constexpr int kThreads = 576;                        // 16 epilogue warps + TMA + MMA
 constexpr int kWTma = 16, kWMma = 17;
@@ -54,7 +61,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kOffMerge = kStages * kStage;     // [2 item parities][3 warpgroups][128 rows] (m, s, t, -)
 constexpr uint32_t kOffBar = kOffMerge + 2 * 3 * kBM * 16;
 // full[kStages], empty[kStages], acc_full[2], acc_free[2], item_full[2], item_empty[2], drain,
-// merge_full[2], merge_free[2]
+// merge_full[2], merge_free[2] (full, acc_free and item_empty are used on the even CTA)
 constexpr int kNBar = 2 * kStages + 13;
 constexpr uint32_t kOffMisc = kOffBar + kNBar * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 32;       // base checked 1024-byte aligned
@@ -86,6 +93,13 @@ __device__ __forceinline__ LmhItem decode(const LmhParams& p, int it) {
   return LmhItem{base + rem % rg, rem / rg};
 }
 
+// one arrival per warp on the even CTA's copy of `bar`
+__device__ __forceinline__ void warp_arrive_lead(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) tc::mbar_arrive_remote(tc::peer_addr(bar, 0));
+  __syncwarp();
+}
+
 // Tree and position of compact row r (tok_base is the exclusive prefix sum).
 __device__ __forceinline__ void row_to_pos(const LmhParams& p, int64_t r, int& b, int& pos) {
   int lo = 0, hi = p.n_trees - 1;
@@ -110,14 +124,16 @@ __device__ __forceinline__ void stats_merge(Stats& a, const Stats& b) {
   a.m = m;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lmh_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                const LmhParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  if (tc::smem_u32(smem) & 1023u) {  // uniform over the CTA: every thread leaves
+  if (tc::smem_u32(smem) & 1023u) {  // the same for every CTA of the launch: all leave
     if (threadIdx.x == 0) atomicOr(&g_status_lmh, 2u);
     return;
   }
+  const uint32_t crank = tc::cta_rank();
+  const bool lead = crank == 0;
   float4* sMerge = reinterpret_cast<float4*>(smem + kOffMerge);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* full = bar;
@@ -134,6 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* item_ring = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);  // [2]
   const int warp = threadIdx.x >> 5;
   const int n_k = p.hidden / kBK;
+  // item-slot consumers, on the even CTA: its MMA thread and 16 epilogue
+  // warps, the odd CTA's producer and 16 epilogue warps
+  constexpr int kCons = 1 + 16 + 1 + 16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -142,9 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(acc_full + s, 1);
-      tc::mbar_init(acc_free + s, 512);
+      tc::mbar_init(acc_free + s, 32);  // one arrival per epilogue warp of either CTA
       tc::mbar_init(item_full + s, 1);
-      tc::mbar_init(item_empty + s, 1 + 512);
+      tc::mbar_init(item_empty + s, kCons);
       tc::mbar_init(merge_full + s, 384);
       tc::mbar_init(merge_free + s, 128);
     }
@@ -152,13 +171,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
-  if (warp == kWMma) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == kWMma) tc::tmem_alloc2(tmem_slot, 512);
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto wait_u = [&](uint64_t* b_, uint32_t par) {
     return __all_sync(0xffffffffu, tc::mbar_wait(b_, par, abort_flag, &g_status_lmh));
+  };
+  auto wait_ring = [&](uint64_t* b_, uint32_t par) {  // item slots: written across the pair
+    return __all_sync(0xffffffffu, tc::mbar_wait_cluster(b_, par, abort_flag, &g_status_lmh));
   };
 
   if (warp == kWTma) {
@@ -174,38 +196,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q = 0;  // stage loads issued
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        if (!(ok = wait1(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
-        const uint32_t u = atomicAdd(p.ctr, 1u);
-        const int it = u < uint32_t(p.n_items) ? int(u) : -1;
-        item_ring[k & 1] = it;
-        tc::mbar_arrive(item_full + (k & 1));
+        int it;
+        if (lead) {  // take the pair's next item, into both CTAs' rings
+          if (!(ok = wait1(item_empty + (k & 1), ((k >> 1) & 1) ^ 1))) break;
+          const uint32_t u = atomicAdd(p.ctr, 1u);
+          it = u < uint32_t(p.n_items) ? int(u) : -1;
+          item_ring[k & 1] = it;
+          tc::st_cluster_u32(tc::peer_addr(const_cast<int*>(item_ring + (k & 1)), 1), uint32_t(it));
+          tc::mbar_arrive(item_full + (k & 1));
+          tc::mbar_arrive_release_cluster(tc::peer_addr(item_full + (k & 1), 1));  // after the ring store
+        } else {
+          if (!(ok = tc::mbar_wait_cluster(item_full + (k & 1), (k >> 1) & 1, abort_flag, &g_status_lmh))) break;
+          it = item_ring[k & 1];
+          tc::mbar_arrive_remote(tc::peer_addr(item_empty + (k & 1), 0));
+        }
         if (it < 0) break;
         const LmhItem I = decode(p, it);
         const int vt1 = min(p.n_vt, (I.vc + 1) * kVt);
+        const int rows0 = I.rt * 2 * kBM + kBM * int(crank);  // this CTA's hidden rows
         for (int vt = I.vc * kVt; ok && vt < vt1; ++vt) {
           for (int kc = 0; kc < n_k; ++kc, ++q) {
             const int s = q % kStages;
             if (!(ok = wait1(empty + s, ((q / kStages) & 1) ^ 1))) break;
             uint8_t* dst = smem + s * kStage;
-            tc::mbar_arrive_expect_tx(full + s, kStage);
-            tc::tma_load_3d(dst, &tm_h, full + s, kc * kBK, 0, I.rt * kBM);
-            tc::tma_load_3d(dst + kATile, &tm_w, full + s, kc * kBK, 0, vt * kBN);
+            if (lead) tc::mbar_arrive_expect_tx(full + s, 2 * kStage);  // both CTAs' tiles
+            const uint32_t lb = tc::peer_addr(full + s, 0);
+            tc::tma_load_3d_pair(dst, &tm_h, lb, kc * kBK, 0, rows0);
+            tc::tma_load_3d_pair(dst + kATile, &tm_w, lb, kc * kBK, 0, vt * kBN + kBN / 2 * int(crank));
           }
         }
       }
-      if (*abort_flag) {  // let the copies already issued land before the CTA exits
-        volatile int never = 0;
-        for (int j = (q > kStages ? q - kStages : 0); j < q; ++j)
-          tc::mbar_wait(full + (j % kStages), (j / kStages) & 1, &never, &g_status_lmh, 100000000ull);
+      if (*abort_flag) {  // copies into this CTA's shared memory complete on the even CTA's barriers:
+        const long long t0 = clock64();  // give any still in flight time to land before the CTA leaves
+        while (clock64() - t0 < 400000) {
+        }
       }
     }
     __syncwarp();
   } else if (warp == kWMma) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = tc::idesc_bf16(kBM, kBN, false, false);
+    constexpr uint32_t idesc = tc::idesc_bf16(2 * kBM, kBN, false, false);
     const uint64_t dA = tc::smem_desc(tc::smem_u32(smem), 16, 1024);
     const uint64_t dB = tc::smem_desc(tc::smem_u32(smem + kATile), 16, 1024);
-    if (tc::elect_one()) {
+    if (lead && tc::elect_one()) {
       auto wait1 = [&](uint64_t* b_, uint32_t par) { return tc::mbar_wait(b_, par, abort_flag, &g_status_lmh); };
       int q = 0, nt = 0;  // stages consumed, tiles accumulated
       bool ok = true;
@@ -226,16 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t so = (s * kStage) >> 4;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              tc::mma_ss(tmem + 256 * ab, dA + so + ((kk * 32) >> 4), dB + so + ((kk * 32) >> 4), idesc,
-                         (kc > 0 || kk > 0) ? 1u : 0u);
-            tc::mma_commit(empty + s);
-            if (kc + 1 == n_k) tc::mma_commit(acc_full + ab);
+              tc::mma2_ss(tmem + 256 * ab, dA + so + ((kk * 32) >> 4), dB + so + ((kk * 32) >> 4), idesc,
+                          (kc > 0 || kk > 0) ? 1u : 0u);
+            tc::mma2_commit_both(empty + s);
+            if (kc + 1 == n_k) tc::mma2_commit_both(acc_full + ab);
           }
         }
       }
       if (*abort_flag) {  // let issued MMAs finish before TMEM is released
         volatile int never = 0;
-        tc::mma_commit(drain);
+        tc::mma2_commit_both(drain);
         tc::mbar_wait(drain, 0, &never, &g_status_lmh, 100000000ull);
       }
     }
@@ -248,12 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nt = 0, ni = 0;  // tiles and items with work processed
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      if (!wait_u(item_full + (k & 1), (k >> 1) & 1)) break;
+      if (!wait_ring(item_full + (k & 1), (k >> 1) & 1)) break;
       const int it = item_ring[k & 1];
-      tc::mbar_arrive(item_empty + (k & 1));
+      warp_arrive_lead(item_empty + (k & 1));
       if (it < 0) break;
       const LmhItem I = decode(p, it);
-      const int64_t row = int64_t(I.rt) * kBM + r;
+      const int64_t row = int64_t(I.rt) * 2 * kBM + kBM * int(crank) + r;
       const bool real = row < p.rows;
       // children of this row: their tokens are its labels
       int b = 0, pos = 0, c0 = 0, c1 = 0, lmin = 0x7fffffff, lmax = -1;
@@ -287,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld_wait();
           if (h == 1) {
             tc::tc_fence_before();
-            tc::mbar_arrive(acc_free + ab);  // both halves are in registers
+            warp_arrive_lead(acc_free + ab);  // both halves are in registers
           }
           const int vb = v0 + 32 * h;
           float mx = -INFINITY;
@@ -351,9 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cluster_sync();  // the pair's MMAs into either CTA's TMEM are done before it is freed
   tc::tc_fence_after();
-  if (warp == kWMma) tc::tmem_dealloc(tmem, 512);
+  if (warp == kWMma) tc::tmem_dealloc2(tmem, 512);
 }
 
 // One thread per tree position (b, pos): merges its row's partials; writes its
@@ -442,11 +475,11 @@ extern "C" int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const voi
   p.t_pad = tree->t_pad;
   p.vocab = vocab;
   p.hidden = hidden_size;
-  p.n_rt = int((rows + kBM - 1) / kBM);
+  p.n_rt = int((rows + 2 * kBM - 1) / (2 * kBM));  // 256-row tiles of a CTA pair
   p.n_vt = (vocab + kBN - 1) / kBN;
   p.n_vc = (p.n_vt + kVt - 1) / kVt;
-  // rows of a group: their hidden tiles (128 x H bf16 each) take about 48 MB of L2
-  const int64_t per_tile = int64_t(kBM) * hidden_size * 2;
+  // rows of a group: their hidden tiles (256 x H bf16 each) take about 48 MB of L2
+  const int64_t per_tile = int64_t(2 * kBM) * hidden_size * 2;
   p.group = int(std::max<int64_t>(1, std::min<int64_t>(p.n_rt, (int64_t(48) << 20) / per_tile)));
   p.n_items = p.n_rt * p.n_vc;
   p.ctr = reinterpret_cast<uint32_t*>(ws);
@@ -454,12 +487,12 @@ extern "C" int tpa_lm_head_logprobs_entropy(const tpa_tree_view* tree, const voi
   p.pair_logit = reinterpret_cast<float*>(ws + 256 + al256(uint64_t(rows) * p.n_vc * 16));
   CUtensorMap tm_h, tm_w;
   if (!tmap::make_rows_heads_d(&tm_h, hidden, uint64_t(rows), 1, uint64_t(hidden_size), kBM) ||
-      !tmap::make_rows_heads_d(&tm_w, weight, uint64_t(vocab), 1, uint64_t(hidden_size), kBN))
+      !tmap::make_rows_heads_d(&tm_w, weight, uint64_t(vocab), 1, uint64_t(hidden_size), kBN / 2))
     return TPA_ERR_CUDA;
   TPA_CUDA_TRY(cudaMemsetAsync(ws, 0, 16, st));
   TPA_CUDA_TRY(cudaFuncSetAttribute(lmh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-  const int sms = num_sms_lmh();
-  lmh_kernel<<<p.n_items < sms ? p.n_items : sms, kThreads, kSmemBytes, st>>>(tm_h, tm_w, p);
+  const int pairs = std::max(1, num_sms_lmh() / 2);
+  lmh_kernel<<<2 * (p.n_items < pairs ? p.n_items : pairs), kThreads, kSmemBytes, st>>>(tm_h, tm_w, p);
   TPA_CUDA_TRY(cudaGetLastError());
   const int64_t n_pos = int64_t(tree->n_trees) * tree->t_pad;
   lmh_combine_kernel<<<int((n_pos + 255) / 256), 256, 0, st>>>(p, tree->parent, pos_logp, pos_entropy);
