@@ -119,6 +119,10 @@ CASES = [
     (4, 3, 128, 50, 256, 2, 1, 64),     # exact block multiple, little sharing
     (5, 14, 120, 3, 512, 8, 2, 128),    # several trees
     (6, 6, 120, 3, 384, 8, 1, 128),     # group of 8 query heads per kv head, odd block count
+    # an odd group of 3 query heads per kv head: the one-head forward and the
+    # single-CTA dQ kernel at d 128, and key columns stepping over three heads
+    (7, 8, 200, 3, 384, 6, 2, 128),
+    (8, 7, 220, 3, 384, 3, 1, 64),
 ]
 
 
