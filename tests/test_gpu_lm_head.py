@@ -70,6 +70,15 @@ def test_lm_head_small_full(tpa, V, H):
     _check_full(pk, seqs, hid, w, out)
 
 
+def test_lm_head_tiny_tree(tpa):
+    # fewer rows than one CTA's 128: the pair's second CTA has no real row and
+    # its hidden-row loads lie wholly past the end (zero fill)
+    seqs = random_small_sequences(np.random.default_rng(77), 4, 20, 30)
+    pk, tree, hid, w, out = _run(tpa, seqs, 128, 300, 64, 2)
+    assert tree.info.total_tree_tokens < 128
+    _check_full(pk, seqs, hid, w, out)
+
+
 def test_lm_head_config1_full(tpa):
     cfg, seqs = workload(1)
     pk, tree, hid, w, out = _run(tpa, seqs, cfg.max_tokens_per_mb, 1000, 512, 1)
