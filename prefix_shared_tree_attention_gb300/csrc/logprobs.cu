@@ -23,7 +23,7 @@ namespace {
 
 __device__ unsigned int g_status_logprobs = 0;
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -129,8 +129,18 @@ __global__ void __launch_bounds__(kRowThreads) row_kernel(
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   const int nvec = vocab >> 3;
 
+  // Eight 16-byte loads in flight per thread, then four, then one: with 256
+  // threads a row (eight CTAs an SM) this read 2.3 % faster than four loads
+  // with 512 threads, and more loads or more threads a row were slower.
   Acc a{-INFINITY, 0.f, 0.f};
   int i = threadIdx.x;
+  for (; i + 7 * kRowThreads < nvec; i += 8 * kRowThreads) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcs(xv + i + u * kRowThreads);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc_add8(a, v[u]);
+  }
   for (; i + 3 * kRowThreads < nvec; i += 4 * kRowThreads) {
     const uint4 v0 = __ldcs(xv + i);
     const uint4 v1 = __ldcs(xv + i + kRowThreads);
