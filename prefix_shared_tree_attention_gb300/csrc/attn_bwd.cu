@@ -1752,8 +1752,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
 // rows themselves (and those of the key tiles no query sees, which no item
 // visits), with bf16 gradients the staging rows and the per-warp item
 // counters; every other row is written whole by its single item.
+// Four CTAs an SM: 64 registers a thread instead of 80 (three CTAs), which
+// keeps a third more loads in flight (152 -> 142 us on the GRPO-shaped batch).
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+__global__ void __launch_bounds__(256, 4) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                      const __nv_bfloat16* __restrict__ dout,
                                                      const int32_t* __restrict__ n_tokens, int32_t t_pad,
                                                      int32_t hq, int64_t n_rows, float* __restrict__ dvec,
