@@ -78,7 +78,9 @@ class ChildTable {
   size_t used_ = 0;
 };
 
-// Uncompressed token trie; vertex 0 is the root.
+// Uncompressed token trie; vertex 0 is the root.  A vertex's first child is
+// found through `first`; only its later children (the branch points) go into
+// the hash table, so walking or extending a chain does no hashing.
 struct Trie {
   std::vector<int32_t> tok{-1}, par{-1}, first{-1}, last{-1}, next{-1}, nchild{0};
   ChildTable table;
@@ -86,21 +88,28 @@ struct Trie {
 
   int32_t n_tokens() const { return int32_t(tok.size()) - 1; }
 
-  int64_t shared_prefix(const int32_t* s, int64_t len) const {
+  int32_t child(int32_t v, int32_t t) const {
+    const int32_t c = first[v];
+    if (c < 0) return -1;
+    if (tok[c] == t) return c;
+    return nchild[v] > 1 ? table.find(v, t) : -1;
+  }
+
+  // Whether the first `need` tokens of s are a path from the root: the
+  // sequence then adds at most len - need new tokens.
+  bool shares_at_least(const int32_t* s, int64_t need) const {
     int32_t v = 0;
-    int64_t n = 0;
-    for (; n < len; ++n) {
-      const int32_t c = table.find(v, s[n]);
-      if (c < 0) break;
-      v = c;
+    for (int64_t n = 0; n < need; ++n) {
+      v = child(v, s[n]);
+      if (v < 0) return false;
     }
-    return n;
+    return true;
   }
 
   void insert(const int32_t* s, int64_t len, int32_t* vertex_out) {
     int32_t v = 0;
     for (int64_t t = 0; t < len; ++t) {
-      int32_t c = table.find(v, s[t]);
+      int32_t c = child(v, s[t]);
       if (c < 0) {
         c = int32_t(tok.size());
         tok.push_back(s[t]);
@@ -109,10 +118,14 @@ struct Trie {
         last.push_back(-1);
         next.push_back(-1);
         nchild.push_back(0);
-        if (last[v] < 0) first[v] = c; else next[last[v]] = c;
+        if (last[v] < 0) {
+          first[v] = c;
+        } else {
+          next[last[v]] = c;
+          table.insert(v, s[t], c);  // a second or later child
+        }
         last[v] = c;
         ++nchild[v];
-        table.insert(v, s[t], c);
       }
       vertex_out[t] = c;
       v = c;
@@ -191,9 +204,15 @@ int pack_impl(const int32_t* tokens, const int64_t* offs, int32_t n_seqs, int32_
   for (int32_t s : order) {
     const int32_t* seq = tokens + offs[s];
     const int64_t len = offs[s + 1] - offs[s];
+    // First fit: the first tree whose token count plus the sequence's new
+    // tokens (those past its shared prefix) stays within mb.  A tree with room
+    // for the whole sequence takes it without a walk; otherwise the walk stops
+    // once the prefix is long enough or the trie ends.
     size_t b = 0;
-    for (; b < tries.size(); ++b)
-      if (tries[b].n_tokens() + (len - tries[b].shared_prefix(seq, len)) <= mb) break;
+    for (; b < tries.size(); ++b) {
+      const int64_t room = int64_t(mb) - tries[b].n_tokens();
+      if (len <= room || tries[b].shares_at_least(seq, len - room)) break;
+    }
     if (b == tries.size()) tries.emplace_back();
     tries[b].insert(seq, len, seq_vertex.data() + offs[s]);
     tries[b].members.push_back(s);
