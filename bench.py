@@ -546,8 +546,8 @@ def run_gpu(args, rank, world, local):
         # stream while the attention inputs arrive, the attention runs and its
         # gradients go back (the other direction of the link).
         def e2e_step():
-            tr = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
-            dt = tr.upload(dev, buffer=blob_buf)
+            # The copies that need no tree start first; the host packs the
+            # sequences while they run.
             q.copy_(qp, non_blocking=True); k.copy_(kp, non_blocking=True)
             v.copy_(vp, non_blocking=True); do.copy_(dop, non_blocking=True)
             if run_lp:
@@ -555,6 +555,8 @@ def run_gpu(args, rank, world, local):
                 with torch.cuda.stream(side):
                     logits.copy_(lg_host, non_blocking=True)
                     lg_ready.record(side)
+            tr = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
+            dt = tr.upload(dev, buffer=blob_buf)
             tpa.block_classify(dt, out=mask)
             tpa.tree_attn_fwd(dt, mask, q, k, v, out=o, lse=lse)
             tpa.tree_attn_bwd(dt, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv), grad_dtype=gdt)
@@ -588,7 +590,8 @@ def run_gpu(args, rank, world, local):
         d2h = sum(x.numel() * x.element_size() for x in out_host) + (2 * 4 * N if run_lp else 0)
         e2e = {"value": job_flops / e2e_sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": e2e_sec * 1e3,
-               "includes": "host pack + metadata upload + pinned H2D of q,k,v,dO" + (",logits" if run_lp else "") +
+               "includes": "pinned H2D of q,k,v,dO" + (",logits" if run_lp else "") + " (started before the host pack)"
+                           " + host pack + metadata upload" +
                            " + device step + D2H of O,dQ,dK,dV" +
                            (",seq log-probs/entropies; the logits H2D overlaps the attention and its "
                             "gradients' D2H on a second stream" if run_lp else "")}
@@ -614,16 +617,22 @@ def run_gpu(args, rank, world, local):
         seq_host = [torch.empty(N, dtype=torch.float32, pin_memory=True) for _ in range(2)]
         blob_buf = torch.empty(int(info.blob_bytes), dtype=torch.uint8, device=dev)
 
+        d2h = torch.cuda.Stream(device=dev)
+
         def e2e_lmh_step():
-            tr = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
-            dt = tr.upload(dev, buffer=blob_buf)
+            # inputs that need no tree are copied while the host packs; the
+            # attention results go back on a second stream during the LM head
             for d_, h_ in zip((q, k, v, do, hid_d), (qp, kp, vp, dop, hid_h)):
                 d_.copy_(h_, non_blocking=True)
+            tr = tpa.tree_pack(tokens=toks, offsets=offs, max_tokens_per_mb=T)
+            dt = tr.upload(dev, buffer=blob_buf)
             tpa.block_classify(dt, out=mask)
             tpa.tree_attn_fwd(dt, mask, q, k, v, out=o, lse=lse)
             tpa.tree_attn_bwd(dt, mask, q, k, v, o, lse, do, workspace=ws, out=(dq, dk, dv), grad_dtype=gdt)
-            for h_, d_ in zip(out_host, (o, dq, dk, dv)):
-                h_.copy_(d_, non_blocking=True)
+            d2h.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(d2h):
+                for h_, d_ in zip(out_host, (o, dq, dk, dv)):
+                    h_.copy_(d_, non_blocking=True)
             tpa.lm_head_logprobs_entropy(dt, hid_d, wlm, out=lp_out, workspace=lws)
             seq_host[0].copy_(lp_out[2], non_blocking=True)
             seq_host[1].copy_(lp_out[3], non_blocking=True)
@@ -643,9 +652,9 @@ def run_gpu(args, rank, world, local):
         d2h = sum(x.numel() * x.element_size() for x in out_host) + 2 * 4 * N
         e2e_lmh = {"value": job_flops / sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h, "steps": n_e, "ms_per_step": sec * 1e3, "hidden": Hh,
-                   "includes": "host pack + metadata upload + pinned H2D of q,k,v,dO and hidden states + device "
-                               "step with the fused LM-head log-prob pass (weight resident) + D2H of O,dQ,dK,dV, "
-                               "seq log-probs/entropies"}
+                   "includes": "pinned H2D of q,k,v,dO and hidden states (overlapping the host pack) + metadata "
+                               "upload + device step with the fused LM-head log-prob pass (weight resident) + D2H of "
+                               "O,dQ,dK,dV (on a second stream, overlapping the LM head), seq log-probs/entropies"}
         del hid_h, hid_d, wlm, lws
 
     timed_s = total_ms / 1e3
