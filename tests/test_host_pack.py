@@ -102,6 +102,18 @@ def test_pack_bit_exact_workloads(tpa, cid):
     _compare(make_sequences(cid), CONFIGS[cid].max_tokens_per_mb, tpa)
 
 
+def test_pack_full_tree_takes_only_paths_it_holds(tpa):
+    # A tree filled to exactly T_pad still takes a sequence that is a path
+    # already in it (no new tokens) and refuses one that adds a single token;
+    # a short prefix of its first sequence goes back into it too.
+    A = list(range(1, 129))
+    seqs = [A, list(A), A[:127] + [999], A[:64], [5] * 64 + [6] * 64]
+    _compare(seqs, 128, tpa)
+    tree = tpa.tree_pack(seqs, 128)
+    assert tree.arrays()["seq_tree"].tolist() == [0, 0, 1, 0, 2]
+    assert tree.arrays()["n_tokens"].tolist() == [128, 128, 128]
+
+
 def test_pack_worked_example(tpa):
     tree = tpa.tree_pack([[0, 1, 2, 3], [0, 1, 4, 5], [0, 6, 7]], 128)
     assert tree.info.total_tree_tokens == 8 and tree.info.total_seq_tokens == 11
