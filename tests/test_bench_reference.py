@@ -59,3 +59,13 @@ def test_reference_arm_other_config():
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["config"]["workload"].startswith("Tiny") and line["value"] > 0
     assert "the whole workload" in line["cpu_baseline"]["sample"]
+
+
+def test_profiles_match_the_kernel_sources():
+    # The roofline's `traffic` comes from the ncu summaries under profiles/,
+    # each naming the source it was captured from and that file's sha256
+    # prefix; a kernel edited since its capture makes the figure null.
+    sys.path.insert(0, ROOT)
+    import bench
+    for entry in bench.PROFILES:
+        assert bench._profile_traffic(entry, 51809) is not None, entry
